@@ -1,0 +1,458 @@
+#!/usr/bin/env python
+"""Benchmark of the k-quant weight matmul on GB300.
+
+Headline (one JSON line on stdout): decode weight GB/s of the Q4_K x Q8_1
+matvec on W[4096, 11008] and W[11008, 4096] (x fp32 N(0,1), Q8_1 quantisation
+fused). A step is one decode sweep over 8 rotated weight copies of each shape
+(16 launches, 406 MB of weights: larger than the 129 MB L2, so no flush is
+needed). Extra keys report the prefill GEMMs (N = 64, 512, 2048; Q4_K and Q6_K)
+and the MoE grouped GEMM as TFLOP/s, each call timed cold (L2 flushed between
+calls).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU
+(replicas; the path is not sharded), timing is the max over ranks, and the
+value is the sum over ranks. ``--impl reference`` times the CPU oracle on
+bounded samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DECODE_SHAPES = [(4096, 11008), (11008, 4096)]
+DECODE_COPIES = 8
+Q4K_ROW = lambda K: (K // 256) * 144          # noqa: E731
+METRIC = "Q4_K matmul: decode weight GB/s, prefill TFLOP/s, % of GB300 roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------------------
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-sections", action="store_true", help="skip the prefill/MoE sections")
+    p.add_argument("--section-iters", type=int, default=10)
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class Dist:
+    def __init__(self, n_gpus):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch
+            import torch.distributed as dist
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if backend == "nccl":
+                torch.cuda.set_device(self.local)
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, v: float) -> float:
+        if not self.pg:
+            return v
+        import torch
+        t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 200 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.path = tempfile.mktemp(suffix=".csv")
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        smax = [num(r[2]) for r in rows if num(r[2]) is not None]
+        power = [num(r[3]) for r in rows if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        loaded = [s for s, p in zip(sm, power) if p is not None] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(power) if power else None}
+
+
+def traffic_for(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if the
+    kernel source is unchanged since the capture (else None)."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(kernel)
+    if not e:
+        return None
+    src = os.path.join(ROOT, e["source"])
+    with open(src, "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()[:16]
+    return e["dram_bytes_per_launch"] if h == e["source_sha256_16"] else None
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle timing (spawned, single-threaded, never after a CUDA fork)
+# ----------------------------------------------------------------------------
+def _oracle_decode_sample(rows: int, reps: int, min_seconds: float):
+    """Runs the oracle matvec on the first `rows` rows of each decode shape;
+    returns (weight bytes, seconds)."""
+    import numpy as np
+    from oracle import kq_oracle as ora
+    from quantized_weight_matmul_q4_gb300 import synthetic as syn
+    data = []
+    for (M, K) in DECODE_SHAPES:
+        rng = np.random.default_rng(M)
+        W = syn.q4_k_weights(rng, rows, K)
+        x = syn.activations(rng, K, 1)
+        data.append((W, x, K))
+    nbytes = 0
+    t0 = time.perf_counter()
+    done = 0
+    while done < reps or time.perf_counter() - t0 < min_seconds:
+        for W, x, K in data:
+            ora.matmul("q4_k", W, x, W.shape[0], K)
+            nbytes += W.nbytes
+        done += 1
+        if done >= 50:
+            break
+    return nbytes, time.perf_counter() - t0
+
+
+def oracle_decode_gbs(rows: int, reps: int, min_seconds: float):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    code = ("import json, bench; b, s = bench._oracle_decode_sample(%d, %d, %f); "
+            "print(json.dumps([b, s]))" % (rows, reps, min_seconds))
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError("oracle timing failed: " + r.stderr[-2000:])
+    b, s = json.loads(r.stdout.strip().splitlines()[-1])
+    return b / s / 1e9, s
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+def run_ours(args, dist):
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import quantized_weight_matmul_q4_gb300 as kq
+    from quantized_weight_matmul_q4_gb300 import synthetic as syn
+
+    dev = torch.device("cuda", dist.local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    pk, pk_kind = peaks()
+
+    # ---- decode inputs: 8 independent weight copies per shape ----------------
+    sets = []
+    for name in ("decode_q4k_4096x11008", "decode_q4k_11008x4096"):
+        wl = syn.make_workload(name, copies=DECODE_COPIES)
+        Ws = [torch.from_numpy(w).to(dev) for w in wl["W"]]
+        x = torch.from_numpy(wl["X"][0]).to(dev)
+        y = torch.empty(wl["M"], dtype=torch.float32, device=dev)
+        sets.append((wl["M"], wl["K"], Ws, x, y, wl["X"][0]))
+    w_bytes_step = sum(W.numel() for s in sets for W in s[2])
+    alg_bytes_launch = [M * Q4K_ROW(K) + 4 * K + 4 * M for (M, K) in DECODE_SHAPES]
+    launches_step = DECODE_COPIES * len(sets)
+
+    def step():
+        for c in range(DECODE_COPIES):
+            for (M, K, Ws, x, y, _) in sets:
+                kq.kq_matvec(kq.KQ_Q4_K, Ws[c], x, M, K, y=y)
+
+    clocks = ClockSampler(dist.local)
+    clocks.start()
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    ms_local = e0.elapsed_time(e1)
+    ms_total = dist.max(ms_local)
+    ms_step = ms_total / args.steps
+    code = kq.kq_get_device_error()
+    if code:
+        raise RuntimeError(f"device error {code} during the decode bench")
+
+    # ---- end to end: pinned host x in, y out, through the public API ---------
+    hx = [torch.from_numpy(s[5]).pin_memory() for s in sets]
+    hy = [torch.empty(s[0], dtype=torch.float32).pin_memory() for s in sets]
+
+    def step_e2e():
+        for i, s in enumerate(sets):
+            s[3].copy_(hx[i], non_blocking=True)
+        step()
+        for i, s in enumerate(sets):
+            hy[i].copy_(s[4], non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        step_e2e()
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step_e2e()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    ms_e2e = dist.max(e0.elapsed_time(e1)) / args.steps
+
+    # ---- sections: prefill GEMMs and MoE, each call timed with L2 flushed ----
+    sections = {}
+    if not args.no_sections:
+        sections = run_sections(args, kq, syn, torch, dev, stream, pk)
+    clk = clocks.stop()
+
+    avg_launch_s = ms_step / 1e3 / launches_step
+    achieved = statistics.mean(alg_bytes_launch) / avg_launch_s / 1e9
+    value = dist.world * w_bytes_step / (ms_step / 1e3) / 1e9
+    out = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": dist.world,
+        "steps": args.steps,
+        "warmup": max(3, args.warmup),
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "u8 weights (Q4_K), int8 activations (Q8_1), i32 dots, f32 accumulate",
+        "data": "synthetic (seeded; Q4_K fields per the workload distributions, x ~ N(0,1))",
+        "config": {
+            "workload": "decode matvec N=1, Q4_K W[4096,11008] and W[11008,4096], Q8_1 quant fused",
+            "step": "16 kq_matvec launches: 8 rotated weight copies x 2 shapes",
+            "l2": "inputs larger than L2 (8 weight copies per shape, 406 MB of weights)",
+            "parallelism": f"replicas x{dist.world}",
+        },
+        "roofline": {
+            "kernel": "matvec_kernel<Q4_K>",
+            "bound": "hbm",
+            "achieved": round(achieved, 1),
+            "peak": pk["hbm_gbs"],
+            "unit": "GB/s",
+            "frac": round(achieved / pk["hbm_gbs"], 4),
+            "peak_source": f"{pk_kind} (copy bandwidth)",
+            "traffic": traffic_for("matvec_kernel_q4k_decode"),
+            "algorithmic_bytes_per_launch": statistics.mean(alg_bytes_launch),
+        },
+        "e2e": {
+            "value": round(dist.world * w_bytes_step / (ms_e2e / 1e3) / 1e9, 2),
+            "unit": "GB/s",
+            "h2d_bytes_per_step": sum(4 * K for (_, K) in DECODE_SHAPES),
+            "d2h_bytes_per_step": sum(4 * M for (M, _) in DECODE_SHAPES),
+            "ms_per_step": round(ms_e2e, 5),
+        },
+        "gpu_launches": launches_step * args.steps,
+        "clocks": clk,
+        "sections": sections,
+    }
+    return out
+
+
+def _timed_calls(fn, iters, warm, flush, torch, stream):
+    """Mean device time (ms) of fn() over iters calls, L2 flushed before each."""
+    for _ in range(warm):
+        fn()
+    times = []
+    for _ in range(iters):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    return statistics.mean(times), min(times)
+
+
+def run_sections(args, kq, syn, torch, dev, stream, pk):
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # 256 MB > L2
+    res = {}
+    iters = max(3, args.section_iters)
+    gemm_names = ["prefill_q4k_4096x4096_n64", "prefill_q4k_4096x4096_n512",
+                  "prefill_q4k_14336x4096_n2048", "prefill_q6k_4096x14336_n2048"]
+    for name in gemm_names:
+        wl = syn.make_workload(name)
+        M, K, N = wl["M"], wl["K"], wl["N"]
+        W = torch.from_numpy(wl["W"][0]).to(dev)
+        X = torch.from_numpy(wl["X"]).to(dev)
+        Y = torch.empty((N, M), dtype=torch.float32, device=dev)
+        ws = torch.empty(kq.kq_workspace_bytes(kq.KQ_OP_GEMM, wl["wtype"], M, K, N), dtype=torch.uint8, device=dev)
+        fn = lambda: kq.kq_gemm(wl["wtype"], W, X, M, K, Y=Y, ws=ws)  # noqa: E731
+        ms, ms_min = _timed_calls(fn, iters, 2, flush, torch, stream)
+        flops = 2.0 * M * N * K
+        wbytes = W.numel() + X.numel() * 4 + Y.numel() * 4
+        tf = flops / (ms / 1e3) / 1e12
+        res[name] = {"ms": round(ms, 4), "ms_min": round(ms_min, 4), "tflops": round(tf, 1),
+                     "frac_bf16_peak": round(tf / pk["bf16_tflops"], 4),
+                     "alg_gbs": round(wbytes / (ms / 1e3) / 1e9, 1),
+                     "frac_hbm_peak": round(wbytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"], 4),
+                     "launches_per_call": None}
+        del W, X, Y, ws
+    wl = syn.make_workload("moe_q4k_128x768x2048_t1024_top8")
+    E, M, K, T, top_k = wl["n_experts"], wl["M"], wl["K"], wl["T"], wl["top_k"]
+    W = torch.from_numpy(wl["W"][0]).to(dev)
+    X = torch.from_numpy(wl["X"]).to(dev)
+    ids = torch.from_numpy(wl["ids"]).to(dev)
+    Y = torch.empty((T, top_k, M), dtype=torch.float32, device=dev)
+    ws = torch.empty(kq.kq_workspace_bytes(kq.KQ_OP_MOE, "q4_k", M, K, T, E, top_k), dtype=torch.uint8, device=dev)
+    fn = lambda: kq.kq_moe_grouped_gemm("q4_k", W, E, ids, X, M, K, Y=Y, ws=ws)  # noqa: E731
+    ms, ms_min = _timed_calls(fn, iters, 2, flush, torch, stream)
+    flops = 2.0 * M * K * T * top_k
+    nbytes = W.numel() + X.numel() * 4 + Y.numel() * 4 + ids.numel() * 4
+    tf = flops / (ms / 1e3) / 1e12
+    res["moe_q4k_128x768x2048_t1024_top8"] = {
+        "ms": round(ms, 4), "ms_min": round(ms_min, 4), "tflops": round(tf, 1),
+        "frac_bf16_peak": round(tf / pk["bf16_tflops"], 4),
+        "alg_gbs": round(nbytes / (ms / 1e3) / 1e9, 1),
+        "frac_hbm_peak": round(nbytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"], 4)}
+    if kq.kq_get_device_error():
+        raise RuntimeError("device error during the sections")
+    return res
+
+
+# ----------------------------------------------------------------------------
+def run_reference(args):
+    """The CPU oracle, as it stands, on bounded samples of the decode workload."""
+    cores = 1
+    rows = 256
+    vals = []
+    for _ in range(args.warmup):
+        oracle_decode_gbs(rows, 1, 0.0)
+    t_all = 0.0
+    for _ in range(args.steps):
+        gbs, s = oracle_decode_gbs(rows, 1, 0.0)
+        vals.append(gbs)
+        t_all += s
+    v = statistics.mean(vals)
+    sample = f"oracle matvec on the first {rows} rows of each decode shape per step (single thread)"
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(v, 4),
+        "unit": "GB/s",
+        "n_gpus": args.gpus,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(t_all / max(1, args.steps) * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64 oracle (fp32 Q8_1 quantisation)",
+        "data": "synthetic (seeded)",
+        "config": {"workload": "decode matvec N=1, Q4_K W[4096,11008] and W[11008,4096], Q8_1 quant fused",
+                   "parallelism": "cpu oracle"},
+        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args)), flush=True)
+        return
+    dist = Dist(args.gpus)
+    out = run_ours(args, dist)
+    if dist.rank == 0:
+        gbs, secs = oracle_decode_gbs(512, 2, 10.0)
+        out["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                               "sample": f"oracle matvec on the first 512 rows of each decode shape, "
+                                         f"repeated for {secs:.1f} s (single thread)"}
+        print(json.dumps(out), flush=True)
+    dist.close()
+
+
+if __name__ == "__main__":
+    main()

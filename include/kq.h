@@ -1,0 +1,160 @@
+/*
+ * kq.h — k-quant weight matmul on NVIDIA GB300 (sm_103a): C ABI of libkq.
+ *
+ *   Y[M, N] = dequant(W)[M, K] . X[K, N]
+ *
+ * W holds 4-bit Q4_K or 6-bit Q6_K super-blocks; X is fp32 and is quantised to
+ * Q8_1 (int8 codes with an fp16 scale per 32 values) inside every call.
+ *
+ * Sources (page title, section):
+ *  [MMVQ]  "06 · 8e/8e② — decode MMVQ: dp4a integer dot products + the llama.cpp
+ *          launch table": §2 Principle (Q4_K value d*sc*nib - dmin*m, the min-term
+ *          identity, the q8 activation quantiser), §3.2 Key code (Q4_K byte
+ *          offsets, quantize_pad40_block), §3.3 Pitfalls (Q6_K layout, d at 208).
+ *  [MMQv2] "ZINC MMQ v2 — Fused Q4_K×Q8_1 Tensor-Core GEMM (beat llama.cpp)": What
+ *          they do right (Q8_1 activations, fused dequant), Kernel architecture,
+ *          Persistent kernel + atomic work queue, MoE routing (fused gather).
+ *  [GAP]   "Prefill Gap Closure Plan — ZINC CUDA vs llama.cpp": T1 (fused dequant
+ *          tensor-core GEMM), T2 (grouped MoE expert GEMM: histogram, prefix sum,
+ *          scatter, per-expert GEMM).
+ *
+ * Conventions for every entry point
+ *  - Pointers are device pointers owned by the caller (cudaMalloc / a framework
+ *    allocator) unless stated otherwise. The library allocates no memory, keeps
+ *    no pointer after the call returns, and does not synchronise the stream
+ *    (except kq_get_device_error).
+ *  - Layouts (row-major everywhere):
+ *      W : M rows x (K/256) super-blocks; a Q4_K block is 144 bytes
+ *          [fp16 d][fp16 dmin][12 B packed 6-bit scales/mins][128 B nibbles],
+ *          a Q6_K block is 210 bytes [ql 128][qh 64][int8 scales 16][fp16 d].
+ *          For MoE the experts' matrices are concatenated, expert-major.
+ *      X : fp32, token-major: token n occupies X[n*K .. n*K+K-1].
+ *      Y : fp32, token-major: Y[n*M + m].
+ *      Xq: N x (K/32) Q8_1 blocks of 36 bytes [fp16 d][fp16 s][int8 q[32]].
+ *  - Alignment: W, X, Y, Xq and ws must be 16-byte aligned.
+ *  - Sizes: K must be a multiple of 256 (32 for kq_quantize_q8_1); M, N, T >= 1;
+ *    all sizes below 2^31.
+ *  - Work is queued on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *    A status other than KQ_OK means nothing was queued, except KQ_ERR_CUDA
+ *    after a failed launch.
+ *  - Results are deterministic: the same inputs give bit-identical outputs.
+ *  - Accuracy: Q8_1 codes and block sums are bit-exact against the IEEE fp32
+ *    definition. Y satisfies |Y - Y_ref| <= 1e-3 * Sum_k |w_k x_k| + 1e-5 per
+ *    element, Y_ref being the exact product of the dequantised operands. The
+ *    tensor-core paths (kq_gemm, kq_moe_grouped_gemm) round dequantised
+ *    weights and activations to fp16, so they need |w|, |x| < 65504.
+ */
+#ifndef KQ_H
+#define KQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define KQ_API __attribute__((visibility("default")))
+#else
+#define KQ_API
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* kq_stream_t;
+
+typedef enum kq_status {
+  KQ_OK = 0,
+  KQ_ERR_NULL = 1,      /* a required pointer is NULL */
+  KQ_ERR_SHAPE = 2,     /* a size is out of range or not a multiple of its block */
+  KQ_ERR_ALIGN = 3,     /* a pointer is not 16-byte aligned */
+  KQ_ERR_TYPE = 4,      /* unknown weight type */
+  KQ_ERR_WORKSPACE = 5, /* ws_bytes is smaller than kq_workspace_bytes() */
+  KQ_ERR_CUDA = 6,      /* a CUDA runtime call failed (no device, launch failure) */
+  KQ_ERR_DEVICE = 7     /* a kernel recorded an error; see kq_get_device_error */
+} kq_status;
+
+typedef enum kq_wtype { KQ_Q4_K = 1, KQ_Q6_K = 2 } kq_wtype;
+
+typedef enum kq_op { KQ_OP_MATVEC = 1, KQ_OP_GEMM = 2, KQ_OP_MOE = 3 } kq_op;
+
+/* Device error codes reported by kq_get_device_error. */
+#define KQ_DEVERR_NONE 0
+#define KQ_DEVERR_WAIT_TIMEOUT 1 /* a pipeline wait gave up (the kernel returned early) */
+#define KQ_DEVERR_EXPERT_ID 2    /* an expert id was outside [0, n_experts) */
+
+/*
+ * kq_quantize_q8_1 — fp32 activations to Q8_1 blocks ([MMVQ] §2 and §3.2
+ * quantize_pad40_block; the Q8_1 block sum of [MMQv2] "What they do right").
+ * For every 32 consecutive values x of a token:
+ *   d = max|x| / 127, q = clamp(rint(x * (d != 0 ? 1/d : 0)), -128, 127),
+ *   stored d_h = fp16(d), s_h = fp16(d_h * Sum q), all in IEEE fp32 with
+ *   round-half-even.
+ * X: fp32 [N][K]; Xq: N*(K/32)*36 bytes, written. K % 32 == 0.
+ */
+KQ_API kq_status kq_quantize_q8_1(const float* X, void* Xq, int64_t K, int64_t N, kq_stream_t stream);
+
+/*
+ * kq_matvec — decode matvec y = dequant(W) . x for one token ([MMVQ] §2, §3.2:
+ * integer dot products of the 4/6-bit codes with the Q8_1 codes of x, the
+ * min term from the Q8_1 block sum, warp-shuffle row reductions). x is
+ * quantised to Q8_1 inside the call.
+ * wtype: KQ_Q4_K or KQ_Q6_K. W: M rows of K/256 blocks; x: fp32 [K];
+ * y: fp32 [M], written. Needs no workspace. A Q6_K row whose byte length is not
+ * a multiple of 16 must have K <= 15360.
+ */
+KQ_API kq_status kq_matvec(int wtype, const void* W, const float* x, float* y, int64_t M, int64_t K,
+                    kq_stream_t stream);
+
+/*
+ * kq_gemm — prefill GEMM Y = dequant(W) . X for N tokens ([MMQv2] Kernel
+ * architecture; [GAP] T1). X is quantised to Q8_1 (as x_hat = fp16(d_h * q))
+ * into the workspace once per call; weight super-blocks are staged by TMA and
+ * unpacked to fp16 in shared memory; tcgen05 MMAs accumulate in tensor memory.
+ * W: M x K weights; X: fp32 [N][K]; Y: fp32 [N][M], written.
+ * ws: device workspace of at least kq_workspace_bytes(KQ_OP_GEMM, ...) bytes.
+ * Q6_K needs K % 2048 == 0 (rows whose byte length is a multiple of 16).
+ */
+KQ_API kq_status kq_gemm(int wtype, const void* W, const float* X, float* Y, int64_t M, int64_t K, int64_t N, void* ws,
+                  size_t ws_bytes, kq_stream_t stream);
+
+/*
+ * kq_moe_grouped_gemm — MoE expert matmul ([MMQv2] MoE routing; [GAP] T2).
+ * For every token t and slot j < top_k: Y[t][j][:] = dequant(W_e) . x_t with
+ * e = expert_ids[t*top_k + j]. The (token, slot) pairs are grouped by expert
+ * (histogram, prefix sum, scatter), the activations are gathered per expert,
+ * and each expert's weight tile is read once for all of its tokens.
+ * W_experts: n_experts * M rows of K/256 blocks (expert-major);
+ * expert_ids: int32 [T][top_k]; X: fp32 [T][K]; Y: fp32 [T][top_k][M], written.
+ * No router weighting and no sum over slots. An out-of-range expert id records
+ * KQ_DEVERR_EXPERT_ID and that slot's output row is written as zeros.
+ * ws: at least kq_workspace_bytes(KQ_OP_MOE, ...) bytes.
+ */
+KQ_API kq_status kq_moe_grouped_gemm(int wtype, const void* W_experts, int32_t n_experts, const int32_t* expert_ids,
+                              int32_t top_k, const float* X, float* Y, int64_t M, int64_t K, int64_t T, void* ws,
+                              size_t ws_bytes, kq_stream_t stream);
+
+/*
+ * kq_workspace_bytes — device workspace needed by an operation (0 for
+ * KQ_OP_MATVEC). N_or_T is N for KQ_OP_GEMM and T for KQ_OP_MOE; n_experts
+ * and top_k are read for KQ_OP_MOE only. The size depends on the SM count of
+ * the current device. Returns 0 for invalid arguments.
+ */
+KQ_API size_t kq_workspace_bytes(int op, int wtype, int64_t M, int64_t K, int64_t N_or_T, int32_t n_experts,
+                          int32_t top_k);
+
+/*
+ * kq_get_device_error — waits for `stream`, then returns in *code the first
+ * device error recorded on the current device since the previous call
+ * (KQ_DEVERR_*), and clears it. Returns KQ_ERR_DEVICE when *code != 0.
+ */
+KQ_API kq_status kq_get_device_error(int32_t* code, kq_stream_t stream);
+
+/* Name of a status code (static string). */
+KQ_API const char* kq_status_str(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KQ_H */

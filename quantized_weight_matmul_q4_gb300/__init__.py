@@ -1,0 +1,127 @@
+"""kq — k-quant (Q4_K / Q6_K) weight matmul for NVIDIA GB300.
+
+Thin Python binding over the C ABI of libkq (include/kq.h): every function
+here only checks and marshals its arguments (device pointers, sizes, the
+current CUDA stream) and calls the library of the same name. All arithmetic
+runs in the library's CUDA kernels; there is no CPU path. PyTorch provides
+device memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+
+from ._native import (KQ_DEVERR_EXPERT_ID, KQ_DEVERR_NONE, KQ_DEVERR_WAIT_TIMEOUT, KQ_OP_GEMM, KQ_OP_MATVEC,
+                      KQ_OP_MOE, KQ_Q4_K, KQ_Q6_K, KQError, check, lib)
+
+__all__ = [
+    "KQ_Q4_K", "KQ_Q6_K", "KQ_OP_MATVEC", "KQ_OP_GEMM", "KQ_OP_MOE", "KQError",
+    "KQ_DEVERR_NONE", "KQ_DEVERR_WAIT_TIMEOUT", "KQ_DEVERR_EXPERT_ID",
+    "kq_quantize_q8_1", "kq_matvec", "kq_gemm", "kq_moe_grouped_gemm", "kq_workspace_bytes",
+    "kq_get_device_error", "block_bytes", "row_bytes",
+]
+
+_BLOCK_BYTES = {KQ_Q4_K: 144, KQ_Q6_K: 210}
+
+
+def _wt(wtype) -> int:
+    if isinstance(wtype, str):
+        return {"q4_k": KQ_Q4_K, "q6_k": KQ_Q6_K}[wtype.lower()]
+    return int(wtype)
+
+
+def block_bytes(wtype) -> int:
+    return _BLOCK_BYTES[_wt(wtype)]
+
+
+def row_bytes(wtype, K: int) -> int:
+    return (K // 256) * block_bytes(wtype)
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dev(t, name: str, dtype=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor (libkq has no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must have dtype {dtype}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def kq_quantize_q8_1(X, Xq=None, stream=None):
+    """X: fp32 [N, K] -> Q8_1 bytes uint8 [N, K/32, 36]."""
+    torch = _torch()
+    N, K = X.shape
+    if Xq is None:
+        Xq = torch.empty((N, K // 32, 36), dtype=torch.uint8, device=X.device)
+    check(lib().kq_quantize_q8_1(_dev(X, "X", torch.float32), _dev(Xq, "Xq", torch.uint8), K, N,
+                                 _stream(stream)), "kq_quantize_q8_1")
+    return Xq
+
+
+def kq_matvec(wtype, W, x, M: int, K: int, y=None, stream=None):
+    """y[M] = dequant(W) . x; W uint8 [M, row_bytes], x fp32 [K]."""
+    torch = _torch()
+    if y is None:
+        y = torch.empty(M, dtype=torch.float32, device=x.device)
+    check(lib().kq_matvec(_wt(wtype), _dev(W, "W", torch.uint8), _dev(x, "x", torch.float32),
+                          _dev(y, "y", torch.float32), M, K, _stream(stream)), "kq_matvec")
+    return y
+
+
+def kq_workspace_bytes(op: int, wtype, M: int, K: int, N_or_T: int, n_experts: int = 0, top_k: int = 0) -> int:
+    return int(lib().kq_workspace_bytes(int(op), _wt(wtype), M, K, N_or_T, n_experts, top_k))
+
+
+def kq_gemm(wtype, W, X, M: int, K: int, Y=None, ws=None, stream=None):
+    """Y[N, M] = (dequant(W) . X^T)^T for X fp32 [N, K]."""
+    torch = _torch()
+    N = X.shape[0]
+    if Y is None:
+        Y = torch.empty((N, M), dtype=torch.float32, device=X.device)
+    if ws is None:
+        ws = torch.empty(max(1, kq_workspace_bytes(KQ_OP_GEMM, wtype, M, K, N)), dtype=torch.uint8,
+                         device=X.device)
+    check(lib().kq_gemm(_wt(wtype), _dev(W, "W", torch.uint8), _dev(X, "X", torch.float32),
+                        _dev(Y, "Y", torch.float32), M, K, N, _dev(ws, "ws", torch.uint8), ws.numel(),
+                        _stream(stream)), "kq_gemm")
+    return Y
+
+
+def kq_moe_grouped_gemm(wtype, W_experts, n_experts: int, expert_ids, X, M: int, K: int, Y=None, ws=None,
+                        stream=None):
+    """Y[T, top_k, M]: per (token, slot) product with the routed expert's weights."""
+    torch = _torch()
+    T, top_k = expert_ids.shape
+    if Y is None:
+        Y = torch.empty((T, top_k, M), dtype=torch.float32, device=X.device)
+    if ws is None:
+        ws = torch.empty(max(1, kq_workspace_bytes(KQ_OP_MOE, wtype, M, K, T, n_experts, top_k)),
+                         dtype=torch.uint8, device=X.device)
+    check(lib().kq_moe_grouped_gemm(_wt(wtype), _dev(W_experts, "W_experts", torch.uint8), n_experts,
+                                    _dev(expert_ids, "expert_ids", torch.int32), top_k,
+                                    _dev(X, "X", torch.float32), _dev(Y, "Y", torch.float32), M, K, T,
+                                    _dev(ws, "ws", torch.uint8), ws.numel(), _stream(stream)),
+          "kq_moe_grouped_gemm")
+    return Y
+
+
+def kq_get_device_error(stream=None) -> int:
+    """Waits for the stream; returns and clears the first recorded device error code."""
+    code = ctypes.c_int32(0)
+    st = lib().kq_get_device_error(ctypes.byref(code), _stream(stream))
+    if st not in (0, 7):
+        raise KQError(st, "kq_get_device_error")
+    return int(code.value)

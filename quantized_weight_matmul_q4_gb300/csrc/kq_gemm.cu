@@ -1,0 +1,818 @@
+// Prefill GEMM and MoE grouped GEMM on the fifth-generation tensor cores.
+//
+// Y[n, m] = Sum_k dequant(W)[m, k] * x_hat[n, k], x_hat = fp16(d_h * q) of the
+// Q8_1 activations.
+//
+// Method: "ZINC MMQ v2 — Fused Q4_K×Q8_1 Tensor-Core GEMM" (Kernel
+// architecture: weight tiles unpacked once in shared memory and fed to the
+// tensor cores; Persistent kernel + atomic work queue; MoE routing: the
+// expert's weight tile is loaded once for all of its tokens) and "Prefill Gap
+// Closure Plan" (T1 fused dequant GEMM; T2 grouped expert GEMM with histogram,
+// prefix sum and scatter). The pages' kernels target sm_89/sm_120 with
+// mma.sync and cp.async; this one is built for sm_103a:
+//
+//  * warp 12 streams raw weight super-blocks (128 rows x 1 super-block per
+//    stage) with 2-D TMA, warp 14 streams x_hat tiles (128-byte swizzle) with
+//    2-D TMA, each into its own mbarrier ring;
+//  * warps 0-7 unpack Q4_K / Q6_K to fp16 straight into the swizzled K-major
+//    layout the tensor core reads (the "in-SMEM dequant" of the page), four
+//    64-wide K steps per super-block;
+//  * one thread of warp 13 issues tcgen05.mma (M=128, N<=256, K=16) into one
+//    of two 256-column accumulators in tensor memory;
+//  * warps 8-11 drain the other accumulator (tcgen05.ld) to global memory
+//    while the next tile is being computed.
+//
+// Tiles are statically strided over a persistent grid (one CTA per SM), so
+// results do not depend on scheduling; a split K range is summed afterwards in
+// a fixed order. Every wait is bounded (ERR_WAIT_TIMEOUT, no hang).
+#include "kq_internal.h"
+#include "kq_common.cuh"
+
+namespace kq {
+
+constexpr int GM_BM = 128;            // weight rows per tile (MMA M)
+constexpr int GM_BNMAX = 256;         // largest token tile (MMA N)
+constexpr int GM_BK = 64;             // K per A/B stage: one 128-byte swizzled row of fp16
+constexpr int GM_A_BYTES = GM_BM * GM_BK * 2;
+constexpr int GM_BBOX = 64;           // token rows per x_hat TMA box
+constexpr int GM_BBOX_BYTES = GM_BBOX * GM_BK * 2;
+constexpr int GM_DQ_WARPS = 8;        // warps 0..7
+constexpr int GM_EPI_WARP0 = 8;       // warps 8..11
+constexpr int GM_RAW_WARP = 12;
+constexpr int GM_MMA_WARP = 13;
+constexpr int GM_B_WARP = 14;
+constexpr int GM_THREADS = 15 * 32;
+constexpr int GM_TMEM_COLS = 512;     // two accumulators of 256 fp32 columns
+constexpr int GM_SMEM_LIMIT = 227 * 1024;
+constexpr int MOE_MAX_EXPERTS = 512;
+
+template <int WT>
+struct RawBox;
+template <>
+struct RawBox<KQ_Q4_K> {
+  static constexpr int BYTES = 144;  // one Q4_K super-block per row, 16-byte aligned in a row
+};
+template <>
+struct RawBox<KQ_Q6_K> {
+  static constexpr int BYTES = 224;  // a 16-byte aligned window covering one 210-byte Q6_K block
+};
+
+struct GemmArgs {
+  int M;            // output rows (per expert for MoE)
+  int N;            // token rows of x_hat
+  int nb;           // super-blocks per weight row
+  int m_tiles, n_tiles, splits, bn;
+  int ab_stages, raw_stages;
+  int b_stage_bytes;
+  float* Y;
+  float* partial;   // split-K partial sums [splits][N][M]
+  // MoE
+  int n_experts;
+  const int* counts;
+  const int* offsets;
+  const int* tile_start;
+  const int* entries;
+  int* err;
+};
+
+struct Tile {
+  int wrow0;   // first weight row (global row of the concatenated matrix)
+  int m0;      // first output row
+  int xrow0;   // first x_hat row
+  int ncols;   // valid tokens in the tile
+  int kb0, kb1;
+  int split;
+  int e;       // expert (MoE)
+  int nbase;   // entries index of column 0 (MoE)
+};
+
+template <bool MOE>
+__device__ __forceinline__ Tile decode_tile(const GemmArgs& a, int t, const int* s_tile_start, const int* s_counts,
+                                            const int* s_offsets) {
+  Tile T;
+  if (!MOE) {
+    const int split = t % a.splits;
+    const int mn = t / a.splits;
+    const int nt = mn % a.n_tiles, mt = mn / a.n_tiles;
+    T.m0 = mt * GM_BM;
+    T.wrow0 = T.m0;
+    T.xrow0 = nt * a.bn;
+    T.ncols = min(a.bn, a.N - T.xrow0);
+    T.split = split;
+    T.kb0 = static_cast<int>(static_cast<int64_t>(split) * a.nb / a.splits);
+    T.kb1 = static_cast<int>(static_cast<int64_t>(split + 1) * a.nb / a.splits);
+    T.e = 0;
+    T.nbase = 0;
+  } else {
+    int lo = 0, hi = a.n_experts;  // find e with tile_start[e] <= t < tile_start[e+1]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_tile_start[mid] <= t) lo = mid; else hi = mid;
+    }
+    const int e = lo;
+    const int local = t - s_tile_start[e];
+    const int nch = (s_counts[e] + a.bn - 1) / a.bn;
+    const int mt = local / nch, nc = local % nch;
+    T.e = e;
+    T.m0 = mt * GM_BM;
+    T.wrow0 = e * a.M + T.m0;
+    T.nbase = s_offsets[e] + nc * a.bn;
+    T.xrow0 = T.nbase;
+    T.ncols = min(a.bn, s_counts[e] - nc * a.bn);
+    T.kb0 = 0;
+    T.kb1 = a.nb;
+    T.split = 0;
+  }
+  return T;
+}
+
+// --- weight unpacking into the 128-byte-swizzled K-major fp16 A tile ----------
+// A tile: 128 rows x 64 fp16; 16-byte chunk c of row r lives at
+// r*128 + ((c ^ (r & 7)) << 4).
+__device__ __forceinline__ void store_chunk(uint8_t* a_tile, int r, int c, uint32_t o0, uint32_t o1, uint32_t o2,
+                                            uint32_t o3) {
+  *reinterpret_cast<uint4*>(a_tile + r * 128 + ((c ^ (r & 7)) << 4)) = make_uint4(o0, o1, o2, o3);
+}
+
+// Q4_K, K step s (0..3) of a super-block covers sub-blocks 2s (low nibbles of
+// qs[32s..32s+31]) and 2s+1 (high nibbles). Thread tid: row tid/2, sub-block
+// 2s + (tid&1), 32 weights w = d*sc*nib - dmin*m computed as one fp16 fma on
+// the exact nibble.
+__device__ __forceinline__ void dequant_q4k(const uint8_t* __restrict__ raw, int s, uint8_t* a_tile, int tid) {
+  const int r = tid >> 1, hf = tid & 1;
+  const uint8_t* blk = raw + r * Q4K_BYTES;
+  const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
+  const uint4 q0 = *reinterpret_cast<const uint4*>(blk + 16 + 32 * s);
+  const uint4 q1 = *reinterpret_cast<const uint4*>(blk + 32 + 32 * s);
+  const int j = 2 * s + hf;
+  uint32_t scw, mw;
+  if (s < 2) {
+    scw = hdr.y & 0x3F3F3F3Fu;
+    mw = hdr.z & 0x3F3F3F3Fu;
+  } else {
+    scw = (hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u);
+    mw = ((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u);
+  }
+  const int bi = (j & 3) * 8;
+  const float sc = static_cast<float>((scw >> bi) & 0xFFu);
+  const float mn = static_cast<float>((mw >> bi) & 0xFFu);
+  const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x & 0xFFFFu)));
+  const float dmin = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x >> 16)));
+  const __half2 scale2 = __float2half2_rn(d * sc);
+  const __half2 negmin2 = __float2half2_rn(-(dmin * mn));
+  const __half2 k1024 = __float2half2_rn(1024.f);
+  const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc) {
+    uint32_t o[4];
+#pragma unroll
+    for (int ww = 0; ww < 2; ++ww) {
+      const uint32_t src = hf ? (w[2 * cc + ww] >> 4) : w[2 * cc + ww];
+      // bytes 0,1 (and 2,3) -> fp16 (1024 + nibble) pairs
+      const uint32_t t0 = __byte_perm(src, 0x64646464u, 0x5140) & 0xFF0FFF0Fu;
+      const uint32_t t1 = __byte_perm(src, 0x64646464u, 0x7362) & 0xFF0FFF0Fu;
+      o[2 * ww] = half2_bits(__hfma2(__hsub2(bits_half2(t0), k1024), scale2, negmin2));
+      o[2 * ww + 1] = half2_bits(__hfma2(__hsub2(bits_half2(t1), k1024), scale2, negmin2));
+    }
+    store_chunk(a_tile, r, 4 * hf + cc, o[0], o[1], o[2], o[3]);
+  }
+}
+
+// Q6_K, K step s covers weights 64s..64s+63 of the super-block: half h = s/2,
+// quarters g = 2(s&1) and 2(s&1)+1. Thread tid: row tid/2, quarter
+// g = 2(s&1) + (tid&1), 32 weights d*sc*(q-32), q = 4 bits of ql | 2 bits of qh.
+// The block starts `rem` bytes into the row's 16-byte aligned window.
+__device__ __forceinline__ void dequant_q6k(const uint8_t* __restrict__ raw, int rem, int s, uint8_t* a_tile,
+                                            int tid) {
+  const int r = tid >> 1, gg = tid & 1;
+  const uint8_t* blk = raw + r * RawBox<KQ_Q6_K>::BYTES + rem;
+  const int h = s >> 1, g = 2 * (s & 1) + gg;
+  const int sh = (rem & 3) * 8;  // 0 or 16
+  const uint32_t* pl = reinterpret_cast<const uint32_t*>(blk - (rem & 3) + 64 * h + 32 * (g & 1));
+  const uint32_t* ph = reinterpret_cast<const uint32_t*>(blk - (rem & 3) + 128 + 32 * h);
+  uint32_t ql[8], qh[8];
+  {
+    uint32_t a[9], b[9];
+#pragma unroll
+    for (int i = 0; i < 9; ++i) {
+      a[i] = pl[i];
+      b[i] = ph[i];
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      ql[i] = __funnelshift_r(a[i], a[i + 1], sh);
+      qh[i] = __funnelshift_r(b[i], b[i + 1], sh);
+    }
+  }
+  const float d = __half2float(*reinterpret_cast<const __half*>(blk + 208));
+  const int8_t* scp = reinterpret_cast<const int8_t*>(blk + 192 + 8 * h + 2 * g);
+  const __half2 s0 = __float2half2_rn(d * static_cast<float>(scp[0]));
+  const __half2 s1 = __float2half2_rn(d * static_cast<float>(scp[1]));
+  const __half2 k1056 = __float2half2_rn(1056.f);
+  const bool low = (s & 1) == 0;  // quarters 0,1 use low nibbles, 2,3 high
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc) {
+    uint32_t o[4];
+#pragma unroll
+    for (int ww = 0; ww < 2; ++ww) {
+      const int i = 2 * cc + ww;
+      const uint32_t lo = low ? (ql[i] & 0x0F0F0F0Fu) : ((ql[i] >> 4) & 0x0F0F0F0Fu);
+      const uint32_t q = lo | (((qh[i] >> (2 * g)) & 0x03030303u) << 4);
+      const uint32_t t0 = __byte_perm(q, 0x64646464u, 0x5140);
+      const uint32_t t1 = __byte_perm(q, 0x64646464u, 0x7362);
+      const __half2 sc2 = (i < 4) ? s0 : s1;
+      o[2 * ww] = half2_bits(__hmul2(__hsub2(bits_half2(t0), k1056), sc2));
+      o[2 * ww + 1] = half2_bits(__hmul2(__hsub2(bits_half2(t1), k1056), sc2));
+    }
+    store_chunk(a_tile, r, 4 * gg + cc, o[0], o[1], o[2], o[3]);
+  }
+}
+
+template <int WT, bool MOE>
+__global__ void __launch_bounds__(GM_THREADS, 1)
+    kq_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                   const GemmArgs a) {
+  extern __shared__ uint8_t smem_dyn[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+  constexpr int RAW_BYTES = RawBox<WT>::BYTES * GM_BM;
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + a.ab_stages * GM_A_BYTES;
+  uint8_t* sRaw = sB + a.ab_stages * a.b_stage_bytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sRaw + a.raw_stages * RAW_BYTES);
+  uint64_t* raw_full = bars;
+  uint64_t* raw_empty = raw_full + a.raw_stages;
+  uint64_t* a_full = raw_empty + a.raw_stages;
+  uint64_t* b_full = a_full + a.ab_stages;
+  uint64_t* ab_empty = b_full + a.ab_stages;
+  uint64_t* acc_full = ab_empty + a.ab_stages;
+  uint64_t* acc_empty = acc_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* s_tile_start = reinterpret_cast<int*>(tmem_slot + 4);
+  int* s_counts = s_tile_start + (a.n_experts + 1);
+  int* s_offsets = s_counts + a.n_experts;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < a.raw_stages; ++i) {
+      mbar_init(&raw_full[i], 1);
+      mbar_init(&raw_empty[i], GM_DQ_WARPS);
+    }
+    for (int i = 0; i < a.ab_stages; ++i) {
+      mbar_init(&a_full[i], GM_DQ_WARPS);
+      mbar_init(&b_full[i], 1);
+      mbar_init(&ab_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], 4);
+    }
+    *abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == GM_MMA_WARP) {
+    tmem_alloc(tmem_slot, GM_TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == GM_RAW_WARP && lane == 0) {
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmX);
+  }
+  int total_tiles;
+  if (MOE) {
+    for (int i = threadIdx.x; i <= a.n_experts; i += GM_THREADS) s_tile_start[i] = a.tile_start[i];
+    for (int i = threadIdx.x; i < a.n_experts; i += GM_THREADS) {
+      s_counts[i] = a.counts[i];
+      s_offsets[i] = a.offsets[i];
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  if (MOE)
+    total_tiles = s_tile_start[a.n_experts];
+  else
+    total_tiles = a.m_tiles * a.n_tiles * a.splits;
+
+  if (warp == GM_RAW_WARP) {
+    // ---- raw weight producer -------------------------------------------------
+    if (lane == 0) {
+      int st = 0;
+      uint32_t ph = 0;
+      for (int t = blockIdx.x; t < total_tiles && !*abort; t += gridDim.x) {
+        const Tile T = decode_tile<MOE>(a, t, s_tile_start, s_counts, s_offsets);
+        for (int kb = T.kb0; kb < T.kb1; ++kb) {
+          if (!mbar_wait(&raw_empty[st], ph ^ 1, abort, a.err)) break;
+          mbar_expect_tx(&raw_full[st], RAW_BYTES);
+          const int x = (WT == KQ_Q4_K) ? kb * Q4K_BYTES : ((kb * Q6K_BYTES) & ~15);
+          tma_load_2d(sRaw + st * RAW_BYTES, &tmW, &raw_full[st], x, T.wrow0);
+          if (++st == a.raw_stages) {
+            st = 0;
+            ph ^= 1;
+          }
+        }
+      }
+    }
+  } else if (warp == GM_B_WARP) {
+    // ---- activation producer -------------------------------------------------
+    if (lane == 0) {
+      int st = 0;
+      uint32_t ph = 0;
+      for (int t = blockIdx.x; t < total_tiles && !*abort; t += gridDim.x) {
+        const Tile T = decode_tile<MOE>(a, t, s_tile_start, s_counts, s_offsets);
+        const int nbox = (T.ncols + GM_BBOX - 1) / GM_BBOX;
+        for (int kb = T.kb0; kb < T.kb1 && !*abort; ++kb) {
+          for (int s = 0; s < 4; ++s) {
+            if (!mbar_wait(&ab_empty[st], ph ^ 1, abort, a.err)) break;
+            mbar_expect_tx(&b_full[st], nbox * GM_BBOX_BYTES);
+            for (int j = 0; j < nbox; ++j)
+              tma_load_2d(sB + st * a.b_stage_bytes + j * GM_BBOX_BYTES, &tmX, &b_full[st],
+                          kb * QK_K + s * GM_BK, T.xrow0 + j * GM_BBOX);
+            if (++st == a.ab_stages) {
+              st = 0;
+              ph ^= 1;
+            }
+          }
+        }
+      }
+    }
+  } else if (warp == GM_MMA_WARP) {
+    // ---- tensor-core issuer --------------------------------------------------
+    if (lane == 0) {
+      int st = 0;
+      uint32_t ph = 0;
+      int it = 0;
+      for (int t = blockIdx.x; t < total_tiles && !*abort; t += gridDim.x, ++it) {
+        const Tile T = decode_tile<MOE>(a, t, s_tile_start, s_counts, s_offsets);
+        const int acc = it & 1;
+        if (!mbar_wait(&acc_empty[acc], ((it >> 1) & 1) ^ 1, abort, a.err)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * GM_BNMAX;
+        const int n_mma = (T.ncols + 15) & ~15;
+        const uint32_t idesc = idesc_f16_f32(GM_BM, n_mma);
+        bool first = true;
+        for (int kb = T.kb0; kb < T.kb1 && !*abort; ++kb) {
+          for (int s = 0; s < 4; ++s) {
+            if (!mbar_wait(&a_full[st], ph, abort, a.err)) break;
+            if (!mbar_wait(&b_full[st], ph, abort, a.err)) break;
+            tc_fence_after();
+            const uint64_t ad = smem_desc_sw128(smem_u32(sA + st * GM_A_BYTES));
+            const uint64_t bd = smem_desc_sw128(smem_u32(sB + st * a.b_stage_bytes));
+#pragma unroll
+            for (int k = 0; k < GM_BK / 16; ++k) {
+              // +32 bytes per K=16 step inside the 128-byte swizzled row
+              umma_f16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (first && k == 0) ? 0u : 1u);
+            }
+            first = false;
+            umma_commit(&ab_empty[st]);
+            if (++st == a.ab_stages) {
+              st = 0;
+              ph ^= 1;
+            }
+          }
+        }
+        umma_commit(&acc_full[acc]);
+      }
+    }
+  } else if (warp < GM_DQ_WARPS) {
+    // ---- weight unpackers ----------------------------------------------------
+    const int tid = threadIdx.x;  // 0..255
+    int rst = 0, ast = 0;
+    uint32_t rph = 0, aph = 0;
+    for (int t = blockIdx.x; t < total_tiles && !*abort; t += gridDim.x) {
+      const Tile T = decode_tile<MOE>(a, t, s_tile_start, s_counts, s_offsets);
+      for (int kb = T.kb0; kb < T.kb1 && !*abort; ++kb) {
+        if (!mbar_wait(&raw_full[rst], rph, abort, a.err)) break;
+        const uint8_t* raw = sRaw + rst * RAW_BYTES;
+        for (int s = 0; s < 4; ++s) {
+          if (!mbar_wait(&ab_empty[ast], aph ^ 1, abort, a.err)) break;
+          uint8_t* at = sA + ast * GM_A_BYTES;
+          if (WT == KQ_Q4_K)
+            dequant_q4k(raw, s, at, tid);
+          else
+            dequant_q6k(raw, (kb * Q6K_BYTES) & 15, s, at, tid);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&a_full[ast]);
+          if (++ast == a.ab_stages) {
+            ast = 0;
+            aph ^= 1;
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&raw_empty[rst]);
+        if (++rst == a.raw_stages) {
+          rst = 0;
+          rph ^= 1;
+        }
+      }
+    }
+  } else {
+    // ---- epilogue: tensor memory -> fp32 Y -----------------------------------
+    const int wq = warp - GM_EPI_WARP0;  // == warp % 4: this warp's 32 TMEM lanes
+    int it = 0;
+    for (int t = blockIdx.x; t < total_tiles && !*abort; t += gridDim.x, ++it) {
+      const Tile T = decode_tile<MOE>(a, t, s_tile_start, s_counts, s_offsets);
+      const int acc = it & 1;
+      if (!mbar_wait(&acc_full[acc], (it >> 1) & 1, abort, a.err)) break;
+      tc_fence_after();
+      const int m = T.m0 + 32 * wq + lane;
+      const bool mok = m < a.M;
+      for (int c0 = 0; c0 < T.ncols; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tmem_base + acc * GM_BNMAX + (static_cast<uint32_t>(32 * wq) << 16) + c0, r);
+        tmem_ld_wait();
+        if (MOE) {
+          const int my_slot = (c0 + lane < T.ncols) ? __ldg(a.entries + T.nbase + c0 + lane) : 0;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int slot = __shfl_sync(0xffffffffu, my_slot, j);
+            if (c0 + j < T.ncols && mok) a.Y[static_cast<int64_t>(slot) * a.M + m] = __uint_as_float(r[j]);
+          }
+        } else {
+          float* out = (a.splits == 1)
+                           ? a.Y + static_cast<int64_t>(T.xrow0) * a.M
+                           : a.partial + (static_cast<int64_t>(T.split) * a.N + T.xrow0) * a.M;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (c0 + j < T.ncols && mok) out[static_cast<int64_t>(c0 + j) * a.M + m] = __uint_as_float(r[j]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == GM_MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, GM_TMEM_COLS);
+  }
+}
+
+// Fixed-order sum of the split-K partials: Y[i] = Sum_s P[s][i] (n elements).
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restrict__ P, float* __restrict__ Y,
+                                                            int64_t n, int splits) {
+  const int64_t i4 = (static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x) * 4;
+  if (i4 >= n) return;
+  if (i4 + 4 <= n && (n & 3) == 0) {
+    float4 acc = __ldg(reinterpret_cast<const float4*>(P + i4));
+    for (int s = 1; s < splits; ++s) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(P + static_cast<int64_t>(s) * n + i4));
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    *reinterpret_cast<float4*>(Y + i4) = acc;
+  } else {
+    for (int64_t i = i4; i < n && i < i4 + 4; ++i) {
+      float acc = __ldg(P + i);
+      for (int s = 1; s < splits; ++s) acc += __ldg(P + static_cast<int64_t>(s) * n + i);
+      Y[i] = acc;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// MoE routing ("Prefill Gap Closure Plan", T2 step 1; "ZINC MMQ v2", MoE
+// routing): histogram of expert ids -> exclusive prefix sum -> scatter of the
+// (token, slot) ids into per-expert buckets, in token-then-slot order. One CTA;
+// warp w owns a contiguous range of slots, so per-warp counts plus two scans
+// give every slot its bucket position without atomics (deterministic).
+// Also lays out the tile list: expert e owns m_tiles * ceil(count_e / bn)
+// consecutive tiles starting at tile_start[e].
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int block_excl_scan_1024(int v, int* wsum, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) wsum[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = wsum[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    wsum[lane] = w;
+  }
+  __syncthreads();
+  const int excl = x - v + (warp > 0 ? wsum[warp - 1] : 0);
+  *total = wsum[31];
+  __syncthreads();
+  return excl;
+}
+
+__global__ void __launch_bounds__(1024) moe_route_kernel(const int* __restrict__ ids, int n, int top_k, int E,
+                                                         int m_tiles, int bn, int* counts, int* offsets,
+                                                         int* tile_start, int* entries, int* src, float* Y, int M,
+                                                         int* err) {
+  extern __shared__ int rsm[];
+  int* cnt = rsm;                 // [32][E]: per-warp counts, then per-warp bases
+  int* base = cnt + 32 * E;       // [E]: bucket start
+  int* wsum = base + E;           // [32]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < 32 * E; i += 1024) cnt[i] = 0;
+  __syncthreads();
+  const int L = (((n + 31) / 32) + 31) & ~31;
+  const int lo = min(n, warp * L), hi = min(n, lo + L);
+  for (int b0 = lo; b0 < hi; b0 += 32) {
+    const int i = b0 + lane;
+    int e = (i < hi) ? __ldg(ids + i) : -1;
+    if (i < hi && (e < 0 || e >= E)) {
+      report_error(err, ERR_EXPERT_ID);
+      e = -1;
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && lane == __ffs(peers) - 1) cnt[warp * E + e] += __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+  int tot = 0;
+  if (threadIdx.x < E) {
+    const int e = threadIdx.x;
+    for (int w = 0; w < 32; ++w) {
+      const int c = cnt[w * E + e];
+      cnt[w * E + e] = tot;
+      tot += c;
+    }
+  }
+  int n_valid, n_tiles;
+  const int off = block_excl_scan_1024(threadIdx.x < E ? tot : 0, wsum, &n_valid);
+  const int my_tiles = threadIdx.x < E ? m_tiles * ((tot + bn - 1) / bn) : 0;
+  const int toff = block_excl_scan_1024(my_tiles, wsum, &n_tiles);
+  if (threadIdx.x < E) {
+    counts[threadIdx.x] = tot;
+    offsets[threadIdx.x] = off;
+    tile_start[threadIdx.x] = toff;
+    base[threadIdx.x] = off;
+  }
+  if (threadIdx.x == 0) {
+    offsets[E] = n_valid;
+    tile_start[E] = n_tiles;
+  }
+  __syncthreads();
+  const unsigned lt = (1u << lane) - 1u;
+  for (int b0 = lo; b0 < hi; b0 += 32) {
+    const int i = b0 + lane;
+    int e = (i < hi) ? __ldg(ids + i) : -1;
+    const bool bad = (i < hi) && (e < 0 || e >= E);
+    if (bad) e = -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (e >= 0) {
+      const int pos = base[e] + cnt[warp * E + e] + __popc(peers & lt);
+      entries[pos] = i;
+      src[pos] = i / top_k;
+    }
+    __syncwarp();
+    if (e >= 0 && lane == __ffs(peers) - 1) cnt[warp * E + e] += __popc(peers);
+    __syncwarp();
+    if (bad)
+      for (int m = 0; m < M; ++m) Y[static_cast<int64_t>(i) * M + m] = 0.f;
+  }
+  for (int p = n_valid + threadIdx.x; p < n; p += 1024) src[p] = -1;
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+static inline int64_t round_up64(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
+
+bool encode_tmap_2d(CUtensorMap* tm, CUtensorMapDataType dtype, const void* base, uint64_t dim0, uint64_t dim1,
+                    uint64_t stride1_bytes, uint32_t box0, uint32_t box1, CUtensorMapSwizzle swizzle) {
+  typedef CUresult (*EncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                               const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                               CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  static EncodeFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !p)
+      return false;
+    fn = reinterpret_cast<EncodeFn>(p);
+  }
+  const cuuint64_t dims[2] = {dim0, dim1};
+  const cuuint64_t strides[1] = {stride1_bytes};
+  const cuuint32_t box[2] = {box0, box1};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(tm, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+static int raw_box_bytes(int wtype) { return wtype == KQ_Q4_K ? RawBox<KQ_Q4_K>::BYTES : RawBox<KQ_Q6_K>::BYTES; }
+
+// Ring depths for a token tile of bn rows: 3-4 A/B stages, then as many raw
+// weight stages (2..8) as the remaining shared memory holds.
+static bool choose_stages(int wtype, int bn, int n_experts, GemmArgs* a, size_t* smem) {
+  const int b_bytes = ((bn + GM_BBOX - 1) / GM_BBOX) * GM_BBOX_BYTES;
+  const int raw_bytes = raw_box_bytes(wtype) * GM_BM;
+  const int tables = (MOE_MAX_EXPERTS >= n_experts ? 3 * (n_experts + 1) * 4 : 0) + 64;
+  for (int ab = 4; ab >= 2; --ab) {
+    const int fixed = 1024 + ab * (GM_A_BYTES + b_bytes) + tables + 256;
+    int raw = (GM_SMEM_LIMIT - fixed) / raw_bytes;
+    if (raw > 8) raw = 8;
+    if (raw >= 2 && (ab < 4 || raw >= 4)) {
+      a->ab_stages = ab;
+      a->raw_stages = raw;
+      a->b_stage_bytes = b_bytes;
+      *smem = static_cast<size_t>(fixed + raw * raw_bytes);
+      return true;
+    }
+  }
+  return false;
+}
+
+GemmPlan plan_gemm(int wtype, int64_t M, int64_t K, int64_t N, int num_sms) {
+  (void)wtype;
+  GemmPlan p{};
+  const int bn = static_cast<int>(N >= GM_BNMAX ? GM_BNMAX : round_up64(N, GM_BBOX));
+  p.m_tiles = static_cast<int>((M + GM_BM - 1) / GM_BM);
+  p.n_tiles = static_cast<int>((N + bn - 1) / bn);
+  const int nb = static_cast<int>(K / QK_K);
+  const int tiles = p.m_tiles * p.n_tiles;
+  int splits = 1;
+  if (tiles < num_sms) {
+    splits = num_sms / tiles;
+    if (splits > nb) splits = nb;
+    if (splits > 16) splits = 16;
+    if (splits < 1) splits = 1;
+  }
+  p.splits = splits;
+  const int64_t total = static_cast<int64_t>(tiles) * splits;
+  p.grid = static_cast<int>(total < num_sms ? total : num_sms);
+  p.xhat_bytes = static_cast<size_t>(round_up64(N * K * 2, 1024));
+  p.partial_bytes = splits > 1 ? static_cast<size_t>(round_up64(static_cast<int64_t>(splits) * N * M * 4, 1024)) : 0;
+  p.total_bytes = p.xhat_bytes + p.partial_bytes;
+  return p;
+}
+
+template <int WT, bool MOE>
+static cudaError_t launch_kernel(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmArgs& a, int grid,
+                                 size_t smem, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(kq_gemm_kernel<WT, MOE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  kq_gemm_kernel<WT, MOE><<<grid, GM_THREADS, smem, s>>>(tmW, tmX, a);
+  return cudaGetLastError();
+}
+
+static cudaError_t dispatch(int wtype, bool moe, const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmArgs& a,
+                            int grid, size_t smem, cudaStream_t s) {
+  if (wtype == KQ_Q4_K)
+    return moe ? launch_kernel<KQ_Q4_K, true>(tmW, tmX, a, grid, smem, s)
+               : launch_kernel<KQ_Q4_K, false>(tmW, tmX, a, grid, smem, s);
+  return moe ? launch_kernel<KQ_Q6_K, true>(tmW, tmX, a, grid, smem, s)
+             : launch_kernel<KQ_Q6_K, false>(tmW, tmX, a, grid, smem, s);
+}
+
+static bool weight_tmap(CUtensorMap* tm, int wtype, const void* W, int64_t rows, int64_t K) {
+  const int64_t rs = (K / QK_K) * (wtype == KQ_Q4_K ? Q4K_BYTES : Q6K_BYTES);
+  return encode_tmap_2d(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, static_cast<uint64_t>(rs), static_cast<uint64_t>(rows),
+                        static_cast<uint64_t>(rs), static_cast<uint32_t>(raw_box_bytes(wtype)), GM_BM,
+                        CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+static bool xhat_tmap(CUtensorMap* tm, const void* Xh, int64_t rows, int64_t K) {
+  return encode_tmap_2d(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Xh, static_cast<uint64_t>(K),
+                        static_cast<uint64_t>(rows), static_cast<uint64_t>(K * 2), GM_BK, GM_BBOX,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+cudaError_t launch_gemm(int wtype, const void* W, const float* X, float* Y, int64_t M, int64_t K, int64_t N,
+                        void* ws, const GemmPlan& plan, int* err, cudaStream_t s, int* status) {
+  *status = KQ_OK;
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  __half* xh = reinterpret_cast<__half*>(wsb);
+  float* partial = reinterpret_cast<float*>(wsb + plan.xhat_bytes);
+  cudaError_t e = launch_quantize_xhat(X, xh, K, N, nullptr, s);
+  if (e != cudaSuccess) return e;
+  CUtensorMap tmW, tmX;
+  if (!weight_tmap(&tmW, wtype, W, M, K) || !xhat_tmap(&tmX, xh, N, K)) {
+    *status = KQ_ERR_CUDA;
+    return cudaSuccess;
+  }
+  GemmArgs a{};
+  a.M = static_cast<int>(M);
+  a.N = static_cast<int>(N);
+  a.nb = static_cast<int>(K / QK_K);
+  a.m_tiles = plan.m_tiles;
+  a.n_tiles = plan.n_tiles;
+  a.splits = plan.splits;
+  a.bn = static_cast<int>(N >= GM_BNMAX ? GM_BNMAX : round_up64(N, GM_BBOX));
+  a.Y = Y;
+  a.partial = partial;
+  a.n_experts = 0;
+  a.err = err;
+  size_t smem = 0;
+  if (!choose_stages(wtype, a.bn, 0, &a, &smem)) {
+    *status = KQ_ERR_SHAPE;
+    return cudaSuccess;
+  }
+  e = dispatch(wtype, false, tmW, tmX, a, plan.grid, smem, s);
+  if (e != cudaSuccess) return e;
+  if (plan.splits > 1) {
+    const int64_t n = N * M;
+    const int64_t threads = (n + 3) / 4;
+    splitk_reduce_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(partial, Y, n, plan.splits);
+    e = cudaGetLastError();
+  }
+  return e;
+}
+
+// MoE workspace: counts[E] | offsets[E+1] | tile_start[E+1] | entries[n] | src[n] | x_hat[n][K] fp16
+MoePlan plan_moe(int wtype, int64_t M, int64_t K, int64_t T, int n_experts, int top_k) {
+  (void)wtype;
+  MoePlan p{};
+  const int64_t n = T * top_k;
+  p.m_tiles = static_cast<int>((M + GM_BM - 1) / GM_BM);
+  size_t o = 0;
+  p.off_counts = o;
+  o += round_up64(4 * n_experts, 256);
+  p.off_offsets = o;
+  o += round_up64(4 * (n_experts + 1), 256);
+  p.off_tiles = o;
+  o += round_up64(4 * (n_experts + 1), 256);
+  p.off_entries = o;
+  o += round_up64(4 * n, 256);
+  p.off_src = o;
+  o += round_up64(4 * n, 1024);
+  p.off_xhat = o;
+  o += round_up64(n * K * 2, 1024);
+  p.total_bytes = o;
+  return p;
+}
+
+constexpr int MOE_BN = 128;  // tokens per MoE tile (one tile covers a typical expert bucket)
+
+cudaError_t launch_moe(int wtype, const void* W, int n_experts, const int32_t* ids, int top_k, const float* X,
+                       float* Y, int64_t M, int64_t K, int64_t T, void* ws, const MoePlan& plan, int* err,
+                       int num_sms, cudaStream_t s, int* status) {
+  *status = KQ_OK;
+  if (n_experts > MOE_MAX_EXPERTS) {
+    *status = KQ_ERR_SHAPE;
+    return cudaSuccess;
+  }
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  int* counts = reinterpret_cast<int*>(wsb + plan.off_counts);
+  int* offsets = reinterpret_cast<int*>(wsb + plan.off_offsets);
+  int* tile_start = reinterpret_cast<int*>(wsb + plan.off_tiles);
+  int* entries = reinterpret_cast<int*>(wsb + plan.off_entries);
+  int* src = reinterpret_cast<int*>(wsb + plan.off_src);
+  __half* xh = reinterpret_cast<__half*>(wsb + plan.off_xhat);
+  const int64_t n = T * top_k;
+
+  const size_t rsmem = static_cast<size_t>(32 * n_experts + n_experts + 32) * sizeof(int);
+  cudaError_t e = cudaFuncSetAttribute(moe_route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(rsmem));
+  if (e != cudaSuccess) return e;
+  moe_route_kernel<<<1, 1024, rsmem, s>>>(ids, static_cast<int>(n), top_k, n_experts, plan.m_tiles, MOE_BN, counts,
+                                          offsets, tile_start, entries, src, Y, static_cast<int>(M), err);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = launch_quantize_xhat(X, xh, K, n, src, s);
+  if (e != cudaSuccess) return e;
+
+  CUtensorMap tmW, tmX;
+  if (!weight_tmap(&tmW, wtype, W, static_cast<int64_t>(n_experts) * M, K) || !xhat_tmap(&tmX, xh, n, K)) {
+    *status = KQ_ERR_CUDA;
+    return cudaSuccess;
+  }
+  GemmArgs a{};
+  a.M = static_cast<int>(M);
+  a.N = static_cast<int>(n);
+  a.nb = static_cast<int>(K / QK_K);
+  a.m_tiles = plan.m_tiles;
+  a.n_tiles = 0;
+  a.splits = 1;
+  a.bn = MOE_BN;
+  a.Y = Y;
+  a.partial = nullptr;
+  a.n_experts = n_experts;
+  a.counts = counts;
+  a.offsets = offsets;
+  a.tile_start = tile_start;
+  a.entries = entries;
+  a.err = err;
+  size_t smem = 0;
+  if (!choose_stages(wtype, MOE_BN, n_experts, &a, &smem)) {
+    *status = KQ_ERR_SHAPE;
+    return cudaSuccess;
+  }
+  return dispatch(wtype, true, tmW, tmX, a, num_sms, smem, s);
+}
+
+}  // namespace kq

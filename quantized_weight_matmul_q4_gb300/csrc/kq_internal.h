@@ -1,0 +1,42 @@
+// Internal declarations shared by the CUDA translation units of libkq.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kq.h"
+
+namespace kq {
+
+cudaError_t launch_quantize_q8_1(const float* X, void* Xq, int64_t K, int64_t N, cudaStream_t s);
+cudaError_t launch_quantize_xhat(const float* X, __half* Xh, int64_t K, int64_t rows, const int* src_rows,
+                                 cudaStream_t s);
+cudaError_t launch_matvec(int wtype, const void* W, const float* x, float* y, int64_t M, int64_t K, int* err,
+                          int num_sms, cudaStream_t s, int* status);
+
+// Dense prefill GEMM plan: tiles of 128 weight rows x up to 256 tokens, with
+// the K range optionally split across CTAs (fixed-order reduction after).
+struct GemmPlan {
+  int m_tiles, n_tiles, splits, grid;
+  size_t xhat_bytes, partial_bytes, total_bytes;
+};
+GemmPlan plan_gemm(int wtype, int64_t M, int64_t K, int64_t N, int num_sms);
+cudaError_t launch_gemm(int wtype, const void* W, const float* X, float* Y, int64_t M, int64_t K, int64_t N,
+                        void* ws, const GemmPlan& plan, int* err, cudaStream_t s, int* status);
+
+struct MoePlan {
+  int m_tiles;
+  size_t off_counts, off_offsets, off_tiles, off_entries, off_src, off_xhat, total_bytes;
+};
+MoePlan plan_moe(int wtype, int64_t M, int64_t K, int64_t T, int n_experts, int top_k);
+cudaError_t launch_moe(int wtype, const void* W, int n_experts, const int32_t* ids, int top_k, const float* X,
+                       float* Y, int64_t M, int64_t K, int64_t T, void* ws, const MoePlan& plan, int* err,
+                       int num_sms, cudaStream_t s, int* status);
+
+// Builds a 2-D tiled tensor map through the driver entry point.
+bool encode_tmap_2d(CUtensorMap* tm, CUtensorMapDataType dtype, const void* base, uint64_t dim0, uint64_t dim1,
+                    uint64_t stride1_bytes, uint32_t box0, uint32_t box1, CUtensorMapSwizzle swizzle);
+
+}  // namespace kq

@@ -1,0 +1,59 @@
+// fp32 -> Q8_1 activation quantisation, one 32-element block per 8 threads.
+//
+// The quantiser of "06 · 8e/8e② — decode MMVQ" (§2 Principle and §3.2
+// ``quantize_pad40_block``), with the Q8_1 block sum of "ZINC MMQ v2" (What
+// they do right: Q8_1 activations):
+//   amax = max|x|, d = amax / 127, di = d != 0 ? 1 / d : 0,
+//   q = clamp(rint(x * di), -128, 127), stored scale d_h = fp16(d),
+//   block sum s = fp16(d_h * Sum q).
+// Every step is a single IEEE fp32 operation (correctly rounded division,
+// product, round-half-even rint), so the integer codes are reproducible
+// bit for bit on any IEEE machine. The file is compiled without fast-math.
+#pragma once
+
+#include "kq_common.cuh"
+
+namespace kq {
+
+struct Q8Quad {
+  int q[4];        // the four codes of this thread
+  float dh;        // fp16-rounded scale d_h, as fp32
+  __half dh_h;     // d_h
+  __half s_h;      // fp16(d_h * Sum q) over the whole block
+  int sumq;        // Sum q over the whole block
+};
+
+// Quantises the four values v of one thread; the 8 threads of an aligned
+// group of 8 lanes hold one 32-element block (thread j holds elements 4j..4j+3).
+// All 32 lanes of the warp must call this.
+__device__ __forceinline__ Q8Quad quantize_quad(float4 v) {
+  float a = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
+  const float d = __fdiv_rn(a, 127.0f);
+  const float di = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
+  Q8Quad r;
+  const float e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float t = rintf(__fmul_rn(e[j], di));
+    r.q[j] = static_cast<int>(fminf(fmaxf(t, -128.0f), 127.0f));
+  }
+  int s = r.q[0] + r.q[1] + r.q[2] + r.q[3];
+  s += __shfl_xor_sync(0xffffffffu, s, 1);
+  s += __shfl_xor_sync(0xffffffffu, s, 2);
+  s += __shfl_xor_sync(0xffffffffu, s, 4);
+  r.sumq = s;
+  r.dh_h = __float2half_rn(d);
+  r.dh = __half2float(r.dh_h);
+  r.s_h = __float2half_rn(__fmul_rn(r.dh, static_cast<float>(s)));  // exact product, one rounding
+  return r;
+}
+
+__device__ __forceinline__ uint32_t pack_q4(const int (&q)[4]) {
+  return (static_cast<uint32_t>(q[0]) & 0xFFu) | ((static_cast<uint32_t>(q[1]) & 0xFFu) << 8) |
+         ((static_cast<uint32_t>(q[2]) & 0xFFu) << 16) | ((static_cast<uint32_t>(q[3]) & 0xFFu) << 24);
+}
+
+}  // namespace kq

@@ -1,0 +1,75 @@
+"""Decode matvec (N = 1) on the GPU against the oracle, element by element,
+within |y - y_ref| <= 1e-3 * Sum_k |w_k x_k| + 1e-5 ("06 · 8e/8e② — decode
+MMVQ", §2 Principle and §3.2 Key code)."""
+import numpy as np
+import pytest
+
+from oracle import kq_oracle as ora
+from quantized_weight_matmul_q4_gb300 import kq_matvec, synthetic as syn
+from _kqutil import assert_within_bound, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(wtype, W, x, M, K):
+    import torch
+    y = kq_matvec(wtype, to_dev(W, torch), to_dev(x.reshape(-1), torch), M, K)
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+@pytest.mark.parametrize("name", ["matvec_q4k_512x2048", "decode_q4k_4096x11008", "decode_q4k_11008x4096"])
+def test_workload_full_parity(name):
+    wl = syn.make_workload(name)
+    M, K = wl["M"], wl["K"]
+    y = _run("q4_k", wl["W"][0], wl["X"], M, K)
+    Y, B = ora.matmul("q4_k", wl["W"][0], wl["X"], M, K)
+    assert_within_bound(y, Y[0], B[0], name)
+
+
+@pytest.mark.parametrize("wtype", ["q4_k", "q6_k"])
+@pytest.mark.parametrize("M,K", [(1, 256), (17, 512), (37, 11008), (300, 4096), (1000, 2304), (33, 65536)])
+def test_ragged_shapes(wtype, M, K):
+    if wtype == "q6_k" and K == 65536:
+        K = 14336                                    # Q6_K rows of 16-byte multiples, 8 rows per stage
+    rng = np.random.default_rng(M * 7 + K)
+    W = syn.weights(wtype, rng, M, K)
+    x = syn.activations(rng, K, 1)
+    y = _run(wtype, W, x, M, K)
+    Y, B = ora.matmul(wtype, W, x, M, K)
+    assert_within_bound(y, Y[0], B[0], f"{wtype} {M}x{K}")
+
+
+def test_q6k_ragged_tail_bytes():
+    # 43 Q6_K blocks per row = 9030 bytes: rows are not 16-byte multiples, so
+    # ranges start at 8-row boundaries and the last copy ends in a <16-byte tail.
+    M, K = 45, 11008
+    rng = np.random.default_rng(5)
+    W = syn.q6_k_weights(rng, M, K)
+    x = syn.activations(rng, K, 1)
+    y = _run("q6_k", W, x, M, K)
+    Y, B = ora.matmul("q6_k", W, x, M, K)
+    assert_within_bound(y, Y[0], B[0], "q6_k tail")
+
+
+def test_min_term_form_agrees_on_workload_rows():
+    wl = syn.make_workload("decode_q4k_4096x11008")
+    rows = np.arange(0, 4096, 97)
+    y = _run("q4_k", wl["W"][0], wl["X"], 4096, 11008)
+    y_min = ora.q4_k_min_term_matvec(wl["W"][0][rows], wl["X"][0], 11008)
+    _, B = ora.matmul_rows("q4_k", wl["W"][0], wl["X"], 11008, rows)
+    assert_within_bound(y[rows], y_min, B[0], "min-term rows")
+
+
+def test_deterministic():
+    wl = syn.make_workload("decode_q4k_11008x4096")
+    a = _run("q4_k", wl["W"][0], wl["X"], 11008, 4096)
+    b = _run("q4_k", wl["W"][0], wl["X"], 11008, 4096)
+    assert np.array_equal(a, b)
+
+
+def test_zero_activation_gives_zero():
+    M, K = 64, 1024
+    W = syn.q4_k_weights(np.random.default_rng(1), M, K)
+    y = _run("q4_k", W, np.zeros((1, K), np.float32), M, K)
+    assert np.all(y == 0)
