@@ -48,6 +48,9 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-sections", action="store_true", help="skip the prefill/MoE sections")
     p.add_argument("--section-iters", type=int, default=10)
+    p.add_argument("--only", default=None,
+                   help="profiling aid: run only 'decode' or one section (prefill_*/moe_*) and print its numbers")
+    p.add_argument("--eager", action="store_true", help="launch the decode step eagerly instead of as a CUDA graph")
     return p.parse_args()
 
 
@@ -231,24 +234,49 @@ def run_ours(args, dist):
         sets.append((wl["M"], wl["K"], Ws, x, y, wl["X"][0]))
     w_bytes_step = sum(W.numel() for s in sets for W in s[2])
     alg_bytes_launch = [M * Q4K_ROW(K) + 4 * K + 4 * M for (M, K) in DECODE_SHAPES]
-    launches_step = DECODE_COPIES * len(sets)
+    calls_step = DECODE_COPIES * len(sets)
+    launches_step = calls_step  # one kernel per call (x is quantised inside the matvec kernel)
 
     def step():
         for c in range(DECODE_COPIES):
             for (M, K, Ws, x, y, _) in sets:
                 kq.kq_matvec(kq.KQ_Q4_K, Ws[c], x, M, K, y=y)
 
+    if args.only and args.only != "decode":
+        res = run_sections(args, kq, syn, torch, dev, stream, pk, only=args.only)
+        print(json.dumps({"only": args.only, **res}), flush=True)
+        return None
+
     clocks = ClockSampler(dist.local)
     clocks.start()
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
+    # The decode sweep is launch-bound when driven from Python, so it is
+    # captured once in a CUDA graph and replayed (the library's calls allocate
+    # nothing and never synchronise, so they capture as they are).
+    run = step
+    if not args.eager:
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(graph):
+            step()
+        torch.cuda.synchronize()
+        run = graph.replay
+        for _ in range(max(3, args.warmup)):
+            run()
+        torch.cuda.synchronize()
     dist.barrier()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
-        step()
+        run()
     e1.record(stream)
     torch.cuda.synchronize()
     dist.barrier()
@@ -286,11 +314,11 @@ def run_ours(args, dist):
 
     # ---- sections: prefill GEMMs and MoE, each call timed with L2 flushed ----
     sections = {}
-    if not args.no_sections:
+    if not args.no_sections and not args.only:
         sections = run_sections(args, kq, syn, torch, dev, stream, pk)
     clk = clocks.stop()
 
-    avg_launch_s = ms_step / 1e3 / launches_step
+    avg_launch_s = ms_step / 1e3 / calls_step
     achieved = statistics.mean(alg_bytes_launch) / avg_launch_s / 1e9
     value = dist.world * w_bytes_step / (ms_step / 1e3) / 1e9
     out = {
@@ -308,7 +336,8 @@ def run_ours(args, dist):
         "data": "synthetic (seeded; Q4_K fields per the workload distributions, x ~ N(0,1))",
         "config": {
             "workload": "decode matvec N=1, Q4_K W[4096,11008] and W[11008,4096], Q8_1 quant fused",
-            "step": "16 kq_matvec launches: 8 rotated weight copies x 2 shapes",
+            "step": "16 kq_matvec launches: 8 rotated weight copies x 2 shapes"
+                    + ("" if args.eager else ", replayed as one CUDA graph"),
             "l2": "inputs larger than L2 (8 weight copies per shape, 406 MB of weights)",
             "parallelism": f"replicas x{dist.world}",
         },
@@ -322,6 +351,7 @@ def run_ours(args, dist):
             "peak_source": f"{pk_kind} (copy bandwidth)",
             "traffic": traffic_for("matvec_kernel_q4k_decode"),
             "algorithmic_bytes_per_launch": statistics.mean(alg_bytes_launch),
+            "duration": "mean time per kq_matvec launch over the timed region (launches PDL-chained in a CUDA graph)",
         },
         "e2e": {
             "value": round(dist.world * w_bytes_step / (ms_e2e / 1e3) / 1e9, 2),
@@ -353,12 +383,17 @@ def _timed_calls(fn, iters, warm, flush, torch, stream):
     return statistics.mean(times), min(times)
 
 
-def run_sections(args, kq, syn, torch, dev, stream, pk):
+def run_sections(args, kq, syn, torch, dev, stream, pk, only=None):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # 256 MB > L2
     res = {}
     iters = max(3, args.section_iters)
     gemm_names = ["prefill_q4k_4096x4096_n64", "prefill_q4k_4096x4096_n512",
                   "prefill_q4k_14336x4096_n2048", "prefill_q6k_4096x14336_n2048"]
+    moe_name = "moe_q4k_128x768x2048_t1024_top8"
+    if only is not None:
+        if only not in gemm_names + [moe_name]:
+            raise SystemExit(f"unknown section {only!r}")
+        gemm_names = [n for n in gemm_names if n == only]
     for name in gemm_names:
         wl = syn.make_workload(name)
         M, K, N = wl["M"], wl["K"], wl["N"]
@@ -377,7 +412,9 @@ def run_sections(args, kq, syn, torch, dev, stream, pk):
                      "frac_hbm_peak": round(wbytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"], 4),
                      "launches_per_call": None}
         del W, X, Y, ws
-    wl = syn.make_workload("moe_q4k_128x768x2048_t1024_top8")
+    if only is not None and only != moe_name:
+        return res
+    wl = syn.make_workload(moe_name)
     E, M, K, T, top_k = wl["n_experts"], wl["M"], wl["K"], wl["T"], wl["top_k"]
     W = torch.from_numpy(wl["W"][0]).to(dev)
     X = torch.from_numpy(wl["X"]).to(dev)
@@ -445,7 +482,10 @@ def main():
         return
     dist = Dist(args.gpus)
     out = run_ours(args, dist)
-    if dist.rank == 0:
+    if out is None:
+        dist.close()
+        return
+    if dist.rank == 0 and not args.only:
         gbs, secs = oracle_decode_gbs(512, 2, 10.0)
         out["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                                "sample": f"oracle matvec on the first 512 rows of each decode shape, "

@@ -98,13 +98,17 @@ KQ_API kq_status kq_quantize_q8_1(const float* X, void* Xq, int64_t K, int64_t N
  * kq_matvec — decode matvec y = dequant(W) . x for one token ([MMVQ] §2, §3.2:
  * integer dot products of the 4/6-bit codes with the Q8_1 codes of x, the
  * min term from the Q8_1 block sum, warp-shuffle row reductions). x is
- * quantised to Q8_1 inside the call.
+ * quantised to Q8_1 inside the call. Needs no workspace.
  * wtype: KQ_Q4_K or KQ_Q6_K. W: M rows of K/256 blocks; x: fp32 [K];
- * y: fp32 [M], written. Needs no workspace. A Q6_K row whose byte length is not
- * a multiple of 16 must have K <= 15360.
+ * y: fp32 [M], written.
+ * Weight streaming starts before the kernel waits for the previous kernel on
+ * the stream: W must not be written by a kernel that is still running when this
+ * call starts, i.e. by a preceding kernel that allows programmatic dependent
+ * launch. (A preceding ordinary kernel, copy or event is always complete.)
+ * A Q6_K row whose byte length is not a multiple of 16 must have K <= 15360.
  */
 KQ_API kq_status kq_matvec(int wtype, const void* W, const float* x, float* y, int64_t M, int64_t K,
-                    kq_stream_t stream);
+                           kq_stream_t stream);
 
 /*
  * kq_gemm — prefill GEMM Y = dequant(W) . X for N tokens ([MMQv2] Kernel

@@ -1,5 +1,6 @@
 // C ABI of libkq: argument checks, workspace sizing, device error word, and
 // dispatch to the kernels. Declarations and contracts: include/kq.h.
+#include <atomic>
 #include <mutex>
 
 #include "kq_common.cuh"
@@ -48,6 +49,8 @@ int sm_count_or_default() {
   return 152;
 }
 
+std::atomic<uint8_t> g_smem_set[kSmemSlots][kMaxDevices];
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool valid_wtype(int t) { return t == KQ_Q4_K || t == KQ_Q6_K; }
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
@@ -58,6 +61,18 @@ kq_status finish(cudaError_t e, int status) {
 }
 
 }  // namespace
+
+cudaError_t allow_max_smem(const void* kernel, int slot) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (slot < 0 || slot >= kSmemSlots || dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidValue;
+  if (g_smem_set[slot][dev].load(std::memory_order_acquire)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  if (e == cudaSuccess) g_smem_set[slot][dev].store(1, std::memory_order_release);
+  return e;
+}
+
 }  // namespace kq
 
 using namespace kq;

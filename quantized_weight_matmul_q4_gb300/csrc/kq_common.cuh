@@ -42,6 +42,26 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// Programmatic dependent launch: every kernel of the library is launched so
+// that it may start while the previous kernel in the stream drains. It first
+// lets its own dependents be scheduled, then waits until the previous grid has
+// completed and its memory is visible, before touching any global memory.
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// One lane of a converged warp (the same lane on every call) is elected.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "elect.sync _|P, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 __device__ __forceinline__ void report_error(int* err, int code) {
   if (err) atomicCAS(err, 0, code);
 }
@@ -62,14 +82,18 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                : "memory");
 }
+// The waiting thread is suspended (it does not spin on the issue slots) until
+// the phase completes or about 0.2 ms pass.
+constexpr uint32_t WAIT_SUSPEND_HINT_NS = 200000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "n"(WAIT_SUSPEND_HINT_NS)
       : "memory");
   return ok != 0;
 }
@@ -82,7 +106,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255) == 0) {
+    if ((it & 7) == 0) {
       if (*abort) return false;
       if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
         report_error(err, ERR_WAIT_TIMEOUT);

@@ -25,6 +25,8 @@
 // Tiles are statically strided over a persistent grid (one CTA per SM), so
 // results do not depend on scheduling; a split K range is summed afterwards in
 // a fixed order. Every wait is bounded (ERR_WAIT_TIMEOUT, no hang).
+#include <algorithm>
+
 #include "kq_internal.h"
 #include "kq_common.cuh"
 
@@ -62,7 +64,7 @@ struct GemmArgs {
   int N;            // token rows of x_hat
   int nb;           // super-blocks per weight row
   int m_tiles, n_tiles, splits, bn;
-  int ab_stages, raw_stages;
+  int a_stages, b_stages, raw_stages;
   int b_stage_bytes;
   float* Y;
   float* partial;   // split-K partial sums [splits][N][M]
@@ -236,15 +238,16 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
   constexpr int RAW_BYTES = RawBox<WT>::BYTES * GM_BM;
   uint8_t* sA = smem;
-  uint8_t* sB = sA + a.ab_stages * GM_A_BYTES;
-  uint8_t* sRaw = sB + a.ab_stages * a.b_stage_bytes;
+  uint8_t* sB = sA + a.a_stages * GM_A_BYTES;
+  uint8_t* sRaw = sB + a.b_stages * a.b_stage_bytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sRaw + a.raw_stages * RAW_BYTES);
   uint64_t* raw_full = bars;
   uint64_t* raw_empty = raw_full + a.raw_stages;
   uint64_t* a_full = raw_empty + a.raw_stages;
-  uint64_t* b_full = a_full + a.ab_stages;
-  uint64_t* ab_empty = b_full + a.ab_stages;
-  uint64_t* acc_full = ab_empty + a.ab_stages;
+  uint64_t* a_empty = a_full + a.a_stages;
+  uint64_t* b_full = a_empty + a.a_stages;
+  uint64_t* b_empty = b_full + a.b_stages;
+  uint64_t* acc_full = b_empty + a.b_stages;
   uint64_t* acc_empty = acc_full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -259,10 +262,13 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
       mbar_init(&raw_full[i], 1);
       mbar_init(&raw_empty[i], GM_DQ_WARPS);
     }
-    for (int i = 0; i < a.ab_stages; ++i) {
+    for (int i = 0; i < a.a_stages; ++i) {
       mbar_init(&a_full[i], GM_DQ_WARPS);
+      mbar_init(&a_empty[i], 1);
+    }
+    for (int i = 0; i < a.b_stages; ++i) {
       mbar_init(&b_full[i], 1);
-      mbar_init(&ab_empty[i], 1);
+      mbar_init(&b_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
@@ -279,6 +285,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmX);
   }
+  pdl_enter();
   int total_tiles;
   if (MOE) {
     for (int i = threadIdx.x; i <= a.n_experts; i += GM_THREADS) s_tile_start[i] = a.tile_start[i];
@@ -325,12 +332,12 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
         const int nbox = (T.ncols + GM_BBOX - 1) / GM_BBOX;
         for (int kb = T.kb0; kb < T.kb1 && !*abort; ++kb) {
           for (int s = 0; s < 4; ++s) {
-            if (!mbar_wait(&ab_empty[st], ph ^ 1, abort, a.err)) break;
+            if (!mbar_wait(&b_empty[st], ph ^ 1, abort, a.err)) break;
             mbar_expect_tx(&b_full[st], nbox * GM_BBOX_BYTES);
             for (int j = 0; j < nbox; ++j)
               tma_load_2d(sB + st * a.b_stage_bytes + j * GM_BBOX_BYTES, &tmX, &b_full[st],
                           kb * QK_K + s * GM_BK, T.xrow0 + j * GM_BBOX);
-            if (++st == a.ab_stages) {
+            if (++st == a.b_stages) {
               st = 0;
               ph ^= 1;
             }
@@ -340,41 +347,51 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
     }
   } else if (warp == GM_MMA_WARP) {
     // ---- tensor-core issuer --------------------------------------------------
-    if (lane == 0) {
-      int st = 0;
-      uint32_t ph = 0;
-      int it = 0;
-      for (int t = blockIdx.x; t < total_tiles && !*abort; t += gridDim.x, ++it) {
-        const Tile T = decode_tile<MOE>(a, t, s_tile_start, s_counts, s_offsets);
-        const int acc = it & 1;
-        if (!mbar_wait(&acc_empty[acc], ((it >> 1) & 1) ^ 1, abort, a.err)) break;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * GM_BNMAX;
-        const int n_mma = (T.ncols + 15) & ~15;
-        const uint32_t idesc = idesc_f16_f32(GM_BM, n_mma);
-        bool first = true;
-        for (int kb = T.kb0; kb < T.kb1 && !*abort; ++kb) {
-          for (int s = 0; s < 4; ++s) {
-            if (!mbar_wait(&a_full[st], ph, abort, a.err)) break;
-            if (!mbar_wait(&b_full[st], ph, abort, a.err)) break;
-            tc_fence_after();
-            const uint64_t ad = smem_desc_sw128(smem_u32(sA + st * GM_A_BYTES));
-            const uint64_t bd = smem_desc_sw128(smem_u32(sB + st * a.b_stage_bytes));
-#pragma unroll
-            for (int k = 0; k < GM_BK / 16; ++k) {
-              // +32 bytes per K=16 step inside the 128-byte swizzled row
-              umma_f16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (first && k == 0) ? 0u : 1u);
-            }
-            first = false;
-            umma_commit(&ab_empty[st]);
-            if (++st == a.ab_stages) {
-              st = 0;
-              ph ^= 1;
-            }
-          }
+    // The whole warp runs the loop converged, so descriptors and counters stay
+    // warp-uniform; one elected lane issues the MMAs and commits.
+    int ast = 0, bst = 0;
+    uint32_t aph = 0, bph = 0;
+    int it = 0;
+    const uint64_t a_desc0 = smem_desc_sw128(smem_u32(sA));
+    const uint64_t b_desc0 = smem_desc_sw128(smem_u32(sB));
+    for (int t = blockIdx.x; t < total_tiles && !*abort; t += gridDim.x, ++it) {
+      const Tile T = decode_tile<MOE>(a, t, s_tile_start, s_counts, s_offsets);
+      const int acc = it & 1;
+      if (!mbar_wait(&acc_empty[acc], ((it >> 1) & 1) ^ 1, abort, a.err)) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * GM_BNMAX;
+      const uint32_t idesc = idesc_f16_f32(GM_BM, (T.ncols + 15) & ~15);
+      const int nsteps = (T.kb1 - T.kb0) * 4;
+      bool ok = true;
+      for (int ks = 0; ks < nsteps; ++ks) {
+        if (!mbar_wait(&a_full[ast], aph, abort, a.err) || !mbar_wait(&b_full[bst], bph, abort, a.err)) {
+          ok = false;
+          break;
         }
-        umma_commit(&acc_full[acc]);
+        tc_fence_after();
+        // start address field advances by bytes / 16
+        const uint64_t ad = a_desc0 + static_cast<uint64_t>((ast * GM_A_BYTES) >> 4);
+        const uint64_t bd = b_desc0 + static_cast<uint64_t>((bst * a.b_stage_bytes) >> 4);
+        if (elect_one()) {
+#pragma unroll
+          for (int k = 0; k < GM_BK / 16; ++k)  // +32 bytes per K=16 step inside the 128-byte row
+            umma_f16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (ks == 0 && k == 0) ? 0u : 1u);
+          umma_commit(&a_empty[ast]);
+          umma_commit(&b_empty[bst]);
+        }
+        __syncwarp();
+        if (++ast == a.a_stages) {
+          ast = 0;
+          aph ^= 1;
+        }
+        if (++bst == a.b_stages) {
+          bst = 0;
+          bph ^= 1;
+        }
       }
+      if (elect_one()) umma_commit(&acc_full[acc]);
+      __syncwarp();
+      if (!ok) break;
     }
   } else if (warp < GM_DQ_WARPS) {
     // ---- weight unpackers ----------------------------------------------------
@@ -387,7 +404,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
         if (!mbar_wait(&raw_full[rst], rph, abort, a.err)) break;
         const uint8_t* raw = sRaw + rst * RAW_BYTES;
         for (int s = 0; s < 4; ++s) {
-          if (!mbar_wait(&ab_empty[ast], aph ^ 1, abort, a.err)) break;
+          if (!mbar_wait(&a_empty[ast], aph ^ 1, abort, a.err)) break;
           uint8_t* at = sA + ast * GM_A_BYTES;
           if (WT == KQ_Q4_K)
             dequant_q4k(raw, s, at, tid);
@@ -396,7 +413,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(&a_full[ast]);
-          if (++ast == a.ab_stages) {
+          if (++ast == a.a_stages) {
             ast = 0;
             aph ^= 1;
           }
@@ -457,6 +474,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
 // Fixed-order sum of the split-K partials: Y[i] = Sum_s P[s][i] (n elements).
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restrict__ P, float* __restrict__ Y,
                                                             int64_t n, int splits) {
+  pdl_enter();
   const int64_t i4 = (static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x) * 4;
   if (i4 >= n) return;
   if (i4 + 4 <= n && (n & 3) == 0) {
@@ -521,21 +539,32 @@ __global__ void __launch_bounds__(1024) moe_route_kernel(const int* __restrict__
   int* cnt = rsm;                 // [32][E]: per-warp counts, then per-warp bases
   int* base = cnt + 32 * E;       // [E]: bucket start
   int* wsum = base + E;           // [32]
+  pdl_enter();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < 32 * E; i += 1024) cnt[i] = 0;
   __syncthreads();
   const int L = (((n + 31) / 32) + 31) & ~31;
   const int lo = min(n, warp * L), hi = min(n, lo + L);
-  for (int b0 = lo; b0 < hi; b0 += 32) {
-    const int i = b0 + lane;
-    int e = (i < hi) ? __ldg(ids + i) : -1;
-    if (i < hi && (e < 0 || e >= E)) {
-      report_error(err, ERR_EXPERT_ID);
-      e = -1;
+  // pass 1: per-warp counts; ids are fetched 8 per lane at a time so the loads overlap
+  for (int r0 = lo; r0 < hi; r0 += 256) {
+    int e[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = r0 + 32 * j + lane;
+      e[j] = (i < hi) ? __ldg(ids + i) : -1;
     }
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
-    if (e >= 0 && lane == __ffs(peers) - 1) cnt[warp * E + e] += __popc(peers);
-    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = r0 + 32 * j + lane;
+      int ej = e[j];
+      if (i < hi && (ej < 0 || ej >= E)) {
+        report_error(err, ERR_EXPERT_ID);
+        ej = -1;
+      }
+      const unsigned peers = __match_any_sync(0xffffffffu, ej);
+      if (ej >= 0 && lane == __ffs(peers) - 1) cnt[warp * E + ej] += __popc(peers);
+      __syncwarp();
+    }
   }
   __syncthreads();
   int tot = 0;
@@ -562,23 +591,33 @@ __global__ void __launch_bounds__(1024) moe_route_kernel(const int* __restrict__
     tile_start[E] = n_tiles;
   }
   __syncthreads();
+  // pass 2: scatter in (token, slot) order
   const unsigned lt = (1u << lane) - 1u;
-  for (int b0 = lo; b0 < hi; b0 += 32) {
-    const int i = b0 + lane;
-    int e = (i < hi) ? __ldg(ids + i) : -1;
-    const bool bad = (i < hi) && (e < 0 || e >= E);
-    if (bad) e = -1;
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
-    if (e >= 0) {
-      const int pos = base[e] + cnt[warp * E + e] + __popc(peers & lt);
-      entries[pos] = i;
-      src[pos] = i / top_k;
+  for (int r0 = lo; r0 < hi; r0 += 256) {
+    int e[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = r0 + 32 * j + lane;
+      e[j] = (i < hi) ? __ldg(ids + i) : -1;
     }
-    __syncwarp();
-    if (e >= 0 && lane == __ffs(peers) - 1) cnt[warp * E + e] += __popc(peers);
-    __syncwarp();
-    if (bad)
-      for (int m = 0; m < M; ++m) Y[static_cast<int64_t>(i) * M + m] = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = r0 + 32 * j + lane;
+      int ej = e[j];
+      const bool bad = (i < hi) && (ej < 0 || ej >= E);
+      if (bad) ej = -1;
+      const unsigned peers = __match_any_sync(0xffffffffu, ej);
+      if (ej >= 0) {
+        const int pos = base[ej] + cnt[warp * E + ej] + __popc(peers & lt);
+        entries[pos] = i;
+        src[pos] = i / top_k;
+      }
+      __syncwarp();
+      if (ej >= 0 && lane == __ffs(peers) - 1) cnt[warp * E + ej] += __popc(peers);
+      __syncwarp();
+      if (bad)
+        for (int m = 0; m < M; ++m) Y[static_cast<int64_t>(i) * M + m] = 0.f;
+    }
   }
   for (int p = n_valid + threadIdx.x; p < n; p += 1024) src[p] = -1;
 }
@@ -615,25 +654,40 @@ bool encode_tmap_2d(CUtensorMap* tm, CUtensorMapDataType dtype, const void* base
 
 static int raw_box_bytes(int wtype) { return wtype == KQ_Q4_K ? RawBox<KQ_Q4_K>::BYTES : RawBox<KQ_Q6_K>::BYTES; }
 
-// Ring depths for a token tile of bn rows: 3-4 A/B stages, then as many raw
-// weight stages (2..8) as the remaining shared memory holds.
+// Ring depths for a token tile of bn rows. The x_hat (B) ring comes first: its
+// TMA round trip (L2 -> shared memory, 1-2k cycles) must be covered by the MMA
+// time of the stages in flight, which at bn = 256 takes four 64-K stages. Then
+// three A stages (weights unpacked by the CUDA cores) and up to four raw weight
+// super-blocks (each feeds four K steps; they come from HBM). Whatever shared
+// memory is left deepens the A and B rings.
 static bool choose_stages(int wtype, int bn, int n_experts, GemmArgs* a, size_t* smem) {
   const int b_bytes = ((bn + GM_BBOX - 1) / GM_BBOX) * GM_BBOX_BYTES;
   const int raw_bytes = raw_box_bytes(wtype) * GM_BM;
-  const int tables = (MOE_MAX_EXPERTS >= n_experts ? 3 * (n_experts + 1) * 4 : 0) + 64;
-  for (int ab = 4; ab >= 2; --ab) {
-    const int fixed = 1024 + ab * (GM_A_BYTES + b_bytes) + tables + 256;
-    int raw = (GM_SMEM_LIMIT - fixed) / raw_bytes;
-    if (raw > 8) raw = 8;
-    if (raw >= 2 && (ab < 4 || raw >= 4)) {
-      a->ab_stages = ab;
-      a->raw_stages = raw;
-      a->b_stage_bytes = b_bytes;
-      *smem = static_cast<size_t>(fixed + raw * raw_bytes);
-      return true;
+  const int tables = (n_experts > 0 ? 3 * (n_experts + 1) * 4 : 0) + 64;
+  const int budget = GM_SMEM_LIMIT - (1024 + tables + 512);
+  auto bytes = [&](int bs, int as, int rs) { return bs * b_bytes + as * GM_A_BYTES + rs * raw_bytes; };
+  int bs = 4, as = 3, rs = 2;
+  while (bs > 2 && bytes(bs, as, rs) > budget) --bs;
+  if (bytes(bs, as, rs) > budget) as = 2;
+  if (bytes(bs, as, rs) > budget) return false;
+  while (rs < 4 && bytes(bs, as, rs + 1) <= budget) ++rs;
+  for (bool grew = true; grew;) {
+    grew = false;
+    if (as < 6 && bytes(bs, as + 1, rs) <= budget) {
+      ++as;
+      grew = true;
+    }
+    if (bs < 8 && bytes(bs + 1, as, rs) <= budget) {
+      ++bs;
+      grew = true;
     }
   }
-  return false;
+  a->b_stages = bs;
+  a->a_stages = as;
+  a->raw_stages = rs;
+  a->b_stage_bytes = b_bytes;
+  *smem = static_cast<size_t>(bytes(bs, as, rs) + 1024 + tables + 512);
+  return true;
 }
 
 GemmPlan plan_gemm(int wtype, int64_t M, int64_t K, int64_t N, int num_sms) {
@@ -663,11 +717,9 @@ GemmPlan plan_gemm(int wtype, int64_t M, int64_t K, int64_t N, int num_sms) {
 template <int WT, bool MOE>
 static cudaError_t launch_kernel(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmArgs& a, int grid,
                                  size_t smem, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(kq_gemm_kernel<WT, MOE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(kq_gemm_kernel<WT, MOE>), 2 + 2 * WT + (MOE ? 1 : 0));
   if (e != cudaSuccess) return e;
-  kq_gemm_kernel<WT, MOE><<<grid, GM_THREADS, smem, s>>>(tmW, tmX, a);
-  return cudaGetLastError();
+  return launch_pdl(kq_gemm_kernel<WT, MOE>, dim3(grid), dim3(GM_THREADS), smem, s, tmW, tmX, a);
 }
 
 static cudaError_t dispatch(int wtype, bool moe, const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmArgs& a,
@@ -727,8 +779,8 @@ cudaError_t launch_gemm(int wtype, const void* W, const float* X, float* Y, int6
   if (plan.splits > 1) {
     const int64_t n = N * M;
     const int64_t threads = (n + 3) / 4;
-    splitk_reduce_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(partial, Y, n, plan.splits);
-    e = cudaGetLastError();
+    e = launch_pdl(splitk_reduce_kernel, dim3(static_cast<unsigned>((threads + 255) / 256)), dim3(256), 0, s,
+                   partial, Y, n, plan.splits);
   }
   return e;
 }
@@ -776,12 +828,10 @@ cudaError_t launch_moe(int wtype, const void* W, int n_experts, const int32_t* i
   const int64_t n = T * top_k;
 
   const size_t rsmem = static_cast<size_t>(32 * n_experts + n_experts + 32) * sizeof(int);
-  cudaError_t e = cudaFuncSetAttribute(moe_route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(rsmem));
+  cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(moe_route_kernel), 8);
   if (e != cudaSuccess) return e;
-  moe_route_kernel<<<1, 1024, rsmem, s>>>(ids, static_cast<int>(n), top_k, n_experts, plan.m_tiles, MOE_BN, counts,
-                                          offsets, tile_start, entries, src, Y, static_cast<int>(M), err);
-  e = cudaGetLastError();
+  e = launch_pdl(moe_route_kernel, dim3(1), dim3(1024), rsmem, s, ids, static_cast<int>(n), top_k, n_experts,
+                 plan.m_tiles, MOE_BN, counts, offsets, tile_start, entries, src, Y, static_cast<int>(M), err);
   if (e != cudaSuccess) return e;
   e = launch_quantize_xhat(X, xh, K, n, src, s);
   if (e != cudaSuccess) return e;

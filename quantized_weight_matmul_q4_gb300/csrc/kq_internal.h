@@ -6,7 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/kq.h"
+#include "kq.h"
 
 namespace kq {
 
@@ -34,6 +34,29 @@ MoePlan plan_moe(int wtype, int64_t M, int64_t K, int64_t T, int n_experts, int 
 cudaError_t launch_moe(int wtype, const void* W, int n_experts, const int32_t* ids, int top_k, const float* X,
                        float* Y, int64_t M, int64_t K, int64_t T, void* ws, const MoePlan& plan, int* err,
                        int num_sms, cudaStream_t s, int* status);
+
+// Raises a kernel's dynamic shared-memory limit to the 227 KB maximum, once per
+// device (later calls only read a flag, so launches stay cheap and capturable).
+cudaError_t allow_max_smem(const void* kernel, int slot);
+constexpr int kSmemSlots = 16;
+
+// Launches `kernel` on `s` with programmatic stream serialization allowed (the
+// kernel calls pdl_enter() before its first global memory access).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 // Builds a 2-D tiled tensor map through the driver entry point.
 bool encode_tmap_2d(CUtensorMap* tm, CUtensorMapDataType dtype, const void* base, uint64_t dim0, uint64_t dim1,

@@ -9,92 +9,86 @@
 // reduction per row. The page's launch geometry (one 256-thread block per row,
 // plain loads) was made for a 273 GB/s LPDDR part; here the rows of the
 // row-major matrix are contiguous, so each CTA owns a balanced contiguous range
-// of rows and streams it through a shared-memory ring with 1-D bulk copies
-// (one elected producer thread, mbarrier completion). Every byte of W is read
-// from HBM once, in large coalesced transfers, with up to ~200 KB per SM in
-// flight; the consumer warps quantise x into shared memory while the first
-// copies land, then each warp reduces one row (or a share of one row).
+// of rows and streams it through a shared-memory ring of ~16 KB chunks with 1-D
+// bulk copies (one elected producer thread, mbarrier completion): every byte of
+// W is read from HBM once, and at the decode sizes a CTA's whole range is in
+// flight within the first microsecond. The consumer threads quantise x into
+// shared memory while the first chunks land; then each thread takes whole
+// super-blocks (row, block) in arrival order, so a block's header is decoded
+// once for its 256 weights, and writes one partial sum per block; each row's
+// partials are added in a fixed order at the end (deterministic).
+#include <algorithm>
+
 #include "kq_internal.h"
 #include "kq_quant.cuh"
 
 namespace kq {
 
 constexpr int MV_CWARPS = 16;                       // consumer warps
-constexpr int MV_THREADS = (MV_CWARPS + 1) * 32;    // + one producer warp
+constexpr int MV_CTHREADS = MV_CWARPS * 32;
+constexpr int MV_THREADS = MV_CTHREADS + 32;        // + one producer warp
 constexpr int MV_SMEM_LIMIT = 227 * 1024;
-constexpr int MV_STAGE_LIMIT = 100 * 1024;          // largest ring stage (two must fit)
+constexpr int MV_PART_MAX = 4096;                   // block partials per row group
+constexpr int MV_CHUNK_BLOCKS_Q4K = 112;            // 16128 B per chunk
+constexpr int MV_CHUNK_BLOCKS_Q6K = 80;             // 16800 B per chunk
+constexpr int MV_MAX_RING = 14;
 
 struct MatvecParams {
   const uint8_t* W;
   const float* x;
   float* y;
   int M, K, nb;
+  int bb;               // bytes per block (144 or 210)
   int rs;               // bytes per weight row
   int unit_rows;        // CTA row ranges start at multiples of this (16-byte aligned copies)
   int n_units;          // ceil(M / unit_rows)
-  int stage_rows;       // rows per ring stage
-  int warps_per_row;    // MV_CWARPS / stage_rows
-  int n_ring;           // ring depth (stages)
-  int stage_bytes;      // bytes per ring slot (multiple of 128)
-  int xq_bytes;         // bytes reserved for the int8 activation codes
-  int xds_bytes;        // bytes reserved for the per-32 (d8, d8*Sum q) pairs
+  int chunk_blocks;     // blocks per ring chunk
+  int chunk_bytes;      // chunk_blocks * bb (a multiple of 16)
+  int slot_bytes;       // ring slot stride (multiple of 128)
+  int n_ring;           // ring depth (chunks)
+  int rows_per_group;   // rows whose block partials are reduced together
+  int xq_bytes;         // int8 activation codes (block-swizzled 16-byte pieces)
+  int xds_bytes;        // per-32 activation scales and sums
   int* err;
 };
 
-// Position of activation k inside the shared int8 buffer. For Q4_K the four
-// 16-byte pieces of every 64-element group (block b, chunk c) are permuted by
-// h = 2(b&1) + (c>>1) so that the eight lanes of a 128-bit load phase, which
-// read (two blocks) x (four chunks) at the same piece, hit distinct banks.
-template <int WT>
-__device__ __forceinline__ int xq_offset(int k) {
-  if (WT == KQ_Q4_K) {
-    const int b = k >> 8, c = (k >> 6) & 3, v = (k >> 4) & 3;
-    const int h = ((b & 1) << 1) | (c >> 1);
-    return (b << 8) | (c << 6) | ((v ^ h) << 4) | (k & 15);
-  }
-  return k;
-}
+// Activation codes live in 16-byte pieces; piece j (0..15) of K-block b is
+// stored at piece j ^ (b & 7). Threads that read the same piece of eight
+// consecutive blocks hit eight different bank groups.
+__device__ __forceinline__ int xq_piece(int b, int j) { return (b << 8) + ((j ^ (b & 7)) << 4); }
 
-// One lane's share of a Q4_K row: units (block, 32-byte chunk c) with
-// u = first, first + stride, ... Chunk c of a block holds sub-block 2c in its
-// low nibbles and sub-block 2c+1 in its high nibbles.
-__device__ __forceinline__ float row_dot_q4k(const uint8_t* __restrict__ rowp, const uint8_t* __restrict__ xq,
-                                             const float2* __restrict__ xds, int n_units, int first, int stride) {
-  float acc = 0.f;
-  const int c = first & 3;  // stride is a multiple of 4, so c is fixed per lane
-  const int sh = (c & 1) * 16;
-  for (int u = first; u < n_units; u += stride) {
-    const int b = u >> 2;
-    const uint8_t* blk = rowp + b * Q4K_BYTES;
-    const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
+// Q4_K: per (block b, 32-byte chunk c) one int4 {d8 of sub 2c, d8 of sub 2c+1,
+// Sum q of sub 2c, Sum q of sub 2c+1}, stored at 4b + (c ^ ((b >> 1) & 3)).
+__device__ __forceinline__ int xds_q4k(int b, int c) { return 4 * b + (c ^ ((b >> 1) & 3)); }
+// Q6_K: per 32-block g8 (0..7) of block b one int4 {d8, Sum q of the first 16,
+// Sum q of the last 16, 0}, stored at 8b + (g8 ^ (b & 7)).
+__device__ __forceinline__ int xds_q6k(int b, int g8) { return 8 * b + (g8 ^ (b & 7)); }
+
+__device__ __forceinline__ float i2f(int v) { return static_cast<float>(v); }
+
+// Sum over one Q4_K super-block (256 weights) of w * x_hat, by the min-term
+// identity: d * Sum_sub d8*sc*dot(nib, q) - dmin * Sum_sub d8*m*Sum(q).
+__device__ __forceinline__ float block_dot_q4k(const uint8_t* __restrict__ blk, int b, const uint8_t* __restrict__ xq,
+                                               const int4* __restrict__ xds) {
+  const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
+  const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x & 0xFFFFu)));
+  const float dmin = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x >> 16)));
+  // 6-bit scales and mins, one per byte: sub-blocks 0..3 and 4..7
+  const uint32_t sc_lo = hdr.y & 0x3F3F3F3Fu, m_lo = hdr.z & 0x3F3F3F3Fu;
+  const uint32_t sc_hi = (hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u);
+  const uint32_t m_hi = ((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u);
+  float acc_lo = 0.f, acc_hi = 0.f, acc_m = 0.f;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
     const uint4 qa = *reinterpret_cast<const uint4*>(blk + 16 + 32 * c);
     const uint4 qb = *reinterpret_cast<const uint4*>(blk + 32 + 32 * c);
-    const int h = ((b & 1) << 1) | (c >> 1);
-    const uint8_t* xb = xq + (b << 8) + (c << 6);
-    const int4 x0 = *reinterpret_cast<const int4*>(xb + ((0 ^ h) << 4));
-    const int4 x1 = *reinterpret_cast<const int4*>(xb + ((1 ^ h) << 4));
-    const int4 x2 = *reinterpret_cast<const int4*>(xb + ((2 ^ h) << 4));
-    const int4 x3 = *reinterpret_cast<const int4*>(xb + ((3 ^ h) << 4));
-    const float4 ds = *reinterpret_cast<const float4*>(xds + 8 * b + 2 * c);  // d8A, sA, d8B, sB
-
-    const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x & 0xFFFFu)));
-    const float dmin = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x >> 16)));
-    // 6-bit scales/mins of sub-blocks 0..3 (c < 2) or 4..7 (c >= 2), one per byte.
-    uint32_t scw, mw;
-    if (c < 2) {
-      scw = hdr.y & 0x3F3F3F3Fu;
-      mw = hdr.z & 0x3F3F3F3Fu;
-    } else {
-      scw = (hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u);
-      mw = ((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u);
-    }
-    const float scA = static_cast<float>((scw >> sh) & 0xFFu);
-    const float scB = static_cast<float>((scw >> (sh + 8)) & 0xFFu);
-    const float mA = static_cast<float>((mw >> sh) & 0xFFu);
-    const float mB = static_cast<float>((mw >> (sh + 8)) & 0xFFu);
-
-    int dA = 0, dB = 0;
-    dA = __dp4a(static_cast<int>(qa.x & 0x0F0F0F0Fu), x0.x, dA);
+    const int4 x0 = *reinterpret_cast<const int4*>(xq + xq_piece(b, 4 * c + 0));
+    const int4 x1 = *reinterpret_cast<const int4*>(xq + xq_piece(b, 4 * c + 1));
+    const int4 x2 = *reinterpret_cast<const int4*>(xq + xq_piece(b, 4 * c + 2));
+    const int4 x3 = *reinterpret_cast<const int4*>(xq + xq_piece(b, 4 * c + 3));
+    const int4 ds = xds[xds_q4k(b, c)];
+    // sub-block 2c: low nibbles against elements 0..31 of the chunk
+    int dA = __dp4a(static_cast<int>(qa.x & 0x0F0F0F0Fu), x0.x, 0);
     dA = __dp4a(static_cast<int>(qa.y & 0x0F0F0F0Fu), x0.y, dA);
     dA = __dp4a(static_cast<int>(qa.z & 0x0F0F0F0Fu), x0.z, dA);
     dA = __dp4a(static_cast<int>(qa.w & 0x0F0F0F0Fu), x0.w, dA);
@@ -102,171 +96,408 @@ __device__ __forceinline__ float row_dot_q4k(const uint8_t* __restrict__ rowp, c
     dA = __dp4a(static_cast<int>(qb.y & 0x0F0F0F0Fu), x1.y, dA);
     dA = __dp4a(static_cast<int>(qb.z & 0x0F0F0F0Fu), x1.z, dA);
     dA = __dp4a(static_cast<int>(qb.w & 0x0F0F0F0Fu), x1.w, dA);
-    dB = __dp4a(static_cast<int>((qa.x >> 4) & 0x0F0F0F0Fu), x2.x, dB);
-    dB = __dp4a(static_cast<int>((qa.y >> 4) & 0x0F0F0F0Fu), x2.y, dB);
-    dB = __dp4a(static_cast<int>((qa.z >> 4) & 0x0F0F0F0Fu), x2.z, dB);
-    dB = __dp4a(static_cast<int>((qa.w >> 4) & 0x0F0F0F0Fu), x2.w, dB);
-    dB = __dp4a(static_cast<int>((qb.x >> 4) & 0x0F0F0F0Fu), x3.x, dB);
-    dB = __dp4a(static_cast<int>((qb.y >> 4) & 0x0F0F0F0Fu), x3.y, dB);
-    dB = __dp4a(static_cast<int>((qb.z >> 4) & 0x0F0F0F0Fu), x3.z, dB);
-    dB = __dp4a(static_cast<int>((qb.w >> 4) & 0x0F0F0F0Fu), x3.w, dB);
-
-    acc = fmaf(ds.x * (d * scA), static_cast<float>(dA), acc);
-    acc = fmaf(-(dmin * mA), ds.y, acc);
-    acc = fmaf(ds.z * (d * scB), static_cast<float>(dB), acc);
-    acc = fmaf(-(dmin * mB), ds.w, acc);
+    // sub-block 2c+1: high nibbles kept in place (16 x nibble), against 32..63
+    int dB = dp4a_us(qa.x & 0xF0F0F0F0u, x2.x, 0);
+    dB = dp4a_us(qa.y & 0xF0F0F0F0u, x2.y, dB);
+    dB = dp4a_us(qa.z & 0xF0F0F0F0u, x2.z, dB);
+    dB = dp4a_us(qa.w & 0xF0F0F0F0u, x2.w, dB);
+    dB = dp4a_us(qb.x & 0xF0F0F0F0u, x3.x, dB);
+    dB = dp4a_us(qb.y & 0xF0F0F0F0u, x3.y, dB);
+    dB = dp4a_us(qb.z & 0xF0F0F0F0u, x3.z, dB);
+    dB = dp4a_us(qb.w & 0xF0F0F0F0u, x3.w, dB);
+    const uint32_t scw = (c < 2) ? sc_lo : sc_hi;
+    const uint32_t mw = (c < 2) ? m_lo : m_hi;
+    const int sh = (c & 1) * 16;
+    const int scA = (scw >> sh) & 0xFF, scB = (scw >> (sh + 8)) & 0xFF;
+    const int mA = (mw >> sh) & 0xFF, mB = (mw >> (sh + 8)) & 0xFF;
+    const float d8A = __int_as_float(ds.x), d8B = __int_as_float(ds.y);
+    acc_lo = fmaf(d8A, i2f(scA * dA), acc_lo);
+    acc_hi = fmaf(d8B, i2f(scB * dB), acc_hi);
+    acc_m = fmaf(d8A, i2f(mA * ds.z), acc_m);
+    acc_m = fmaf(d8B, i2f(mB * ds.w), acc_m);
   }
-  return acc;
+  return d * fmaf(acc_hi, 0.0625f, acc_lo) - dmin * acc_m;
 }
 
-__device__ __forceinline__ uint32_t ld_u32_a2(const uint8_t* p) {  // 2-byte aligned 32-bit load
+// Four bytes from a 2-byte aligned shared address, as one 32-bit word.
+__device__ __forceinline__ uint32_t ld_u32_a2(const uint8_t* p) {
   const uint16_t* q = reinterpret_cast<const uint16_t*>(p);
   return static_cast<uint32_t>(q[0]) | (static_cast<uint32_t>(q[1]) << 16);
 }
 
-// One lane's share of a Q6_K row: units (block, half h, r-range of 8); unit
-// covers weights 128h + 32g + r for g = 0..3 and r in [8*qr, 8*qr + 8).
-__device__ __forceinline__ float row_dot_q6k(const uint8_t* __restrict__ rowp, const uint8_t* __restrict__ xq,
-                                             const float2* __restrict__ xds, int n_units, int first, int stride) {
+// Sum over one Q6_K super-block of w * x_hat, w = d * sc * (q - 32), taken as
+// d * Sum_16 sc * d8 * (dot(q, x) - 32 * Sum x) per group of 16 weights.
+__device__ __forceinline__ float block_dot_q6k(const uint8_t* __restrict__ blk, int b, const uint8_t* __restrict__ xq,
+                                               const int4* __restrict__ xds) {
+  const float d = __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short*>(blk + 208)));
   float acc = 0.f;
-  for (int u = first; u < n_units; u += stride) {
-    const int b = u >> 3, h = (u >> 2) & 1, qr = u & 3;
-    const uint8_t* blk = rowp + b * Q6K_BYTES;
-    const uint8_t* pa = blk + 64 * h + 8 * qr;       // ql, quarters g = 0 (low) and 2 (high)
-    const uint8_t* pb = pa + 32;                     // ql, quarters g = 1 (low) and 3 (high)
-    const uint8_t* ph = blk + 128 + 32 * h + 8 * qr; // qh, two bits per quarter
-    const uint32_t a0 = ld_u32_a2(pa), a1 = ld_u32_a2(pa + 4);
-    const uint32_t b0 = ld_u32_a2(pb), b1 = ld_u32_a2(pb + 4);
-    const uint32_t h0 = ld_u32_a2(ph), h1 = ld_u32_a2(ph + 4);
-    const float d = __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short*>(blk + 208)));
-    const int8_t* sc = reinterpret_cast<const int8_t*>(blk + 192 + 8 * h + (qr >> 1));
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
-      const uint32_t s0 = (g & 1) ? b0 : a0, s1 = (g & 1) ? b1 : a1;
-      const uint32_t l0 = (g < 2) ? (s0 & 0x0F0F0F0Fu) : ((s0 >> 4) & 0x0F0F0F0Fu);
-      const uint32_t l1 = (g < 2) ? (s1 & 0x0F0F0F0Fu) : ((s1 >> 4) & 0x0F0F0F0Fu);
-      const uint32_t q0 = l0 | (((h0 >> (2 * g)) & 0x03030303u) << 4);
-      const uint32_t q1 = l1 | (((h1 >> (2 * g)) & 0x03030303u) << 4);
-      const int k = (b << 8) + 128 * h + 32 * g + 8 * qr;
-      const int2 xw = *reinterpret_cast<const int2*>(xq + k);
-      int dot = dp4a_us(q0, xw.x, 0);
-      dot = dp4a_us(q1, xw.y, dot);
-      int sx = __dp4a(0x01010101, xw.x, 0);
-      sx = __dp4a(0x01010101, xw.y, sx);
-      const float d8 = xds[k >> 5].x;
-      acc = fmaf(d * static_cast<float>(sc[2 * g]) * d8, static_cast<float>(dot - 32 * sx), acc);
+      const uint8_t* ql = blk + 64 * h + 32 * (g & 1);
+      const uint8_t* qh = blk + 128 + 32 * h;
+      const int g8 = 4 * h + g;                    // 32-weight group inside the block
+      const int4 xa = *reinterpret_cast<const int4*>(xq + xq_piece(b, 2 * g8));
+      const int4 xb = *reinterpret_cast<const int4*>(xq + xq_piece(b, 2 * g8 + 1));
+      const int xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+      int dot0 = 0, dot1 = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t l = ld_u32_a2(ql + 4 * i);
+        const uint32_t hb = ld_u32_a2(qh + 4 * i);
+        const uint32_t lo = (g < 2) ? (l & 0x0F0F0F0Fu) : ((l >> 4) & 0x0F0F0F0Fu);
+        const uint32_t q = lo | (((hb >> (2 * g)) & 0x03030303u) << 4);
+        if (i < 4)
+          dot0 = dp4a_us(q, xv[i], dot0);
+        else
+          dot1 = dp4a_us(q, xv[i], dot1);
+      }
+      const int4 ds = xds[xds_q6k(b, g8)];
+      const int sc0 = static_cast<int>(reinterpret_cast<const int8_t*>(blk)[192 + 8 * h + 2 * g]);
+      const int sc1 = static_cast<int>(reinterpret_cast<const int8_t*>(blk)[192 + 8 * h + 2 * g + 1]);
+      const int t = sc0 * (dot0 - 32 * ds.y) + sc1 * (dot1 - 32 * ds.z);
+      acc = fmaf(__int_as_float(ds.x), i2f(t), acc);
     }
   }
-  return acc;
+  return d * acc;
 }
 
 template <int WT>
 __global__ void __launch_bounds__(MV_THREADS, 1) matvec_kernel(const MatvecParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* xq = smem;
-  float2* xds = reinterpret_cast<float2*>(smem + p.xq_bytes);
-  uint8_t* ring = smem + p.xq_bytes + p.xds_bytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(ring + static_cast<size_t>(p.n_ring) * p.stage_bytes);
+  int4* xds = reinterpret_cast<int4*>(smem + p.xq_bytes);
+  float* part = reinterpret_cast<float*>(smem + p.xq_bytes + p.xds_bytes);
+  uint8_t* ring = reinterpret_cast<uint8_t*>(part + MV_PART_MAX);
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + static_cast<size_t>(p.n_ring) * p.slot_bytes);
   uint64_t* empty = full + p.n_ring;
-  float* red = reinterpret_cast<float*>(empty + p.n_ring);  // [MV_CWARPS] partial row sums
-  volatile int* abort = reinterpret_cast<volatile int*>(red + MV_CWARPS);
+  volatile int* abort = reinterpret_cast<volatile int*>(empty + p.n_ring);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t u0 = static_cast<int64_t>(blockIdx.x) * p.n_units / gridDim.x;
   const int64_t u1 = static_cast<int64_t>(blockIdx.x + 1) * p.n_units / gridDim.x;
   const int r0 = static_cast<int>(u0 * p.unit_rows);
   const int r1 = static_cast<int>(min(static_cast<int64_t>(p.M), u1 * p.unit_rows));
-  const int n_stages = (r1 - r0 + p.stage_rows - 1) / p.stage_rows;
+  const int n_items = (r1 - r0) * p.nb;                 // (row, block) pairs of this CTA
+  const int n_chunks = (n_items + p.chunk_blocks - 1) / p.chunk_blocks;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < p.n_ring; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], MV_CWARPS);
+      mbar_init(&empty[i], p.chunk_blocks);
     }
     *abort = 0;
     fence_mbar_init();
   }
+  pdl_enter();
   __syncthreads();
 
   if (warp == MV_CWARPS) {
-    // Producer: stream this CTA's rows, stage by stage, through the ring.
+    // Producer: the CTA's contiguous byte range, chunk by chunk, through the ring.
     if (lane == 0) {
-      for (int s = 0; s < n_stages; ++s) {
-        const int slot = s % p.n_ring;
-        const uint32_t ph = (s / p.n_ring) & 1;
-        if (!mbar_wait(&empty[slot], ph ^ 1, abort, p.err)) break;
-        const int row_a = r0 + s * p.stage_rows;
-        const int rows = min(p.stage_rows, r1 - row_a);
-        const uint32_t bytes = static_cast<uint32_t>(rows) * p.rs;
+      const uint8_t* base = p.W + static_cast<int64_t>(r0) * p.rs;
+      const int64_t total = static_cast<int64_t>(n_items) * p.bb;
+      for (int c = 0; c < n_chunks; ++c) {
+        const int slot = c % p.n_ring;
+        if (c >= p.n_ring && !mbar_wait(&empty[slot], ((c / p.n_ring) & 1) ^ 1, abort, p.err)) break;
+        const int64_t off = static_cast<int64_t>(c) * p.chunk_bytes;
+        const uint32_t bytes = static_cast<uint32_t>(min(static_cast<int64_t>(p.chunk_bytes), total - off));
         const uint32_t main_bytes = bytes & ~15u;
-        const uint8_t* src = p.W + static_cast<int64_t>(row_a) * p.rs;
-        uint8_t* dst = ring + static_cast<size_t>(slot) * p.stage_bytes;
-        for (uint32_t i = main_bytes; i < bytes; ++i) dst[i] = src[i];  // ragged end of W (< 16 bytes)
+        uint8_t* dst = ring + static_cast<size_t>(slot) * p.slot_bytes;
+        for (uint32_t i = main_bytes; i < bytes; ++i) dst[i] = base[off + i];  // ragged end of W (< 16 B)
         mbar_expect_tx(&full[slot], main_bytes);
-        if (main_bytes) bulk_g2s(dst, src, main_bytes, &full[slot]);
+        if (main_bytes) bulk_g2s(dst, base + off, main_bytes, &full[slot]);
       }
     }
     return;
   }
 
-  // Consumers: quantise x to Q8_1 codes in shared memory while the first
-  // stages are in flight.
-  const int ctid = threadIdx.x;
+  // Consumers: quantise x to Q8_1 in shared memory while the first chunks land.
   const int nq = p.K >> 2;
-  for (int base = 0; base < nq; base += MV_CWARPS * 32) {
-    const int qd = base + ctid;
-    const bool v = qd < nq;
-    float4 xv = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (v) xv = __ldg(reinterpret_cast<const float4*>(p.x) + qd);
-    const Q8Quad r = quantize_quad(xv);
-    if (v) {
-      const int k = qd << 2;
-      *reinterpret_cast<uint32_t*>(xq + xq_offset<WT>(k)) = pack_q4(r.q);
-      if ((qd & 7) == 0) xds[k >> 5] = make_float2(r.dh, __fmul_rn(r.dh, static_cast<float>(r.sumq)));
+  for (int base = 0; base < nq; base += 4 * MV_CTHREADS) {
+    float4 xv[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int qd = base + i * MV_CTHREADS + threadIdx.x;
+      xv[i] = qd < nq ? __ldg(reinterpret_cast<const float4*>(p.x) + qd) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int qd = base + i * MV_CTHREADS + threadIdx.x;
+      const Q8Quad r = quantize_quad(xv[i]);
+      // Sum q over this thread's half (16 values) of the 32-block
+      int s4 = r.q[0] + r.q[1] + r.q[2] + r.q[3];
+      s4 += __shfl_xor_sync(0xffffffffu, s4, 1);
+      s4 += __shfl_xor_sync(0xffffffffu, s4, 2);
+      const int s_hi = __shfl_down_sync(0xffffffffu, s4, 4);
+      if (qd < nq) {
+        const int k = qd << 2;
+        const int b = k >> 8, j = (k >> 4) & 15;
+        *reinterpret_cast<uint32_t*>(xq + xq_piece(b, j) + (k & 15)) = pack_q4(r.q);
+        if ((qd & 7) == 0) {
+          const int g8 = (k >> 5) & 7;
+          if (WT == KQ_Q4_K) {
+            int* e = reinterpret_cast<int*>(&xds[xds_q4k(b, g8 >> 1)]);
+            e[g8 & 1] = __float_as_int(r.dh);
+            e[2 + (g8 & 1)] = r.sumq;
+          } else {
+            xds[xds_q6k(b, g8)] = make_int4(__float_as_int(r.dh), s4, s_hi, 0);
+          }
+        }
+      }
     }
   }
-  asm volatile("bar.sync 1, %0;" ::"r"(MV_CWARPS * 32) : "memory");
+  asm volatile("bar.sync 1, %0;" ::"r"(MV_CTHREADS) : "memory");
 
-  const int wpr = p.warps_per_row;
-  const int row_in_stage = warp / wpr, part = warp % wpr;
-  const int units = (WT == KQ_Q4_K) ? p.nb * 4 : p.nb * 8;
-  for (int s = 0; s < n_stages; ++s) {
-    const int slot = s % p.n_ring;
-    const uint32_t ph = (s / p.n_ring) & 1;
-    if (!mbar_wait(&full[slot], ph, abort, p.err)) break;
-    const int row = r0 + s * p.stage_rows + row_in_stage;
-    float acc = 0.f;
-    if (row < r1) {
-      const uint8_t* rowp = ring + static_cast<size_t>(slot) * p.stage_bytes +
-                            static_cast<size_t>(row_in_stage) * p.rs;
-      if (WT == KQ_Q4_K)
-        acc = row_dot_q4k(rowp, xq, xds, units, lane + 32 * part, 32 * wpr);
-      else
-        acc = row_dot_q6k(rowp, xq, xds, units, lane + 32 * part, 32 * wpr);
-      acc = warp_sum_f(acc);
-    }
-    if (wpr == 1) {
-      if (row < r1 && lane == 0) p.y[row] = acc;
-    } else {
-      if (lane == 0) red[warp] = acc;
-      asm volatile("bar.sync 1, %0;" ::"r"(MV_CWARPS * 32) : "memory");
-      if (part == 0 && lane == 0 && row < r1) {
-        float t = red[warp];
-        for (int i = 1; i < wpr; ++i) t += red[warp + i];
-        p.y[row] = t;
+  // Items (row, block) in arrival order; one partial per item, reduced per row.
+  const int items_per_group = p.rows_per_group * p.nb;
+  for (int g0 = 0; g0 < n_items; g0 += items_per_group) {
+    const int g1 = min(n_items, g0 + items_per_group);
+    bool ok = true;
+    for (int it = g0 + threadIdx.x; it < g1; it += MV_CTHREADS) {
+      const int c = it / p.chunk_blocks;
+      const int slot = c % p.n_ring;
+      if (!mbar_wait(&full[slot], (c / p.n_ring) & 1, abort, p.err)) {
+        ok = false;
+        break;
       }
-      asm volatile("bar.sync 1, %0;" ::"r"(MV_CWARPS * 32) : "memory");
+      const uint8_t* blk = ring + static_cast<size_t>(slot) * p.slot_bytes +
+                           static_cast<size_t>(it - c * p.chunk_blocks) * p.bb;
+      const int b = it % p.nb;
+      part[it - g0] = (WT == KQ_Q4_K) ? block_dot_q4k(blk, b, xq, xds) : block_dot_q6k(blk, b, xq, xds);
+      mbar_arrive(&empty[slot]);
+    }
+    (void)ok;
+    asm volatile("bar.sync 1, %0;" ::"r"(MV_CTHREADS) : "memory");
+    const int rows = (g1 - g0) / p.nb;
+    for (int r = threadIdx.x; r < rows; r += MV_CTHREADS) {
+      const float* pr = part + r * p.nb;
+      float acc = 0.f;
+      for (int i = 0; i < p.nb; ++i) acc += pr[i];
+      p.y[r0 + g0 / p.nb + r] = acc;
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(MV_CTHREADS) : "memory");
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Q4_K decode matvec, "lane = row" form (used when a CTA's rows fit in shared
+// memory, which holds for decode sizes up to ~30 MB of weights).
+//
+// Each CTA owns a balanced contiguous range of rows. Its producer thread issues
+// one bulk copy per row as soon as the CTA starts, before the kernel waits for
+// the previous kernel on the stream (the weights do not depend on it), so the
+// weight stream of one call overlaps the tail of the previous one. Rows are
+// staged with a stride whose 16-byte count is odd, so 32 lanes reading the same
+// offset of 32 consecutive rows hit distinct bank groups.
+//
+// After the dependency wait the CTA quantises x to Q8_1 into shared memory.
+// Warp (g, k) then takes the 32 rows of row group g (one row per lane) and the
+// blocks of K-split k: for every block a lane decodes its row's header once
+// (d, dmin, eight 6-bit scales and mins) and accumulates the four 64-weight
+// chunks with dp4a against the shared activation codes, which all lanes read at
+// the same address (broadcast). Per-(row, split) partials are added in a fixed
+// order at the end.
+// ---------------------------------------------------------------------------
+constexpr int LR_NW = 24;  // compute warps per CTA (plus one producer warp)
+
+struct MatvecLaneRowParams {
+  const uint8_t* W;
+  const float* x;
+  float* y;
+  int M, K, nb, rs;
+  int stride;        // staged row stride in shared memory (bytes)
+  int max_rows;      // rows of the largest CTA range
+  int ks;            // K-splits per row group
+  int xq_off, xs_off, part_off, bar_off;  // shared-memory layout (bytes)
+  int* err;
+};
+
+__global__ void __launch_bounds__((LR_NW + 1) * 32, 1) matvec_q4k_lanerow_kernel(const MatvecLaneRowParams p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* rowsm = smem;
+  int8_t* xq = reinterpret_cast<int8_t*>(smem + p.xq_off);
+  float4* xs = reinterpret_cast<float4*>(smem + p.xs_off);  // per 64: d8(2c), d8(2c+1), s(2c), s(2c+1)
+  float* part = reinterpret_cast<float*>(smem + p.part_off);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);  // one per row group
+  volatile int* abort = reinterpret_cast<volatile int*>(full + (p.max_rows + 31) / 32);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * p.M / gridDim.x);
+  const int r1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * p.M / gridDim.x);
+  const int rows = r1 - r0;
+  const int n_groups = (rows + 31) / 32;
+
+  if (threadIdx.x == 0) {
+    for (int g = 0; g < n_groups; ++g) mbar_init(&full[g], 1);
+    *abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  if (warp == LR_NW) {
+    if (lane == 0) {
+      const uint8_t* base = p.W + static_cast<int64_t>(r0) * p.rs;
+      for (int g = 0; g < n_groups; ++g) {
+        const int ra = 32 * g, rb = min(rows, ra + 32);
+        mbar_expect_tx(&full[g], static_cast<uint32_t>((rb - ra) * p.rs));
+        for (int r = ra; r < rb; ++r)
+          bulk_g2s(rowsm + static_cast<size_t>(r) * p.stride, base + static_cast<int64_t>(r) * p.rs,
+                   static_cast<uint32_t>(p.rs), &full[g]);
+      }
+    }
+    return;
+  }
+
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // x may come from the previous kernel
+  constexpr int CT = LR_NW * 32;
+  const int g = warp / p.ks, ksplit = warp % p.ks;
+  if (g < n_groups) {
+    const int b0 = static_cast<int>(static_cast<int64_t>(ksplit) * p.nb / p.ks);
+    const int b1 = static_cast<int>(static_cast<int64_t>(ksplit + 1) * p.nb / p.ks);
+    // Quantise the activations of this K-split (blocks b0..b1) to Q8_1 in shared
+    // memory, 16 per lane. Warps of other row groups with the same split write
+    // the same values to the same place.
+    for (int base = b0 * QK_K; base < b1 * QK_K; base += 512) {
+      // the range is a whole number of 32-blocks, so both lanes of a pair agree on `valid`
+      const bool valid = base + 16 * lane < b1 * QK_K;
+      const int e0 = valid ? base + 16 * lane : b0 * QK_K;
+      float v[16];
+      const float4* src = reinterpret_cast<const float4*>(p.x + e0);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float4 t = __ldg(src + i);
+        v[4 * i] = t.x;
+        v[4 * i + 1] = t.y;
+        v[4 * i + 2] = t.z;
+        v[4 * i + 3] = t.w;
+      }
+      const Q8Half r = quantize_half(v);
+      if (valid) *reinterpret_cast<uint4*>(xq + e0) = make_uint4(r.q[0], r.q[1], r.q[2], r.q[3]);
+      if (valid && (lane & 1) == 0) {
+        float* e = reinterpret_cast<float*>(xs + (e0 >> 6));
+        const float sq = __fmul_rn(r.dh, static_cast<float>(r.sumq));  // exact
+        if (((e0 >> 5) & 1) == 0) {
+          e[0] = r.dh;
+          e[2] = sq;
+        } else {
+          e[1] = r.dh;
+          e[3] = sq;
+        }
+      }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[slot]);
+    const int row = min(32 * g + lane, rows - 1);  // lanes past the last row repeat it; their result is dropped
+    const uint8_t* rowp = rowsm + static_cast<size_t>(row) * p.stride;
+    float acc = 0.f;
+    if (mbar_wait(&full[g], 0, abort, p.err)) {
+      for (int b = b0; b < b1; ++b) {
+        const uint8_t* blk = rowp + b * Q4K_BYTES;
+        const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
+        const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x & 0xFFFFu)));
+        const float dmin = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x >> 16)));
+        const uint32_t sc_lo = hdr.y & 0x3F3F3F3Fu, m_lo = hdr.z & 0x3F3F3F3Fu;
+        const uint32_t sc_hi = (hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u);
+        const uint32_t m_hi = ((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u);
+        const int8_t* xb = xq + (b << 8);
+        float lo = 0.f, mn = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint4 qa = *reinterpret_cast<const uint4*>(blk + 16 + 32 * c);
+          const uint4 qb = *reinterpret_cast<const uint4*>(blk + 32 + 32 * c);
+          const int4 x0 = *reinterpret_cast<const int4*>(xb + 64 * c);
+          const int4 x1 = *reinterpret_cast<const int4*>(xb + 64 * c + 16);
+          const int4 x2 = *reinterpret_cast<const int4*>(xb + 64 * c + 32);
+          const int4 x3 = *reinterpret_cast<const int4*>(xb + 64 * c + 48);
+          const float4 ds = xs[(b << 2) + c];
+          int a0 = __dp4a(static_cast<int>(qa.x & 0x0F0F0F0Fu), x0.x, 0);
+          int a1 = __dp4a(static_cast<int>(qb.x & 0x0F0F0F0Fu), x1.x, 0);
+          int h0 = __dp4a(static_cast<int>((qa.x >> 4) & 0x0F0F0F0Fu), x2.x, 0);
+          int h1 = __dp4a(static_cast<int>((qb.x >> 4) & 0x0F0F0F0Fu), x3.x, 0);
+          a0 = __dp4a(static_cast<int>(qa.y & 0x0F0F0F0Fu), x0.y, a0);
+          a1 = __dp4a(static_cast<int>(qb.y & 0x0F0F0F0Fu), x1.y, a1);
+          h0 = __dp4a(static_cast<int>((qa.y >> 4) & 0x0F0F0F0Fu), x2.y, h0);
+          h1 = __dp4a(static_cast<int>((qb.y >> 4) & 0x0F0F0F0Fu), x3.y, h1);
+          a0 = __dp4a(static_cast<int>(qa.z & 0x0F0F0F0Fu), x0.z, a0);
+          a1 = __dp4a(static_cast<int>(qb.z & 0x0F0F0F0Fu), x1.z, a1);
+          h0 = __dp4a(static_cast<int>((qa.z >> 4) & 0x0F0F0F0Fu), x2.z, h0);
+          h1 = __dp4a(static_cast<int>((qb.z >> 4) & 0x0F0F0F0Fu), x3.z, h1);
+          a0 = __dp4a(static_cast<int>(qa.w & 0x0F0F0F0Fu), x0.w, a0);
+          a1 = __dp4a(static_cast<int>(qb.w & 0x0F0F0F0Fu), x1.w, a1);
+          h0 = __dp4a(static_cast<int>((qa.w >> 4) & 0x0F0F0F0Fu), x2.w, h0);
+          h1 = __dp4a(static_cast<int>((qb.w >> 4) & 0x0F0F0F0Fu), x3.w, h1);
+          const uint32_t scw = (c < 2) ? sc_lo : sc_hi;
+          const uint32_t mw = (c < 2) ? m_lo : m_hi;
+          const int sh = (c & 1) * 16;
+          const int scA = (scw >> sh) & 0xFF, scB = (scw >> (sh + 8)) & 0xFF;
+          const int mA = (mw >> sh) & 0xFF, mB = (mw >> (sh + 8)) & 0xFF;
+          lo = fmaf(ds.x, i2f(scA * (a0 + a1)), lo);
+          lo = fmaf(ds.y, i2f(scB * (h0 + h1)), lo);
+          mn = fmaf(ds.z, i2f(mA), mn);
+          mn = fmaf(ds.w, i2f(mB), mn);
+        }
+        acc = fmaf(d, lo, acc);
+        acc = fmaf(-dmin, mn, acc);
+      }
+    }
+    if (32 * g + lane < rows) part[(32 * g + lane) * p.ks + ksplit] = acc;
+  }
+  asm volatile("bar.sync 1, %0;" ::"r"(CT) : "memory");
+  for (int r = threadIdx.x; r < rows; r += CT) {
+    const float* pr = part + r * p.ks;
+    float acc = pr[0];
+    for (int k = 1; k < p.ks; ++k) acc += pr[k];
+    p.y[r0 + r] = acc;
   }
 }
 
 static inline int round_up(int v, int a) { return (v + a - 1) / a * a; }
 
+// Shared-memory plan of the lane-row kernel; false when the rows do not fit.
+static bool plan_lanerow(int64_t M, int64_t K, int num_sms, MatvecLaneRowParams* p, size_t* smem) {
+  p->M = static_cast<int>(M);
+  p->K = static_cast<int>(K);
+  p->nb = static_cast<int>(K / QK_K);
+  p->rs = p->nb * Q4K_BYTES;
+  p->stride = ((p->rs / 16) & 1) ? p->rs : p->rs + 16;
+  const int G = static_cast<int>(std::min<int64_t>(M, num_sms));
+  p->max_rows = static_cast<int>((M + G - 1) / G);
+  const int n_groups = (p->max_rows + 31) / 32;
+  if (n_groups > LR_NW) return false;
+  p->ks = std::max(1, std::min(p->nb, LR_NW / n_groups));
+  size_t off = round_up(p->max_rows * p->stride, 128);
+  p->xq_off = static_cast<int>(off);
+  off += round_up(p->K, 128);
+  p->xs_off = static_cast<int>(off);
+  off += round_up((p->K / 64) * 16, 128);
+  p->part_off = static_cast<int>(off);
+  off += round_up(p->max_rows * p->ks * 4, 128);
+  p->bar_off = static_cast<int>(off);
+  off += n_groups * 8 + 16;
+  *smem = off;
+  return off <= static_cast<size_t>(MV_SMEM_LIMIT);
+}
+
 cudaError_t launch_matvec(int wtype, const void* W, const float* x, float* y, int64_t M, int64_t K, int* err,
                           int num_sms, cudaStream_t s, int* status) {
   *status = KQ_OK;
+  // Q4_K whose per-CTA rows fit in shared memory: the lane-row kernel.
+  if (wtype == KQ_Q4_K) {
+    MatvecLaneRowParams lp{};
+    size_t smem = 0;
+    if (plan_lanerow(M, K, num_sms, &lp, &smem)) {
+      lp.W = static_cast<const uint8_t*>(W);
+      lp.x = x;
+      lp.y = y;
+      lp.err = err;
+      const int G = static_cast<int>(std::min<int64_t>(M, num_sms));
+      cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(matvec_q4k_lanerow_kernel), 9);
+      if (e != cudaSuccess) return e;
+      return launch_pdl(matvec_q4k_lanerow_kernel, dim3(G), dim3((LR_NW + 1) * 32), smem, s, lp);
+    }
+  }
   MatvecParams p{};
   p.W = static_cast<const uint8_t*>(W);
   p.x = x;
@@ -274,55 +505,47 @@ cudaError_t launch_matvec(int wtype, const void* W, const float* x, float* y, in
   p.M = static_cast<int>(M);
   p.K = static_cast<int>(K);
   p.nb = static_cast<int>(K / QK_K);
-  p.rs = p.nb * (wtype == KQ_Q4_K ? Q4K_BYTES : Q6K_BYTES);
-  p.unit_rows = (p.rs % 16 == 0) ? 1 : 8;
+  p.bb = wtype == KQ_Q4_K ? Q4K_BYTES : Q6K_BYTES;
+  p.rs = p.nb * p.bb;
+  p.unit_rows = (p.rs % 16 == 0) ? 1 : 8;  // 8 rows of 210-byte blocks span a multiple of 16 bytes
+  p.chunk_blocks = wtype == KQ_Q4_K ? MV_CHUNK_BLOCKS_Q4K : MV_CHUNK_BLOCKS_Q6K;
+  p.chunk_bytes = p.chunk_blocks * p.bb;
+  p.slot_bytes = round_up(p.chunk_bytes, 128);
+  p.rows_per_group = MV_PART_MAX / p.nb;
+  p.xq_bytes = round_up(p.K, 128);
+  p.xds_bytes = round_up((p.K / QK_K) * 8 * 16, 128);
   p.err = err;
-  int R = 0;
-  for (int r = MV_CWARPS; r >= p.unit_rows && r >= 1; r >>= 1) {
-    if (static_cast<int64_t>(r) * p.rs <= MV_STAGE_LIMIT) {
-      R = r;
-      break;
-    }
-  }
-  if (R == 0) {
+  if (p.rows_per_group < 1) {
     *status = KQ_ERR_SHAPE;
     return cudaSuccess;
   }
-  p.stage_rows = R;
-  p.warps_per_row = MV_CWARPS / R;
-  p.stage_bytes = round_up(R * p.rs, 128);
-  p.xq_bytes = round_up(p.K, 128);
-  p.xds_bytes = round_up((p.K / QK8_1) * 8, 128);
-  const int fixed = p.xq_bytes + p.xds_bytes;
-  const int tail = 0;
-  int n_ring = (MV_SMEM_LIMIT - fixed - 1024 - tail) / (p.stage_bytes + 16);
-  if (n_ring > 16) n_ring = 16;
+  const int fixed = p.xq_bytes + p.xds_bytes + MV_PART_MAX * 4 + 1024;
+  int n_ring = (MV_SMEM_LIMIT - fixed) / (p.slot_bytes + 16);
+  if (n_ring > MV_MAX_RING) n_ring = MV_MAX_RING;
   if (n_ring < 2) {
     *status = KQ_ERR_SHAPE;
     return cudaSuccess;
   }
   p.n_units = static_cast<int>((M + p.unit_rows - 1) / p.unit_rows);
   const int G = p.n_units < num_sms ? p.n_units : num_sms;
-  // ring depth beyond what the largest CTA range needs buys nothing
+  // a ring deeper than the largest CTA range buys nothing
   const int64_t max_rows = (static_cast<int64_t>(p.n_units + G - 1) / G) * p.unit_rows;
-  const int need = static_cast<int>((max_rows + R - 1) / R);
-  if (n_ring > need) n_ring = need < 2 ? 2 : need;
+  const int64_t need = (max_rows * p.nb + p.chunk_blocks - 1) / p.chunk_blocks;
+  if (n_ring > need) n_ring = static_cast<int>(need < 1 ? 1 : need);
   p.n_ring = n_ring;
-  const size_t smem = static_cast<size_t>(fixed) + static_cast<size_t>(n_ring) * p.stage_bytes +
-                      2 * n_ring * sizeof(uint64_t) + MV_CWARPS * sizeof(float) + 16;
+  const size_t smem = static_cast<size_t>(p.xq_bytes + p.xds_bytes + MV_PART_MAX * 4) +
+                      static_cast<size_t>(n_ring) * p.slot_bytes + 2 * n_ring * sizeof(uint64_t) + 16;
   cudaError_t e;
   if (wtype == KQ_Q4_K) {
-    e = cudaFuncSetAttribute(matvec_kernel<KQ_Q4_K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
+    e = allow_max_smem(reinterpret_cast<const void*>(matvec_kernel<KQ_Q4_K>), 0);
     if (e != cudaSuccess) return e;
-    matvec_kernel<KQ_Q4_K><<<G, MV_THREADS, smem, s>>>(p);
+    e = launch_pdl(matvec_kernel<KQ_Q4_K>, dim3(G), dim3(MV_THREADS), smem, s, p);
   } else {
-    e = cudaFuncSetAttribute(matvec_kernel<KQ_Q6_K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
+    e = allow_max_smem(reinterpret_cast<const void*>(matvec_kernel<KQ_Q6_K>), 1);
     if (e != cudaSuccess) return e;
-    matvec_kernel<KQ_Q6_K><<<G, MV_THREADS, smem, s>>>(p);
+    e = launch_pdl(matvec_kernel<KQ_Q6_K>, dim3(G), dim3(MV_THREADS), smem, s, p);
   }
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace kq

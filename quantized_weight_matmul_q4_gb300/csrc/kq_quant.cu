@@ -9,6 +9,7 @@ namespace kq {
 // laid out as [fp16 d][fp16 s][int8 q[32]].
 __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float* __restrict__ X, uint8_t* __restrict__ Xq,
                                                             int64_t nblk) {
+  pdl_enter();
   const int64_t t = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
   const int64_t b = t >> 3;
   const int j = static_cast<int>(t & 7);
@@ -30,6 +31,7 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float* __restr
 // rounded once.
 __global__ void __launch_bounds__(256) quantize_xhat_kernel(const float* __restrict__ X, __half* __restrict__ Xh,
                                                             int K, int64_t rows, const int* __restrict__ src_rows) {
+  pdl_enter();
   const int64_t t = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;  // quad index in the output
   const int64_t kq4 = K >> 2;
   const int64_t row = t / kq4;
@@ -58,8 +60,8 @@ cudaError_t launch_quantize_q8_1(const float* X, void* Xq, int64_t K, int64_t N,
   const int64_t threads = nblk * 8;
   const int64_t grid = (threads + 255) / 256;
   if (grid == 0) return cudaSuccess;
-  quantize_q8_1_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(X, static_cast<uint8_t*>(Xq), nblk);
-  return cudaGetLastError();
+  return launch_pdl(quantize_q8_1_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, s, X,
+                    static_cast<uint8_t*>(Xq), nblk);
 }
 
 cudaError_t launch_quantize_xhat(const float* X, __half* Xh, int64_t K, int64_t rows, const int* src_rows,
@@ -67,8 +69,8 @@ cudaError_t launch_quantize_xhat(const float* X, __half* Xh, int64_t K, int64_t 
   const int64_t threads = rows * (K / 4);
   const int64_t grid = (threads + 255) / 256;
   if (grid == 0) return cudaSuccess;
-  quantize_xhat_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(X, Xh, static_cast<int>(K), rows, src_rows);
-  return cudaGetLastError();
+  return launch_pdl(quantize_xhat_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, s, X, Xh,
+                    static_cast<int>(K), rows, src_rows);
 }
 
 }  // namespace kq

@@ -56,4 +56,41 @@ __device__ __forceinline__ uint32_t pack_q4(const int (&q)[4]) {
          ((static_cast<uint32_t>(q[2]) & 0xFFu) << 16) | ((static_cast<uint32_t>(q[3]) & 0xFFu) << 24);
 }
 
+// Quantises 16 consecutive values v[0..15] held by one lane; the two lanes of
+// an aligned lane pair hold one 32-element block (lane 2i: elements 0..15).
+// Same arithmetic as quantize_quad (IEEE division, product, round half to even,
+// saturation to [-128, 127]). Both lanes of the pair must call it.
+struct Q8Half {
+  uint32_t q[4];   // 16 packed int8 codes
+  float dh;        // fp16-rounded block scale d_h, as fp32
+  int sumq;        // Sum q over the whole 32-element block
+};
+
+// round half to even, then clamp to [-128, 127]
+__device__ __forceinline__ int cvt_rni_sat_s8(float x) { return max(-128, min(127, __float2int_rn(x))); }
+
+__device__ __forceinline__ Q8Half quantize_half(const float (&v)[16]) {
+  float a = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) a = fmaxf(a, fabsf(v[i]));
+  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+  const float d = __fdiv_rn(a, 127.0f);
+  const float di = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
+  Q8Half r;
+  int s = 0;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const int q0 = cvt_rni_sat_s8(__fmul_rn(v[4 * w + 0], di));
+    const int q1 = cvt_rni_sat_s8(__fmul_rn(v[4 * w + 1], di));
+    const int q2 = cvt_rni_sat_s8(__fmul_rn(v[4 * w + 2], di));
+    const int q3 = cvt_rni_sat_s8(__fmul_rn(v[4 * w + 3], di));
+    s += q0 + q1 + q2 + q3;
+    r.q[w] = (static_cast<uint32_t>(q0) & 0xFFu) | ((static_cast<uint32_t>(q1) & 0xFFu) << 8) |
+             ((static_cast<uint32_t>(q2) & 0xFFu) << 16) | ((static_cast<uint32_t>(q3) & 0xFFu) << 24);
+  }
+  r.sumq = s + __shfl_xor_sync(0xffffffffu, s, 1);
+  r.dh = __half2float(__float2half_rn(d));
+  return r;
+}
+
 }  // namespace kq
