@@ -123,6 +123,39 @@ KQ_API kq_status kq_gemm(int wtype, const void* W, const float* X, float* Y, int
                   size_t ws_bytes, kq_stream_t stream);
 
 /*
+ * kq_gemm_noalloc — kq_gemm without a workspace argument. This entry point is
+ * an addition of this library; the source pages have no counterpart to it.
+ * Same operation, arguments (minus ws/ws_bytes), layouts, accuracy and
+ * determinism as kq_gemm; it runs the same kernels.
+ *
+ * Who needs it: callers that cannot hand the library device memory per call,
+ * e.g. plain C hosts with no device allocator of their own, or runtimes that
+ * plan all device memory ahead and forbid allocation on the per-token path
+ * (cudaMalloc may synchronise the device, which such a loop cannot afford).
+ * The library itself allocates nothing here: the scratch (fp16 x_hat and
+ * split-K partials) is a fixed array of KQ_GEMM_STATIC_WS_BYTES per device,
+ * part of the library's device image, which no caller has to clear.
+ *
+ * Limit: returns KQ_ERR_WORKSPACE, with nothing queued, when the call would
+ * need more scratch than KQ_GEMM_STATIC_WS_BYTES, i.e. when
+ * kq_workspace_bytes(KQ_OP_GEMM, wtype, M, K, N, 0, 0) > KQ_GEMM_STATIC_WS_BYTES
+ * (for instance N = 2048 tokens with K = 14336). Use kq_gemm there.
+ *
+ * Set-up: the first call on each device (with that device current) looks up
+ * the array's device address, which loads the array's module; make that first
+ * call before any stream capture.
+ *
+ * Concurrency: all calls on one device share the one array. Two calls whose
+ * kernels may overlap (on different streams, or from several host threads
+ * without ordering) race on it and give wrong results; order them on one
+ * stream (or with events).
+ */
+#define KQ_GEMM_STATIC_WS_BYTES ((size_t)32 << 20)
+
+KQ_API kq_status kq_gemm_noalloc(int wtype, const void* W, const float* X, float* Y, int64_t M, int64_t K,
+                                 int64_t N, kq_stream_t stream);
+
+/*
  * kq_moe_grouped_gemm — MoE expert matmul ([MMQv2] MoE routing; [GAP] T2).
  * For every token t and slot j < top_k: Y[t][j][:] = dequant(W_e) . x_t with
  * e = expert_ids[t*top_k + j]. The (token, slot) pairs are grouped by expert

@@ -10,14 +10,14 @@ from __future__ import annotations
 
 import ctypes
 
-from ._native import (KQ_DEVERR_EXPERT_ID, KQ_DEVERR_NONE, KQ_DEVERR_WAIT_TIMEOUT, KQ_OP_GEMM, KQ_OP_MATVEC,
-                      KQ_OP_MOE, KQ_Q4_K, KQ_Q6_K, KQError, check, lib)
+from ._native import (KQ_DEVERR_EXPERT_ID, KQ_DEVERR_NONE, KQ_DEVERR_WAIT_TIMEOUT, KQ_GEMM_STATIC_WS_BYTES,
+                      KQ_OP_GEMM, KQ_OP_MATVEC, KQ_OP_MOE, KQ_Q4_K, KQ_Q6_K, KQError, check, lib)
 
 __all__ = [
     "KQ_Q4_K", "KQ_Q6_K", "KQ_OP_MATVEC", "KQ_OP_GEMM", "KQ_OP_MOE", "KQError",
     "KQ_DEVERR_NONE", "KQ_DEVERR_WAIT_TIMEOUT", "KQ_DEVERR_EXPERT_ID",
-    "kq_quantize_q8_1", "kq_matvec", "kq_gemm", "kq_moe_grouped_gemm", "kq_workspace_bytes",
-    "kq_get_device_error", "block_bytes", "row_bytes",
+    "KQ_GEMM_STATIC_WS_BYTES", "kq_quantize_q8_1", "kq_matvec", "kq_gemm", "kq_gemm_noalloc",
+    "kq_moe_grouped_gemm", "kq_workspace_bytes", "kq_get_device_error", "block_bytes", "row_bytes",
 ]
 
 _BLOCK_BYTES = {KQ_Q4_K: 144, KQ_Q6_K: 210}
@@ -97,6 +97,21 @@ def kq_gemm(wtype, W, X, M: int, K: int, Y=None, ws=None, stream=None):
     check(lib().kq_gemm(_wt(wtype), _dev(W, "W", torch.uint8), _dev(X, "X", torch.float32),
                         _dev(Y, "Y", torch.float32), M, K, N, _dev(ws, "ws", torch.uint8), ws.numel(),
                         _stream(stream)), "kq_gemm")
+    return Y
+
+
+def kq_gemm_noalloc(wtype, W, X, M: int, K: int, Y=None, stream=None):
+    """kq_gemm with the library's fixed per-device scratch instead of a workspace.
+
+    Raises KQError(KQ_ERR_WORKSPACE) when the shape needs more than
+    KQ_GEMM_STATIC_WS_BYTES of scratch. Calls that may overlap race on the scratch.
+    """
+    torch = _torch()
+    N = X.shape[0]
+    if Y is None:
+        Y = torch.empty((N, M), dtype=torch.float32, device=X.device)
+    check(lib().kq_gemm_noalloc(_wt(wtype), _dev(W, "W", torch.uint8), _dev(X, "X", torch.float32),
+                                _dev(Y, "Y", torch.float32), M, K, N, _stream(stream)), "kq_gemm_noalloc")
     return Y
 
 

@@ -30,6 +30,8 @@ KQ_DEVERR_NONE = 0
 KQ_DEVERR_WAIT_TIMEOUT = 1
 KQ_DEVERR_EXPERT_ID = 2
 
+KQ_GEMM_STATIC_WS_BYTES = 32 << 20
+
 _vp = ctypes.c_void_p
 _i64 = ctypes.c_int64
 _i32 = ctypes.c_int32
@@ -39,6 +41,7 @@ SIGNATURES = {
     "kq_quantize_q8_1": (ctypes.c_int, [_vp, _vp, _i64, _i64, _vp]),
     "kq_matvec": (ctypes.c_int, [ctypes.c_int, _vp, _vp, _vp, _i64, _i64, _vp]),
     "kq_gemm": (ctypes.c_int, [ctypes.c_int, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _sz, _vp]),
+    "kq_gemm_noalloc": (ctypes.c_int, [ctypes.c_int, _vp, _vp, _vp, _i64, _i64, _i64, _vp]),
     "kq_moe_grouped_gemm": (ctypes.c_int, [ctypes.c_int, _vp, _i32, _vp, _i32, _vp, _vp, _i64, _i64, _i64,
                                            _vp, _sz, _vp]),
     "kq_workspace_bytes": (_sz, [ctypes.c_int, ctypes.c_int, _i64, _i64, _i64, _i32, _i32]),

@@ -62,6 +62,8 @@ kq_status finish(cudaError_t e, int status) {
 
 }  // namespace
 
+cudaError_t device_context(int* dev, int* num_sms, int** err) { return device_state(dev, num_sms, err); }
+
 cudaError_t allow_max_smem(const void* kernel, int slot) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

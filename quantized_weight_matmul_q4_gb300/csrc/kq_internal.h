@@ -35,6 +35,10 @@ cudaError_t launch_moe(int wtype, const void* W, int n_experts, const int32_t* i
                        float* Y, int64_t M, int64_t K, int64_t T, void* ws, const MoePlan& plan, int* err,
                        int num_sms, cudaStream_t s, int* status);
 
+// Current device, its SM count and the device address of its error word
+// (looked up once per device).
+cudaError_t device_context(int* dev, int* num_sms, int** err);
+
 // Raises a kernel's dynamic shared-memory limit to the 227 KB maximum, once per
 // device (later calls only read a flag, so launches stay cheap and capturable).
 cudaError_t allow_max_smem(const void* kernel, int slot);

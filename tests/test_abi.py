@@ -63,6 +63,15 @@ def test_gemm_argument_checks(L):
     assert L.kq_gemm(nat.KQ_Q4_K, A, A, U, 16, 256, 4, A, 1 << 30, NUL) == nat.KQ_ERR_ALIGN
 
 
+def test_gemm_noalloc_argument_checks(L):
+    f = L.kq_gemm_noalloc
+    assert f(0, A, A, A, 16, 256, 4, NUL) == nat.KQ_ERR_TYPE
+    assert f(nat.KQ_Q4_K, A, NUL, A, 16, 256, 4, NUL) == nat.KQ_ERR_NULL
+    assert f(nat.KQ_Q4_K, A, A, A, 16, 128, 4, NUL) == nat.KQ_ERR_SHAPE
+    assert f(nat.KQ_Q6_K, A, A, A, 16, 1024, 4, NUL) == nat.KQ_ERR_SHAPE
+    assert f(nat.KQ_Q4_K, A, A, U, 16, 256, 4, NUL) == nat.KQ_ERR_ALIGN
+
+
 def test_moe_argument_checks(L):
     f = L.kq_moe_grouped_gemm
     assert f(nat.KQ_Q4_K, A, 8, A, 9, A, A, 16, 256, 4, A, 1 << 30, NUL) == nat.KQ_ERR_SHAPE   # top_k > E
