@@ -117,6 +117,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// Waits for the phase with the given parity, ignoring the abort flag (used to
+// let copies already in flight land before a CTA exits). Returns false after
+// WAIT_LIMIT_NS.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 7) == 0 && globaltimer_ns() - t0 > WAIT_LIMIT_NS) return false;
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Bulk and tensor copies (TMA)
 // ---------------------------------------------------------------------------

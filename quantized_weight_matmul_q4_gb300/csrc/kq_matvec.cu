@@ -282,202 +282,247 @@ __global__ void __launch_bounds__(MV_THREADS, 1) matvec_kernel(const MatvecParam
 }
 
 // ---------------------------------------------------------------------------
-// Q4_K decode matvec, "lane = row" form (used when a CTA's rows fit in shared
-// memory, which holds for decode sizes up to ~30 MB of weights).
+// Q4_K decode matvec, "lane = row" form (the decode fast path, used when a
+// CTA's rows fit in shared memory: decode matrices up to ~30 MB).
 //
-// Each CTA owns a balanced contiguous range of rows. Its producer thread issues
-// one bulk copy per row as soon as the CTA starts, before the kernel waits for
-// the previous kernel on the stream (the weights do not depend on it), so the
-// weight stream of one call overlaps the tail of the previous one. Rows are
-// staged with a stride whose 16-byte count is odd, so 32 lanes reading the same
-// offset of 32 consecutive rows hit distinct bank groups.
+// CTA c owns the R rows [c*R, c*R + R) (R <= 128; the last CTA may have
+// fewer) and stages all of them at once, so a whole call's weights are in
+// flight within the first microsecond. The rows are cut into chunks of cb
+// super-blocks (cb odd, up to 7: 1008 contiguous bytes per row); a chunk is one
+// 2-D tensor copy of R rows x cb*144 bytes with its own mbarrier, and the
+// producer thread issues every chunk as soon as the CTA starts, before the
+// kernel waits for the previous kernel on the stream (the weights do not depend
+// on it). The copies are contiguous row segments, which HBM streams at full
+// rate, and chunks land in issue order.
 //
-// After the dependency wait the CTA quantises x to Q8_1 into shared memory.
-// Warp (g, k) then takes the 32 rows of row group g (one row per lane) and the
-// blocks of K-split k: for every block a lane decodes its row's header once
-// (d, dmin, eight 6-bit scales and mins) and accumulates the four 64-weight
-// chunks with dp4a against the shared activation codes, which all lanes read at
-// the same address (broadcast). Per-(row, split) partials are added in a fixed
-// order at the end.
+// After the dependency wait the consumer warps quantise x to Q8_1 in shared
+// memory (eight values per thread, four threads per 32-block). The work items
+// (chunk, row group of 32 rows, block of the chunk) are dealt to the warps in
+// chunk order, so the items of a chunk run on different warps as soon as it
+// lands and only the last chunk's items remain once the stream ends. For an
+// item, each lane takes one row: it decodes the block header (d, dmin, eight
+// 6-bit scales and mins) once and accumulates the four 64-weight chunks with
+// dp4a against the activation codes, which all lanes read at one address
+// (broadcast). The row pitch cb*144 bytes is an odd number of 16-byte units, so
+// 32 lanes reading one offset of 32 rows hit distinct bank groups. A warp
+// adds its items into one register per row group, in item order; the warps'
+// sums are added in warp order at the end (deterministic).
 // ---------------------------------------------------------------------------
-constexpr int LR_NW = 24;  // compute warps per CTA (plus one producer warp)
+constexpr int LR_NW = 24;                    // consumer warps (plus one producer warp)
+constexpr int LR_THREADS = (LR_NW + 1) * 32;
+constexpr int LR_CT = LR_NW * 32;
+constexpr int LR_MAX_ROWS = 128;             // rows per CTA: at most four row groups
+constexpr int LR_XT = 2;                     // 8-value activation tasks loaded per thread per round
 
 struct MatvecLaneRowParams {
-  const uint8_t* W;
   const float* x;
   float* y;
-  int M, K, nb, rs;
-  int stride;        // staged row stride in shared memory (bytes)
-  int max_rows;      // rows of the largest CTA range
-  int ks;            // K-splits per row group
+  int M, K, nb;
+  int R;            // rows per CTA
+  int n_groups;     // ceil(R / 32)
+  int cb;           // super-blocks per chunk (odd)
+  int n_chunks;     // ceil(nb / cb)
+  int chunk_bytes;  // shared-memory stride of a chunk (R * cb * 144 rounded up to 128)
+  uint32_t inv_per_chunk, inv_cb;  // ceil(2^32 / d) for d = n_groups * cb and d = cb
   int xq_off, xs_off, part_off, bar_off;  // shared-memory layout (bytes)
   int* err;
 };
 
-__global__ void __launch_bounds__((LR_NW + 1) * 32, 1) matvec_q4k_lanerow_kernel(const MatvecLaneRowParams p) {
+__global__ void __launch_bounds__(LR_THREADS, 1)
+    matvec_q4k_lanerow_kernel(const __grid_constant__ CUtensorMap tmW, const MatvecLaneRowParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  uint8_t* rowsm = smem;
   int8_t* xq = reinterpret_cast<int8_t*>(smem + p.xq_off);
-  float4* xs = reinterpret_cast<float4*>(smem + p.xs_off);  // per 64: d8(2c), d8(2c+1), s(2c), s(2c+1)
-  float* part = reinterpret_cast<float*>(smem + p.part_off);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);  // one per row group
-  volatile int* abort = reinterpret_cast<volatile int*>(full + (p.max_rows + 31) / 32);
+  float2* xs = reinterpret_cast<float2*>(smem + p.xs_off);  // per 32-block: {d8, d8 * Sum q}
+  float* part = reinterpret_cast<float*>(smem + p.part_off);  // [warp][row group][lane]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);  // one per chunk
+  volatile int* abort = reinterpret_cast<volatile int*>(full + p.n_chunks);
 
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * p.M / gridDim.x);
-  const int r1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * p.M / gridDim.x);
-  const int rows = r1 - r0;
-  const int n_groups = (rows + 31) / 32;
+  const int r0 = blockIdx.x * p.R;
+  const int rows = min(p.R, p.M - r0);
 
   if (threadIdx.x == 0) {
-    for (int g = 0; g < n_groups; ++g) mbar_init(&full[g], 1);
+    for (int c = 0; c < p.n_chunks; ++c) mbar_init(&full[c], 1);
     *abort = 0;
     fence_mbar_init();
   }
   __syncthreads();
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp == LR_NW) {
     if (lane == 0) {
-      const uint8_t* base = p.W + static_cast<int64_t>(r0) * p.rs;
-      for (int g = 0; g < n_groups; ++g) {
-        const int ra = 32 * g, rb = min(rows, ra + 32);
-        mbar_expect_tx(&full[g], static_cast<uint32_t>((rb - ra) * p.rs));
-        for (int r = ra; r < rb; ++r)
-          bulk_g2s(rowsm + static_cast<size_t>(r) * p.stride, base + static_cast<int64_t>(r) * p.rs,
-                   static_cast<uint32_t>(p.rs), &full[g]);
+      tma_prefetch_desc(&tmW);
+      const uint32_t box = static_cast<uint32_t>(p.R * p.cb * Q4K_BYTES);
+      for (int c = 0; c < p.n_chunks; ++c) {
+        mbar_expect_tx(&full[c], box);
+        tma_load_2d(smem + static_cast<size_t>(c) * p.chunk_bytes, &tmW, &full[c], c * p.cb * (Q4K_BYTES / 4), r0);
       }
+      // Every copy lands before the CTA may exit (also when the consumers gave up).
+      for (int c = 0; c < p.n_chunks; ++c)
+        if (!mbar_wait_bounded(&full[c], 0)) report_error(p.err, ERR_WAIT_TIMEOUT);
     }
     return;
   }
 
   asm volatile("griddepcontrol.wait;" ::: "memory");  // x may come from the previous kernel
-  constexpr int CT = LR_NW * 32;
-  const int g = warp / p.ks, ksplit = warp % p.ks;
-  if (g < n_groups) {
-    const int b0 = static_cast<int>(static_cast<int64_t>(ksplit) * p.nb / p.ks);
-    const int b1 = static_cast<int>(static_cast<int64_t>(ksplit + 1) * p.nb / p.ks);
-    // Quantise the activations of this K-split (blocks b0..b1) to Q8_1 in shared
-    // memory, 16 per lane. Warps of other row groups with the same split write
-    // the same values to the same place.
-    for (int base = b0 * QK_K; base < b1 * QK_K; base += 512) {
-      // the range is a whole number of 32-blocks, so both lanes of a pair agree on `valid`
-      const bool valid = base + 16 * lane < b1 * QK_K;
-      const int e0 = valid ? base + 16 * lane : b0 * QK_K;
-      float v[16];
-      const float4* src = reinterpret_cast<const float4*>(p.x + e0);
+
+  // x -> Q8_1 in shared memory: task t quantises x[8t .. 8t+8); the four tasks
+  // of a 32-block sit on four consecutive lanes. nt is a multiple of 32, so a
+  // warp's tasks are all in range or all out of range.
+  const int nt = p.K >> 3;
+  for (int t0 = 0; t0 < nt; t0 += LR_CT * LR_XT) {
+    float v[LR_XT][8];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float4 t = __ldg(src + i);
-        v[4 * i] = t.x;
-        v[4 * i + 1] = t.y;
-        v[4 * i + 2] = t.z;
-        v[4 * i + 3] = t.w;
-      }
-      const Q8Half r = quantize_half(v);
-      if (valid) *reinterpret_cast<uint4*>(xq + e0) = make_uint4(r.q[0], r.q[1], r.q[2], r.q[3]);
-      if (valid && (lane & 1) == 0) {
-        float* e = reinterpret_cast<float*>(xs + (e0 >> 6));
-        const float sq = __fmul_rn(r.dh, static_cast<float>(r.sumq));  // exact
-        if (((e0 >> 5) & 1) == 0) {
-          e[0] = r.dh;
-          e[2] = sq;
-        } else {
-          e[1] = r.dh;
-          e[3] = sq;
-        }
+    for (int i = 0; i < LR_XT; ++i) {
+      const int t = t0 + threadIdx.x + i * LR_CT;
+      if (t < nt) {
+        const float4* src = reinterpret_cast<const float4*>(p.x) + 2 * t;
+        const float4 a = __ldg(src), c = __ldg(src + 1);
+        v[i][0] = a.x; v[i][1] = a.y; v[i][2] = a.z; v[i][3] = a.w;
+        v[i][4] = c.x; v[i][5] = c.y; v[i][6] = c.z; v[i][7] = c.w;
       }
     }
-    __syncwarp();
-    const int row = min(32 * g + lane, rows - 1);  // lanes past the last row repeat it; their result is dropped
-    const uint8_t* rowp = rowsm + static_cast<size_t>(row) * p.stride;
-    float acc = 0.f;
-    if (mbar_wait(&full[g], 0, abort, p.err)) {
-      for (int b = b0; b < b1; ++b) {
-        const uint8_t* blk = rowp + b * Q4K_BYTES;
-        const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
-        const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x & 0xFFFFu)));
-        const float dmin = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x >> 16)));
-        const uint32_t sc_lo = hdr.y & 0x3F3F3F3Fu, m_lo = hdr.z & 0x3F3F3F3Fu;
-        const uint32_t sc_hi = (hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u);
-        const uint32_t m_hi = ((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u);
-        const int8_t* xb = xq + (b << 8);
-        float lo = 0.f, mn = 0.f;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint4 qa = *reinterpret_cast<const uint4*>(blk + 16 + 32 * c);
-          const uint4 qb = *reinterpret_cast<const uint4*>(blk + 32 + 32 * c);
-          const int4 x0 = *reinterpret_cast<const int4*>(xb + 64 * c);
-          const int4 x1 = *reinterpret_cast<const int4*>(xb + 64 * c + 16);
-          const int4 x2 = *reinterpret_cast<const int4*>(xb + 64 * c + 32);
-          const int4 x3 = *reinterpret_cast<const int4*>(xb + 64 * c + 48);
-          const float4 ds = xs[(b << 2) + c];
-          int a0 = __dp4a(static_cast<int>(qa.x & 0x0F0F0F0Fu), x0.x, 0);
-          int a1 = __dp4a(static_cast<int>(qb.x & 0x0F0F0F0Fu), x1.x, 0);
-          int h0 = __dp4a(static_cast<int>((qa.x >> 4) & 0x0F0F0F0Fu), x2.x, 0);
-          int h1 = __dp4a(static_cast<int>((qb.x >> 4) & 0x0F0F0F0Fu), x3.x, 0);
-          a0 = __dp4a(static_cast<int>(qa.y & 0x0F0F0F0Fu), x0.y, a0);
-          a1 = __dp4a(static_cast<int>(qb.y & 0x0F0F0F0Fu), x1.y, a1);
-          h0 = __dp4a(static_cast<int>((qa.y >> 4) & 0x0F0F0F0Fu), x2.y, h0);
-          h1 = __dp4a(static_cast<int>((qb.y >> 4) & 0x0F0F0F0Fu), x3.y, h1);
-          a0 = __dp4a(static_cast<int>(qa.z & 0x0F0F0F0Fu), x0.z, a0);
-          a1 = __dp4a(static_cast<int>(qb.z & 0x0F0F0F0Fu), x1.z, a1);
-          h0 = __dp4a(static_cast<int>((qa.z >> 4) & 0x0F0F0F0Fu), x2.z, h0);
-          h1 = __dp4a(static_cast<int>((qb.z >> 4) & 0x0F0F0F0Fu), x3.z, h1);
-          a0 = __dp4a(static_cast<int>(qa.w & 0x0F0F0F0Fu), x0.w, a0);
-          a1 = __dp4a(static_cast<int>(qb.w & 0x0F0F0F0Fu), x1.w, a1);
-          h0 = __dp4a(static_cast<int>((qa.w >> 4) & 0x0F0F0F0Fu), x2.w, h0);
-          h1 = __dp4a(static_cast<int>((qb.w >> 4) & 0x0F0F0F0Fu), x3.w, h1);
-          const uint32_t scw = (c < 2) ? sc_lo : sc_hi;
-          const uint32_t mw = (c < 2) ? m_lo : m_hi;
-          const int sh = (c & 1) * 16;
-          const int scA = (scw >> sh) & 0xFF, scB = (scw >> (sh + 8)) & 0xFF;
-          const int mA = (mw >> sh) & 0xFF, mB = (mw >> (sh + 8)) & 0xFF;
-          lo = fmaf(ds.x, i2f(scA * (a0 + a1)), lo);
-          lo = fmaf(ds.y, i2f(scB * (h0 + h1)), lo);
-          mn = fmaf(ds.z, i2f(mA), mn);
-          mn = fmaf(ds.w, i2f(mB), mn);
-        }
-        acc = fmaf(d, lo, acc);
-        acc = fmaf(-dmin, mn, acc);
+    for (int i = 0; i < LR_XT; ++i) {
+      const int t = t0 + threadIdx.x + i * LR_CT;
+      if (t < nt) {
+        const Q8Oct r = quantize_oct(v[i]);
+        *reinterpret_cast<uint2*>(xq + 8 * t) = make_uint2(r.q[0], r.q[1]);
+        if ((lane & 3) == 0) xs[t >> 2] = make_float2(r.dh, __fmul_rn(r.dh, static_cast<float>(r.sumq)));  // exact
       }
     }
-    if (32 * g + lane < rows) part[(32 * g + lane) * p.ks + ksplit] = acc;
   }
-  asm volatile("bar.sync 1, %0;" ::"r"(CT) : "memory");
-  for (int r = threadIdx.x; r < rows; r += CT) {
-    const float* pr = part + r * p.ks;
-    float acc = pr[0];
-    for (int k = 1; k < p.ks; ++k) acc += pr[k];
-    p.y[r0 + r] = acc;
+  asm volatile("bar.sync 1, %0;" ::"r"(LR_CT) : "memory");
+
+  const float4* xs4 = reinterpret_cast<const float4*>(xs);
+  const int pitch = p.cb * Q4K_BYTES;
+  const int per_chunk = p.n_groups * p.cb;
+  const int items = p.n_chunks * per_chunk;
+  int ready = -1;  // last chunk this warp has seen land
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};  // this warp's sums for row groups 0..3
+  for (int i = warp; i < items; i += LR_NW) {
+    // i = (c * n_groups + g) * cb + j; quotients by multiply-high (exact in range)
+    const int c = static_cast<int>(__umulhi(static_cast<uint32_t>(i), p.inv_per_chunk));
+    const int rem = i - c * per_chunk;
+    const int g = static_cast<int>(__umulhi(static_cast<uint32_t>(rem), p.inv_cb));
+    const int j = rem - g * p.cb;
+    const int b = c * p.cb + j;
+    if (b >= p.nb) continue;  // zero-filled tail of the last chunk
+    if (c != ready) {
+      if (!mbar_wait(&full[c], 0, abort, p.err)) break;
+      ready = c;
+    }
+    const int row = 32 * g + lane;
+    const int srow = min(row, p.R - 1);  // lanes past the last row repeat it; their result is dropped
+    const uint8_t* blk = smem + static_cast<size_t>(c) * p.chunk_bytes + srow * pitch + j * Q4K_BYTES;
+    const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
+    const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x & 0xFFFFu)));
+    const float dmin = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x >> 16)));
+    // 6-bit scales and mins, one per byte: sub-blocks 0..3 and 4..7
+    const uint32_t sc_lo = hdr.y & 0x3F3F3F3Fu, m_lo = hdr.z & 0x3F3F3F3Fu;
+    const uint32_t sc_hi = (hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u);
+    const uint32_t m_hi = ((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u);
+    const int8_t* xb = xq + (b << 8);
+    float lo = 0.f, mn = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      // bytes 32q .. 32q+31 of the nibbles: low nibbles are sub-block 2q, high nibbles 2q+1
+      const uint4 qa = *reinterpret_cast<const uint4*>(blk + 16 + 32 * q);
+      const uint4 qb = *reinterpret_cast<const uint4*>(blk + 32 + 32 * q);
+      const int4 x0 = *reinterpret_cast<const int4*>(xb + 64 * q);
+      const int4 x1 = *reinterpret_cast<const int4*>(xb + 64 * q + 16);
+      const int4 x2 = *reinterpret_cast<const int4*>(xb + 64 * q + 32);
+      const int4 x3 = *reinterpret_cast<const int4*>(xb + 64 * q + 48);
+      const float4 ds = xs4[(b << 2) + q];  // {d8, s} of sub-blocks 2q and 2q+1
+      // high nibbles are taken in place (w & 0xF0F0F0F0 = 16 * nibble): the sums
+      // h0, h1 are exact multiples of 16
+      int a0 = __dp4a(static_cast<int>(qa.x & 0x0F0F0F0Fu), x0.x, 0);
+      int a1 = __dp4a(static_cast<int>(qb.x & 0x0F0F0F0Fu), x1.x, 0);
+      int h0 = dp4a_us(qa.x & 0xF0F0F0F0u, x2.x, 0);
+      int h1 = dp4a_us(qb.x & 0xF0F0F0F0u, x3.x, 0);
+      a0 = __dp4a(static_cast<int>(qa.y & 0x0F0F0F0Fu), x0.y, a0);
+      a1 = __dp4a(static_cast<int>(qb.y & 0x0F0F0F0Fu), x1.y, a1);
+      h0 = dp4a_us(qa.y & 0xF0F0F0F0u, x2.y, h0);
+      h1 = dp4a_us(qb.y & 0xF0F0F0F0u, x3.y, h1);
+      a0 = __dp4a(static_cast<int>(qa.z & 0x0F0F0F0Fu), x0.z, a0);
+      a1 = __dp4a(static_cast<int>(qb.z & 0x0F0F0F0Fu), x1.z, a1);
+      h0 = dp4a_us(qa.z & 0xF0F0F0F0u, x2.z, h0);
+      h1 = dp4a_us(qb.z & 0xF0F0F0F0u, x3.z, h1);
+      a0 = __dp4a(static_cast<int>(qa.w & 0x0F0F0F0Fu), x0.w, a0);
+      a1 = __dp4a(static_cast<int>(qb.w & 0x0F0F0F0Fu), x1.w, a1);
+      h0 = dp4a_us(qa.w & 0xF0F0F0F0u, x2.w, h0);
+      h1 = dp4a_us(qb.w & 0xF0F0F0F0u, x3.w, h1);
+      const uint32_t scw = (q < 2) ? sc_lo : sc_hi;
+      const uint32_t mw = (q < 2) ? m_lo : m_hi;
+      const int sh = (q & 1) * 16;
+      const int scA = (scw >> sh) & 0xFF, scB = (scw >> (sh + 8)) & 0xFF;
+      const int mA = (mw >> sh) & 0xFF, mB = (mw >> (sh + 8)) & 0xFF;
+      lo = fmaf(ds.x, i2f(scA * (a0 + a1)), lo);
+      lo = fmaf(ds.z, i2f(scB * ((h0 + h1) >> 4)), lo);
+      mn = fmaf(ds.y, i2f(mA), mn);
+      mn = fmaf(ds.w, i2f(mB), mn);
+    }
+    const float v = fmaf(-dmin, mn, d * lo);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc[k] += (g == k) ? v : 0.f;
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    if (k < p.n_groups) part[(warp * p.n_groups + k) * 32 + lane] = acc[k];
+  asm volatile("bar.sync 1, %0;" ::"r"(LR_CT) : "memory");
+  // y[row] = Sum over the warps, in warp order
+  for (int r = threadIdx.x; r < rows; r += LR_CT) {
+    const float* pr = part + (r >> 5) * 32 + (r & 31);
+    float a = pr[0];
+#pragma unroll 8
+    for (int w = 1; w < LR_NW; ++w) a += pr[w * p.n_groups * 32];
+    p.y[r0 + r] = a;
   }
 }
 
 static inline int round_up(int v, int a) { return (v + a - 1) / a * a; }
 
-// Shared-memory plan of the lane-row kernel; false when the rows do not fit.
-static bool plan_lanerow(int64_t M, int64_t K, int num_sms, MatvecLaneRowParams* p, size_t* smem) {
+// Launch plan of the lane-row kernel; false when a CTA's rows do not fit in
+// shared memory (then the item kernel above runs).
+static bool plan_lanerow(int64_t M, int64_t K, int num_sms, MatvecLaneRowParams* p, int* grid, size_t* smem) {
+  if (K > (int64_t(1) << 20)) return false;
   p->M = static_cast<int>(M);
   p->K = static_cast<int>(K);
   p->nb = static_cast<int>(K / QK_K);
-  p->rs = p->nb * Q4K_BYTES;
-  p->stride = ((p->rs / 16) & 1) ? p->rs : p->rs + 16;
-  const int G = static_cast<int>(std::min<int64_t>(M, num_sms));
-  p->max_rows = static_cast<int>((M + G - 1) / G);
-  const int n_groups = (p->max_rows + 31) / 32;
-  if (n_groups > LR_NW) return false;
-  p->ks = std::max(1, std::min(p->nb, LR_NW / n_groups));
-  size_t off = round_up(p->max_rows * p->stride, 128);
-  p->xq_off = static_cast<int>(off);
-  off += round_up(p->K, 128);
-  p->xs_off = static_cast<int>(off);
-  off += round_up((p->K / 64) * 16, 128);
-  p->part_off = static_cast<int>(off);
-  off += round_up(p->max_rows * p->ks * 4, 128);
-  p->bar_off = static_cast<int>(off);
-  off += n_groups * 8 + 16;
-  *smem = off;
-  return off <= static_cast<size_t>(MV_SMEM_LIMIT);
+  const int64_t G0 = std::min<int64_t>(M, num_sms);
+  const int64_t R = (M + G0 - 1) / G0;
+  if (R > LR_MAX_ROWS) return false;
+  p->R = static_cast<int>(R);
+  *grid = static_cast<int>((M + R - 1) / R);
+  p->n_groups = (p->R + 31) / 32;
+  const int part_bytes = LR_NW * p->n_groups * 32 * 4;
+  const int fixed = round_up(p->K, 128)                 // activation codes
+                    + round_up((p->K / 32) * 8, 128)    // {d8, d8 * Sum q} per 32-block
+                    + part_bytes;                       // per-warp partials
+  for (int cb = 7; cb >= 1; cb -= 2) {  // widest odd chunk that fits
+    const int n_chunks = (p->nb + cb - 1) / cb;
+    const int chunk_bytes = round_up(p->R * cb * Q4K_BYTES, 128);
+    const size_t total = static_cast<size_t>(n_chunks) * chunk_bytes + fixed + n_chunks * 8 + 16;
+    if (total > static_cast<size_t>(MV_SMEM_LIMIT)) continue;
+    p->cb = cb;
+    p->n_chunks = n_chunks;
+    // i / d == umulhi(i, ceil(2^32 / d)) holds while i * d < 2^32
+    if (static_cast<int64_t>(n_chunks) * p->n_groups * cb * p->n_groups * cb >= (int64_t(1) << 32)) return false;
+    p->inv_per_chunk = static_cast<uint32_t>(((uint64_t(1) << 32) + p->n_groups * cb - 1) / (p->n_groups * cb));
+    p->inv_cb = static_cast<uint32_t>(((uint64_t(1) << 32) + cb - 1) / cb);
+    p->chunk_bytes = chunk_bytes;
+    size_t off = static_cast<size_t>(n_chunks) * chunk_bytes;
+    p->xq_off = static_cast<int>(off);
+    off += round_up(p->K, 128);
+    p->xs_off = static_cast<int>(off);
+    off += round_up((p->K / 32) * 8, 128);
+    p->part_off = static_cast<int>(off);
+    off += part_bytes;
+    p->bar_off = static_cast<int>(off);
+    *smem = total;
+    return true;
+  }
+  return false;
 }
 
 cudaError_t launch_matvec(int wtype, const void* W, const float* x, float* y, int64_t M, int64_t K, int* err,
@@ -487,15 +532,22 @@ cudaError_t launch_matvec(int wtype, const void* W, const float* x, float* y, in
   if (wtype == KQ_Q4_K) {
     MatvecLaneRowParams lp{};
     size_t smem = 0;
-    if (plan_lanerow(M, K, num_sms, &lp, &smem)) {
-      lp.W = static_cast<const uint8_t*>(W);
+    int grid = 0;
+    if (plan_lanerow(M, K, num_sms, &lp, &grid, &smem)) {
+      CUtensorMap tmW;
+      const uint64_t rs = static_cast<uint64_t>(lp.nb) * Q4K_BYTES;
+      if (!encode_tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT32, W, rs / 4, static_cast<uint64_t>(M), rs,
+                          static_cast<uint32_t>(lp.cb * Q4K_BYTES / 4), static_cast<uint32_t>(lp.R),
+                          CU_TENSOR_MAP_SWIZZLE_NONE)) {
+        *status = KQ_ERR_CUDA;
+        return cudaSuccess;
+      }
       lp.x = x;
       lp.y = y;
       lp.err = err;
-      const int G = static_cast<int>(std::min<int64_t>(M, num_sms));
       cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(matvec_q4k_lanerow_kernel), 9);
       if (e != cudaSuccess) return e;
-      return launch_pdl(matvec_q4k_lanerow_kernel, dim3(G), dim3((LR_NW + 1) * 32), smem, s, lp);
+      return launch_pdl(matvec_q4k_lanerow_kernel, dim3(grid), dim3(LR_THREADS), smem, s, tmW, lp);
     }
   }
   MatvecParams p{};

@@ -93,4 +93,40 @@ __device__ __forceinline__ Q8Half quantize_half(const float (&v)[16]) {
   return r;
 }
 
+// Quantises 8 consecutive values v[0..7] held by one lane; the four lanes of an
+// aligned lane quad hold one 32-element block (lane 4i + j: elements 8j..8j+7).
+// Same arithmetic as quantize_quad. All four lanes of the quad must call it.
+struct Q8Oct {
+  uint32_t q[2];   // 8 packed int8 codes
+  float dh;        // fp16-rounded block scale d_h, as fp32
+  int sumq;        // Sum q over the whole 32-element block
+};
+
+__device__ __forceinline__ Q8Oct quantize_oct(const float (&v)[8]) {
+  float a = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(v[i]));
+  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+  const float d = __fdiv_rn(a, 127.0f);
+  const float di = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
+  Q8Oct r;
+  int s = 0;
+#pragma unroll
+  for (int w = 0; w < 2; ++w) {
+    const int q0 = cvt_rni_sat_s8(__fmul_rn(v[4 * w + 0], di));
+    const int q1 = cvt_rni_sat_s8(__fmul_rn(v[4 * w + 1], di));
+    const int q2 = cvt_rni_sat_s8(__fmul_rn(v[4 * w + 2], di));
+    const int q3 = cvt_rni_sat_s8(__fmul_rn(v[4 * w + 3], di));
+    s += q0 + q1 + q2 + q3;
+    r.q[w] = (static_cast<uint32_t>(q0) & 0xFFu) | ((static_cast<uint32_t>(q1) & 0xFFu) << 8) |
+             ((static_cast<uint32_t>(q2) & 0xFFu) << 16) | ((static_cast<uint32_t>(q3) & 0xFFu) << 24);
+  }
+  s += __shfl_xor_sync(0xffffffffu, s, 1);
+  s += __shfl_xor_sync(0xffffffffu, s, 2);
+  r.sumq = s;
+  r.dh = __half2float(__float2half_rn(d));
+  return r;
+}
+
 }  // namespace kq
