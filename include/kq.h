@@ -114,10 +114,13 @@ KQ_API kq_status kq_matvec(int wtype, const void* W, const float* x, float* y, i
  * kq_gemm — prefill GEMM Y = dequant(W) . X for N tokens ([MMQv2] Kernel
  * architecture; [GAP] T1). X is quantised to Q8_1 (as x_hat = fp16(d_h * q))
  * into the workspace once per call; weight super-blocks are staged by TMA and
- * unpacked to fp16 in shared memory; tcgen05 MMAs accumulate in tensor memory.
+ * unpacked to fp16 into tensor memory; tcgen05 MMAs accumulate in tensor memory.
  * W: M x K weights; X: fp32 [N][K]; Y: fp32 [N][M], written.
  * ws: device workspace of at least kq_workspace_bytes(KQ_OP_GEMM, ...) bytes.
  * Q6_K needs K % 2048 == 0 (rows whose byte length is a multiple of 16).
+ * As in kq_matvec, W is streamed before the GEMM waits for the previous kernel
+ * on the stream: W must not be written by a still-running predecessor that
+ * allows programmatic dependent launch.
  */
 KQ_API kq_status kq_gemm(int wtype, const void* W, const float* X, float* Y, int64_t M, int64_t K, int64_t N, void* ws,
                   size_t ws_bytes, kq_stream_t stream);

@@ -11,16 +11,19 @@
 // prefix sum and scatter). The pages' kernels target sm_89/sm_120 with
 // mma.sync and cp.async; this one is built for sm_103a:
 //
-//  * warp 12 streams raw weight super-blocks (128 rows x 1 super-block per
-//    stage) with 2-D TMA, warp 14 streams x_hat tiles (128-byte swizzle) with
+//  * warp 20 streams raw weight super-blocks (128 rows x 1 super-block per
+//    stage) with 2-D TMA, warp 22 streams x_hat tiles (128-byte swizzle) with
 //    2-D TMA, each into its own mbarrier ring;
-//  * warps 0-7 unpack Q4_K / Q6_K to fp16 straight into the swizzled K-major
-//    layout the tensor core reads (the "in-SMEM dequant" of the page), four
-//    64-wide K steps per super-block;
-//  * one thread of warp 13 issues tcgen05.mma (M=128, N<=256, K=16) into one
-//    of two 256-column accumulators in tensor memory;
-//  * warps 8-11 drain the other accumulator (tcgen05.ld) to global memory
-//    while the next tile is being computed.
+//  * warps 0-15 (two groups of 8 taking alternate K steps, so two steps are
+//    unpacked at once) unpack Q4_K / Q6_K to fp16 and store the A operand straight
+//    into tensor memory (tcgen05.st; the page unpacks into shared memory), four
+//    64-wide K steps per super-block: the weights never pass through shared
+//    memory as fp16, which leaves its bandwidth to the x_hat tiles the MMA
+//    reads from there;
+//  * one thread of warp 21 issues tcgen05.mma (M=128, N<=256, K=16, A from
+//    tensor memory, B from shared memory) into a tensor-memory accumulator;
+//  * warps 16-19 drain finished accumulators (tcgen05.ld) to global memory
+//    (with two accumulators, while the next tile is being computed).
 //
 // Tiles are statically strided over a persistent grid (one CTA per SM), so
 // results do not depend on scheduling; a split K range is summed afterwards in
@@ -35,16 +38,18 @@ namespace kq {
 constexpr int GM_BM = 128;            // weight rows per tile (MMA M)
 constexpr int GM_BNMAX = 256;         // largest token tile (MMA N)
 constexpr int GM_BK = 64;             // K per A/B stage: one 128-byte swizzled row of fp16
-constexpr int GM_A_BYTES = GM_BM * GM_BK * 2;
+constexpr int GM_A_COLS = GM_BK / 2;  // tensor-memory columns of one A stage (two fp16 per column)
+constexpr int GM_A_MAX_STAGES = 8;
 constexpr int GM_BBOX = 64;           // token rows per x_hat TMA box
 constexpr int GM_BBOX_BYTES = GM_BBOX * GM_BK * 2;
-constexpr int GM_DQ_WARPS = 8;        // warps 0..7
-constexpr int GM_EPI_WARP0 = 8;       // warps 8..11
-constexpr int GM_RAW_WARP = 12;
-constexpr int GM_MMA_WARP = 13;
-constexpr int GM_B_WARP = 14;
-constexpr int GM_THREADS = 15 * 32;
-constexpr int GM_TMEM_COLS = 512;     // two accumulators of 256 fp32 columns
+constexpr int GM_DQ_WARPS = 16;       // warps 0..15: two groups of 8, alternate K steps
+constexpr int GM_DQ_GROUP = 8;        // unpacking warps per K step (4 lane quarters x 2 halves)
+constexpr int GM_EPI_WARP0 = 16;      // warps 16..19
+constexpr int GM_RAW_WARP = 20;
+constexpr int GM_MMA_WARP = 21;
+constexpr int GM_B_WARP = 22;
+constexpr int GM_THREADS = 23 * 32;
+constexpr int GM_TMEM_COLS = 512;     // accumulators, then the A stages
 constexpr int GM_SMEM_LIMIT = 227 * 1024;
 constexpr int MOE_MAX_EXPERTS = 512;
 
@@ -64,8 +69,11 @@ struct GemmArgs {
   int N;            // token rows of x_hat
   int nb;           // super-blocks per weight row
   int m_tiles, n_tiles, splits, bn;
-  int a_stages, b_stages, raw_stages;
+  int k_stages, raw_stages;  // K-step stages (A in tensor memory + B in shared memory), raw rings
   int b_stage_bytes;
+  int n_acc;        // tensor-memory accumulators (1 or 2)
+  int acc_cols;     // columns per accumulator
+  int a_col0;       // first tensor-memory column of the A stages
   float* Y;
   float* partial;   // split-K partial sums [splits][N][M]
   // MoE
@@ -128,20 +136,16 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs& a, int t, const int*
   return T;
 }
 
-// --- weight unpacking into the 128-byte-swizzled K-major fp16 A tile ----------
-// A tile: 128 rows x 64 fp16; 16-byte chunk c of row r lives at
-// r*128 + ((c ^ (r & 7)) << 4).
-__device__ __forceinline__ void store_chunk(uint8_t* a_tile, int r, int c, uint32_t o0, uint32_t o1, uint32_t o2,
-                                            uint32_t o3) {
-  *reinterpret_cast<uint4*>(a_tile + r * 128 + ((c ^ (r & 7)) << 4)) = make_uint4(o0, o1, o2, o3);
-}
+// --- weight unpacking into the fp16 A operand ---------------------------------
+// A stage: 128 rows (tensor-memory lanes) x 64 K of fp16, two per 32-bit
+// column, lower k in the low half. The thread of row r and half hf produces the
+// 32 weights k = 32hf .. 32hf+31 of the step as o[0..15] (columns 16hf + i).
 
 // Q4_K, K step s (0..3) of a super-block covers sub-blocks 2s (low nibbles of
-// qs[32s..32s+31]) and 2s+1 (high nibbles). Thread tid: row tid/2, sub-block
-// 2s + (tid&1), 32 weights w = d*sc*nib - dmin*m computed as one fp16 fma on
-// the exact nibble.
-__device__ __forceinline__ void dequant_q4k(const uint8_t* __restrict__ raw, int s, uint8_t* a_tile, int tid) {
-  const int r = tid >> 1, hf = tid & 1;
+// qs[32s..32s+31]) and 2s+1 (high nibbles): half hf is sub-block 2s + hf, 32
+// weights w = d*sc*nib - dmin*m computed as one fp16 fma on the exact nibble.
+__device__ __forceinline__ void dequant_q4k(const uint8_t* __restrict__ raw, int s, int r, int hf,
+                                            uint32_t (&o)[16]) {
   const uint8_t* blk = raw + r * Q4K_BYTES;
   const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
   const uint4 q0 = *reinterpret_cast<const uint4*>(blk + 16 + 32 * s);
@@ -165,28 +169,22 @@ __device__ __forceinline__ void dequant_q4k(const uint8_t* __restrict__ raw, int
   const __half2 k1024 = __float2half2_rn(1024.f);
   const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
-  for (int cc = 0; cc < 4; ++cc) {
-    uint32_t o[4];
-#pragma unroll
-    for (int ww = 0; ww < 2; ++ww) {
-      const uint32_t src = hf ? (w[2 * cc + ww] >> 4) : w[2 * cc + ww];
-      // bytes 0,1 (and 2,3) -> fp16 (1024 + nibble) pairs
-      const uint32_t t0 = __byte_perm(src, 0x64646464u, 0x5140) & 0xFF0FFF0Fu;
-      const uint32_t t1 = __byte_perm(src, 0x64646464u, 0x7362) & 0xFF0FFF0Fu;
-      o[2 * ww] = half2_bits(__hfma2(__hsub2(bits_half2(t0), k1024), scale2, negmin2));
-      o[2 * ww + 1] = half2_bits(__hfma2(__hsub2(bits_half2(t1), k1024), scale2, negmin2));
-    }
-    store_chunk(a_tile, r, 4 * hf + cc, o[0], o[1], o[2], o[3]);
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t src = hf ? (w[i] >> 4) : w[i];
+    // bytes 0,1 (and 2,3) -> fp16 (1024 + nibble) pairs
+    const uint32_t t0 = __byte_perm(src, 0x64646464u, 0x5140) & 0xFF0FFF0Fu;
+    const uint32_t t1 = __byte_perm(src, 0x64646464u, 0x7362) & 0xFF0FFF0Fu;
+    o[2 * i] = half2_bits(__hfma2(__hsub2(bits_half2(t0), k1024), scale2, negmin2));
+    o[2 * i + 1] = half2_bits(__hfma2(__hsub2(bits_half2(t1), k1024), scale2, negmin2));
   }
 }
 
 // Q6_K, K step s covers weights 64s..64s+63 of the super-block: half h = s/2,
-// quarters g = 2(s&1) and 2(s&1)+1. Thread tid: row tid/2, quarter
-// g = 2(s&1) + (tid&1), 32 weights d*sc*(q-32), q = 4 bits of ql | 2 bits of qh.
+// quarters g = 2(s&1) and 2(s&1)+1. Half gg of the step is quarter
+// g = 2(s&1) + gg: 32 weights d*sc*(q-32), q = 4 bits of ql | 2 bits of qh.
 // The block starts `rem` bytes into the row's 16-byte aligned window.
-__device__ __forceinline__ void dequant_q6k(const uint8_t* __restrict__ raw, int rem, int s, uint8_t* a_tile,
-                                            int tid) {
-  const int r = tid >> 1, gg = tid & 1;
+__device__ __forceinline__ void dequant_q6k(const uint8_t* __restrict__ raw, int rem, int s, int r, int gg,
+                                            uint32_t (&o)[16]) {
   const uint8_t* blk = raw + r * RawBox<KQ_Q6_K>::BYTES + rem;
   const int h = s >> 1, g = 2 * (s & 1) + gg;
   const int sh = (rem & 3) * 8;  // 0 or 16
@@ -213,20 +211,14 @@ __device__ __forceinline__ void dequant_q6k(const uint8_t* __restrict__ raw, int
   const __half2 k1056 = __float2half2_rn(1056.f);
   const bool low = (s & 1) == 0;  // quarters 0,1 use low nibbles, 2,3 high
 #pragma unroll
-  for (int cc = 0; cc < 4; ++cc) {
-    uint32_t o[4];
-#pragma unroll
-    for (int ww = 0; ww < 2; ++ww) {
-      const int i = 2 * cc + ww;
-      const uint32_t lo = low ? (ql[i] & 0x0F0F0F0Fu) : ((ql[i] >> 4) & 0x0F0F0F0Fu);
-      const uint32_t q = lo | (((qh[i] >> (2 * g)) & 0x03030303u) << 4);
-      const uint32_t t0 = __byte_perm(q, 0x64646464u, 0x5140);
-      const uint32_t t1 = __byte_perm(q, 0x64646464u, 0x7362);
-      const __half2 sc2 = (i < 4) ? s0 : s1;
-      o[2 * ww] = half2_bits(__hmul2(__hsub2(bits_half2(t0), k1056), sc2));
-      o[2 * ww + 1] = half2_bits(__hmul2(__hsub2(bits_half2(t1), k1056), sc2));
-    }
-    store_chunk(a_tile, r, 4 * gg + cc, o[0], o[1], o[2], o[3]);
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t lo = low ? (ql[i] & 0x0F0F0F0Fu) : ((ql[i] >> 4) & 0x0F0F0F0Fu);
+    const uint32_t q = lo | (((qh[i] >> (2 * g)) & 0x03030303u) << 4);
+    const uint32_t t0 = __byte_perm(q, 0x64646464u, 0x5140);
+    const uint32_t t1 = __byte_perm(q, 0x64646464u, 0x7362);
+    const __half2 sc2 = (i < 4) ? s0 : s1;
+    o[2 * i] = half2_bits(__hmul2(__hsub2(bits_half2(t0), k1056), sc2));
+    o[2 * i + 1] = half2_bits(__hmul2(__hsub2(bits_half2(t1), k1056), sc2));
   }
 }
 
@@ -237,17 +229,17 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
   constexpr int RAW_BYTES = RawBox<WT>::BYTES * GM_BM;
-  uint8_t* sA = smem;
-  uint8_t* sB = sA + a.a_stages * GM_A_BYTES;
-  uint8_t* sRaw = sB + a.b_stages * a.b_stage_bytes;
+  uint8_t* sB = smem;
+  uint8_t* sRaw = sB + a.k_stages * a.b_stage_bytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sRaw + a.raw_stages * RAW_BYTES);
   uint64_t* raw_full = bars;
   uint64_t* raw_empty = raw_full + a.raw_stages;
-  uint64_t* a_full = raw_empty + a.raw_stages;
-  uint64_t* a_empty = a_full + a.a_stages;
-  uint64_t* b_full = a_empty + a.a_stages;
-  uint64_t* b_empty = b_full + a.b_stages;
-  uint64_t* acc_full = b_empty + a.b_stages;
+  // One full/empty barrier pair per K step: the x_hat TMA (its transaction
+  // bytes and the producer's arrival) and the eight unpacking warps of the
+  // step complete `full`; one MMA commit frees both operands through `empty`.
+  uint64_t* k_full = raw_empty + a.raw_stages;
+  uint64_t* k_empty = k_full + a.k_stages;
+  uint64_t* acc_full = k_empty + a.k_stages;
   uint64_t* acc_empty = acc_full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -262,13 +254,9 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
       mbar_init(&raw_full[i], 1);
       mbar_init(&raw_empty[i], GM_DQ_WARPS);
     }
-    for (int i = 0; i < a.a_stages; ++i) {
-      mbar_init(&a_full[i], GM_DQ_WARPS);
-      mbar_init(&a_empty[i], 1);
-    }
-    for (int i = 0; i < a.b_stages; ++i) {
-      mbar_init(&b_full[i], 1);
-      mbar_init(&b_empty[i], 1);
+    for (int i = 0; i < a.k_stages; ++i) {
+      mbar_init(&k_full[i], 1 + GM_DQ_GROUP);
+      mbar_init(&k_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
@@ -285,7 +273,13 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmX);
   }
-  pdl_enter();
+  // Programmatic dependent launch: the dense GEMM's weight stream does not
+  // depend on the previous kernel (W is read-only; the caller's contract), so
+  // the raw producer starts at once; the x_hat producer and the epilogue wait
+  // for the previous grid below. The MoE tile tables come from the routing
+  // kernel, so every role of the MoE kernel waits here.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (MOE) asm volatile("griddepcontrol.wait;" ::: "memory");
   int total_tiles;
   if (MOE) {
     for (int i = threadIdx.x; i <= a.n_experts; i += GM_THREADS) s_tile_start[i] = a.tile_start[i];
@@ -324,6 +318,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
     }
   } else if (warp == GM_B_WARP) {
     // ---- activation producer -------------------------------------------------
+    if (!MOE) asm volatile("griddepcontrol.wait;" ::: "memory");  // x_hat comes from the previous kernel
     if (lane == 0) {
       int st = 0;
       uint32_t ph = 0;
@@ -332,12 +327,12 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
         const int nbox = (T.ncols + GM_BBOX - 1) / GM_BBOX;
         for (int kb = T.kb0; kb < T.kb1 && !*abort; ++kb) {
           for (int s = 0; s < 4; ++s) {
-            if (!mbar_wait(&b_empty[st], ph ^ 1, abort, a.err)) break;
-            mbar_expect_tx(&b_full[st], nbox * GM_BBOX_BYTES);
+            if (!mbar_wait(&k_empty[st], ph ^ 1, abort, a.err)) break;
+            mbar_expect_tx(&k_full[st], nbox * GM_BBOX_BYTES);
             for (int j = 0; j < nbox; ++j)
-              tma_load_2d(sB + st * a.b_stage_bytes + j * GM_BBOX_BYTES, &tmX, &b_full[st],
+              tma_load_2d(sB + st * a.b_stage_bytes + j * GM_BBOX_BYTES, &tmX, &k_full[st],
                           kb * QK_K + s * GM_BK, T.xrow0 + j * GM_BBOX);
-            if (++st == a.b_stages) {
+            if (++st == a.k_stages) {
               st = 0;
               ph ^= 1;
             }
@@ -349,44 +344,40 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
     // ---- tensor-core issuer --------------------------------------------------
     // The whole warp runs the loop converged, so descriptors and counters stay
     // warp-uniform; one elected lane issues the MMAs and commits.
-    int ast = 0, bst = 0;
-    uint32_t aph = 0, bph = 0;
+    int kst = 0;
+    uint32_t kph = 0;
     int it = 0;
-    const uint64_t a_desc0 = smem_desc_sw128(smem_u32(sA));
+    const uint32_t a_tmem0 = tmem_base + a.a_col0;
     const uint64_t b_desc0 = smem_desc_sw128(smem_u32(sB));
     for (int t = blockIdx.x; t < total_tiles && !*abort; t += gridDim.x, ++it) {
       const Tile T = decode_tile<MOE>(a, t, s_tile_start, s_counts, s_offsets);
-      const int acc = it & 1;
-      if (!mbar_wait(&acc_empty[acc], ((it >> 1) & 1) ^ 1, abort, a.err)) break;
+      const int acc = (a.n_acc == 2) ? (it & 1) : 0;
+      const uint32_t acc_ph = (a.n_acc == 2) ? ((it >> 1) & 1) : (it & 1);
+      if (!mbar_wait(&acc_empty[acc], acc_ph ^ 1, abort, a.err)) break;
       tc_fence_after();
-      const uint32_t d_tmem = tmem_base + acc * GM_BNMAX;
+      const uint32_t d_tmem = tmem_base + acc * a.acc_cols;
       const uint32_t idesc = idesc_f16_f32(GM_BM, (T.ncols + 15) & ~15);
       const int nsteps = (T.kb1 - T.kb0) * 4;
       bool ok = true;
       for (int ks = 0; ks < nsteps; ++ks) {
-        if (!mbar_wait(&a_full[ast], aph, abort, a.err) || !mbar_wait(&b_full[bst], bph, abort, a.err)) {
+        if (!mbar_wait(&k_full[kst], kph, abort, a.err)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        // start address field advances by bytes / 16
-        const uint64_t ad = a_desc0 + static_cast<uint64_t>((ast * GM_A_BYTES) >> 4);
-        const uint64_t bd = b_desc0 + static_cast<uint64_t>((bst * a.b_stage_bytes) >> 4);
+        // B: the start address field advances by bytes / 16; A: 8 columns per K=16
+        const uint32_t at = a_tmem0 + kst * GM_A_COLS;
+        const uint64_t bd = b_desc0 + static_cast<uint64_t>((kst * a.b_stage_bytes) >> 4);
         if (elect_one()) {
 #pragma unroll
           for (int k = 0; k < GM_BK / 16; ++k)  // +32 bytes per K=16 step inside the 128-byte row
-            umma_f16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (ks == 0 && k == 0) ? 0u : 1u);
-          umma_commit(&a_empty[ast]);
-          umma_commit(&b_empty[bst]);
+            umma_f16_ta(d_tmem, at + 8 * k, bd + 2 * k, idesc, (ks == 0 && k == 0) ? 0u : 1u);
+          umma_commit(&k_empty[kst]);
         }
         __syncwarp();
-        if (++ast == a.a_stages) {
-          ast = 0;
-          aph ^= 1;
-        }
-        if (++bst == a.b_stages) {
-          bst = 0;
-          bph ^= 1;
+        if (++kst == a.k_stages) {
+          kst = 0;
+          kph ^= 1;
         }
       }
       if (elect_one()) umma_commit(&acc_full[acc]);
@@ -395,25 +386,33 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
     }
   } else if (warp < GM_DQ_WARPS) {
     // ---- weight unpackers ----------------------------------------------------
-    const int tid = threadIdx.x;  // 0..255
-    int rst = 0, ast = 0;
+    // warp w owns tensor-memory lanes 32 (w % 4) .. +31 (rows of the tile), the
+    // half (w / 4) % 2 of a K step, and the K steps of parity w / 8
+    const int r = 32 * (warp & 3) + lane, hf = (warp >> 2) & 1, grp = warp >> 3;
+    const uint32_t a_row = tmem_base + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + a.a_col0 + 16 * hf;
+    int rst = 0, ast = 0, gs = 0;
     uint32_t rph = 0, aph = 0;
     for (int t = blockIdx.x; t < total_tiles && !*abort; t += gridDim.x) {
       const Tile T = decode_tile<MOE>(a, t, s_tile_start, s_counts, s_offsets);
       for (int kb = T.kb0; kb < T.kb1 && !*abort; ++kb) {
         if (!mbar_wait(&raw_full[rst], rph, abort, a.err)) break;
         const uint8_t* raw = sRaw + rst * RAW_BYTES;
-        for (int s = 0; s < 4; ++s) {
-          if (!mbar_wait(&a_empty[ast], aph ^ 1, abort, a.err)) break;
-          uint8_t* at = sA + ast * GM_A_BYTES;
-          if (WT == KQ_Q4_K)
-            dequant_q4k(raw, s, at, tid);
-          else
-            dequant_q6k(raw, (kb * Q6K_BYTES) & 15, s, at, tid);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&a_full[ast]);
-          if (++ast == a.a_stages) {
+        for (int s = 0; s < 4; ++s, ++gs) {
+          if ((gs & 1) == grp) {
+            if (!mbar_wait(&k_empty[ast], aph ^ 1, abort, a.err)) break;
+            tc_fence_after();
+            uint32_t o[16];
+            if (WT == KQ_Q4_K)
+              dequant_q4k(raw, s, r, hf, o);
+            else
+              dequant_q6k(raw, (kb * Q6K_BYTES) & 15, s, r, hf, o);
+            tmem_st_32x32b_x16(a_row + ast * GM_A_COLS, o);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&k_full[ast]);
+          }
+          if (++ast == a.k_stages) {
             ast = 0;
             aph ^= 1;
           }
@@ -428,18 +427,20 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
     }
   } else {
     // ---- epilogue: tensor memory -> fp32 Y -----------------------------------
+    if (!MOE) asm volatile("griddepcontrol.wait;" ::: "memory");  // Y may still be read by the previous kernel
     const int wq = warp - GM_EPI_WARP0;  // == warp % 4: this warp's 32 TMEM lanes
     int it = 0;
     for (int t = blockIdx.x; t < total_tiles && !*abort; t += gridDim.x, ++it) {
       const Tile T = decode_tile<MOE>(a, t, s_tile_start, s_counts, s_offsets);
-      const int acc = it & 1;
-      if (!mbar_wait(&acc_full[acc], (it >> 1) & 1, abort, a.err)) break;
+      const int acc = (a.n_acc == 2) ? (it & 1) : 0;
+      const uint32_t acc_ph = (a.n_acc == 2) ? ((it >> 1) & 1) : (it & 1);
+      if (!mbar_wait(&acc_full[acc], acc_ph, abort, a.err)) break;
       tc_fence_after();
       const int m = T.m0 + 32 * wq + lane;
       const bool mok = m < a.M;
       for (int c0 = 0; c0 < T.ncols; c0 += 32) {
         uint32_t r[32];
-        tmem_ld_32x32b_x32(tmem_base + acc * GM_BNMAX + (static_cast<uint32_t>(32 * wq) << 16) + c0, r);
+        tmem_ld_32x32b_x32(tmem_base + acc * a.acc_cols + (static_cast<uint32_t>(32 * wq) << 16) + c0, r);
         tmem_ld_wait();
         if (MOE) {
           const int my_slot = (c0 + lane < T.ncols) ? __ldg(a.entries + T.nbase + c0 + lane) : 0;
@@ -654,39 +655,34 @@ bool encode_tmap_2d(CUtensorMap* tm, CUtensorMapDataType dtype, const void* base
 
 static int raw_box_bytes(int wtype) { return wtype == KQ_Q4_K ? RawBox<KQ_Q4_K>::BYTES : RawBox<KQ_Q6_K>::BYTES; }
 
-// Ring depths for a token tile of bn rows. The x_hat (B) ring comes first: its
-// TMA round trip (L2 -> shared memory, 1-2k cycles) must be covered by the MMA
-// time of the stages in flight, which at bn = 256 takes four 64-K stages. Then
-// three A stages (weights unpacked by the CUDA cores) and up to four raw weight
-// super-blocks (each feeds four K steps; they come from HBM). Whatever shared
-// memory is left deepens the A and B rings.
+// Tensor memory: the accumulators (two when that leaves room for four A stages,
+// so the epilogue of one tile overlaps the next tile's MMAs), then up to eight
+// 64-K A stages of 32 columns. Shared memory: the x_hat (B) ring, whose L2 ->
+// shared memory round trip (1-2k cycles) the stages in flight must cover, and
+// the raw weight ring (each super-block feeds four K steps; they come from HBM).
 static bool choose_stages(int wtype, int bn, int n_experts, GemmArgs* a, size_t* smem) {
+  const int acc_cols = (bn + 15) & ~15;
+  a->n_acc = (2 * acc_cols + 4 * GM_A_COLS <= GM_TMEM_COLS) ? 2 : 1;
+  a->acc_cols = acc_cols;
+  a->a_col0 = a->n_acc * acc_cols;
+  const int a_max = std::min(GM_A_MAX_STAGES, (GM_TMEM_COLS - a->a_col0) / GM_A_COLS);
+  if (a_max < 2) return false;
   const int b_bytes = ((bn + GM_BBOX - 1) / GM_BBOX) * GM_BBOX_BYTES;
   const int raw_bytes = raw_box_bytes(wtype) * GM_BM;
   const int tables = (n_experts > 0 ? 3 * (n_experts + 1) * 4 : 0) + 64;
   const int budget = GM_SMEM_LIMIT - (1024 + tables + 512);
-  auto bytes = [&](int bs, int as, int rs) { return bs * b_bytes + as * GM_A_BYTES + rs * raw_bytes; };
-  int bs = 4, as = 3, rs = 2;
-  while (bs > 2 && bytes(bs, as, rs) > budget) --bs;
-  if (bytes(bs, as, rs) > budget) as = 2;
-  if (bytes(bs, as, rs) > budget) return false;
-  while (rs < 4 && bytes(bs, as, rs + 1) <= budget) ++rs;
-  for (bool grew = true; grew;) {
-    grew = false;
-    if (as < 6 && bytes(bs, as + 1, rs) <= budget) {
-      ++as;
-      grew = true;
-    }
-    if (bs < 8 && bytes(bs + 1, as, rs) <= budget) {
-      ++bs;
-      grew = true;
-    }
-  }
-  a->b_stages = bs;
-  a->a_stages = as;
+  auto bytes = [&](int bs, int rs) { return bs * b_bytes + rs * raw_bytes; };
+  // The B ring gets priority: an x_hat stage takes ~1.4k cycles from issue to
+  // arrival under load while the MMAs consume one every ~560 cycles (N = 256),
+  // so about five must be in flight; two raw stages already cover eight K steps.
+  int bs = 2, rs = 2;
+  if (bytes(bs, rs) > budget) return false;
+  while (bs < a_max && bytes(bs + 1, rs) <= budget) ++bs;
+  while (rs < 4 && bytes(bs, rs + 1) <= budget) ++rs;
+  a->k_stages = bs;
   a->raw_stages = rs;
   a->b_stage_bytes = b_bytes;
-  *smem = static_cast<size_t>(bytes(bs, as, rs) + 1024 + tables + 512);
+  *smem = static_cast<size_t>(bytes(bs, rs) + 1024 + tables + 512);
   return true;
 }
 
