@@ -499,12 +499,14 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restr
 
 // ---------------------------------------------------------------------------
 // MoE routing ("Prefill Gap Closure Plan", T2 step 1; "ZINC MMQ v2", MoE
-// routing): histogram of expert ids -> exclusive prefix sum -> scatter of the
-// (token, slot) ids into per-expert buckets, in token-then-slot order. One CTA;
-// warp w owns a contiguous range of slots, so per-warp counts plus two scans
-// give every slot its bucket position without atomics (deterministic).
-// Also lays out the tile list: expert e owns m_tiles * ceil(count_e / bn)
-// consecutive tiles starting at tile_start[e].
+// routing): histogram of expert ids -> exclusive prefix sum -> a bucket
+// position for every (token, slot) id. One CTA, shared-memory atomics; the
+// positions are written in slot order (coalesced) and the gather kernel that
+// follows scatters the rows and the slot ids. The order of slots inside a
+// bucket depends on the atomics, but no result does: a slot's output row is
+// the same dot products wherever it sits in its expert's tile. Also lays out
+// the tile list: expert e owns m_tiles * ceil(count_e / bn) consecutive tiles
+// starting at tile_start[e].
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ int block_excl_scan_1024(int v, int* wsum, int* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -532,95 +534,69 @@ __device__ __forceinline__ int block_excl_scan_1024(int v, int* wsum, int* total
   return excl;
 }
 
+constexpr int ROUTE_IDS_PER_THREAD = 16;  // ids held in registers between the two passes
+
 __global__ void __launch_bounds__(1024) moe_route_kernel(const int* __restrict__ ids, int n, int top_k, int E,
                                                          int m_tiles, int bn, int* counts, int* offsets,
-                                                         int* tile_start, int* entries, int* src, float* Y, int M,
-                                                         int* err) {
+                                                         int* tile_start, int* slot_pos, float* Y, int M, int* err) {
   extern __shared__ int rsm[];
-  int* cnt = rsm;                 // [32][E]: per-warp counts, then per-warp bases
-  int* base = cnt + 32 * E;       // [E]: bucket start
-  int* wsum = base + E;           // [32]
+  int* cnt = rsm;        // [E]: histogram, then the scatter cursor of each bucket
+  int* wsum = cnt + E;   // [32]
   pdl_enter();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int i = threadIdx.x; i < 32 * E; i += 1024) cnt[i] = 0;
+  for (int i = threadIdx.x; i < E; i += 1024) cnt[i] = 0;
   __syncthreads();
-  const int L = (((n + 31) / 32) + 31) & ~31;
-  const int lo = min(n, warp * L), hi = min(n, lo + L);
-  // pass 1: per-warp counts; ids are fetched 8 per lane at a time so the loads overlap
-  for (int r0 = lo; r0 < hi; r0 += 256) {
-    int e[8];
+  // pass 1: histogram (ids beyond 16 per thread are re-read in pass 2)
+  int e_reg[ROUTE_IDS_PER_THREAD];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int i = r0 + 32 * j + lane;
-      e[j] = (i < hi) ? __ldg(ids + i) : -1;
-    }
+  for (int j = 0; j < ROUTE_IDS_PER_THREAD; ++j) {
+    const int i = threadIdx.x + 1024 * j;
+    e_reg[j] = (i < n) ? __ldg(ids + i) : -1;
+  }
+  for (int i0 = 0; i0 < n; i0 += 1024 * ROUTE_IDS_PER_THREAD) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int i = r0 + 32 * j + lane;
-      int ej = e[j];
-      if (i < hi && (ej < 0 || ej >= E)) {
+    for (int j = 0; j < ROUTE_IDS_PER_THREAD; ++j) {
+      const int i = i0 + threadIdx.x + 1024 * j;
+      if (i >= n) continue;
+      const int e = (i0 == 0) ? e_reg[j] : __ldg(ids + i);
+      if (e < 0 || e >= E)
         report_error(err, ERR_EXPERT_ID);
-        ej = -1;
-      }
-      const unsigned peers = __match_any_sync(0xffffffffu, ej);
-      if (ej >= 0 && lane == __ffs(peers) - 1) cnt[warp * E + ej] += __popc(peers);
-      __syncwarp();
+      else
+        atomicAdd(&cnt[e], 1);
     }
   }
   __syncthreads();
-  int tot = 0;
-  if (threadIdx.x < E) {
-    const int e = threadIdx.x;
-    for (int w = 0; w < 32; ++w) {
-      const int c = cnt[w * E + e];
-      cnt[w * E + e] = tot;
-      tot += c;
-    }
-  }
+  const int tot = threadIdx.x < E ? cnt[threadIdx.x] : 0;
   int n_valid, n_tiles;
-  const int off = block_excl_scan_1024(threadIdx.x < E ? tot : 0, wsum, &n_valid);
+  const int off = block_excl_scan_1024(tot, wsum, &n_valid);
   const int my_tiles = threadIdx.x < E ? m_tiles * ((tot + bn - 1) / bn) : 0;
   const int toff = block_excl_scan_1024(my_tiles, wsum, &n_tiles);
   if (threadIdx.x < E) {
     counts[threadIdx.x] = tot;
     offsets[threadIdx.x] = off;
     tile_start[threadIdx.x] = toff;
-    base[threadIdx.x] = off;
+    cnt[threadIdx.x] = off;  // scatter cursor
   }
   if (threadIdx.x == 0) {
     offsets[E] = n_valid;
     tile_start[E] = n_tiles;
   }
   __syncthreads();
-  // pass 2: scatter in (token, slot) order
-  const unsigned lt = (1u << lane) - 1u;
-  for (int r0 = lo; r0 < hi; r0 += 256) {
-    int e[8];
+  // pass 2: bucket positions (-1 for an invalid id, whose output row is zeroed)
+  for (int i0 = 0; i0 < n; i0 += 1024 * ROUTE_IDS_PER_THREAD) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int i = r0 + 32 * j + lane;
-      e[j] = (i < hi) ? __ldg(ids + i) : -1;
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int i = r0 + 32 * j + lane;
-      int ej = e[j];
-      const bool bad = (i < hi) && (ej < 0 || ej >= E);
-      if (bad) ej = -1;
-      const unsigned peers = __match_any_sync(0xffffffffu, ej);
-      if (ej >= 0) {
-        const int pos = base[ej] + cnt[warp * E + ej] + __popc(peers & lt);
-        entries[pos] = i;
-        src[pos] = i / top_k;
-      }
-      __syncwarp();
-      if (ej >= 0 && lane == __ffs(peers) - 1) cnt[warp * E + ej] += __popc(peers);
-      __syncwarp();
-      if (bad)
+    for (int j = 0; j < ROUTE_IDS_PER_THREAD; ++j) {
+      const int i = i0 + threadIdx.x + 1024 * j;
+      if (i >= n) continue;
+      const int e = (i0 == 0) ? e_reg[j] : __ldg(ids + i);
+      if (e < 0 || e >= E) {
+        slot_pos[i] = -1;
         for (int m = 0; m < M; ++m) Y[static_cast<int64_t>(i) * M + m] = 0.f;
+        continue;
+      }
+      slot_pos[i] = atomicAdd(&cnt[e], 1);
     }
   }
-  for (int p = n_valid + threadIdx.x; p < n; p += 1024) src[p] = -1;
+  (void)top_k;
 }
 
 // ---------------------------------------------------------------------------
@@ -746,7 +722,7 @@ cudaError_t launch_gemm(int wtype, const void* W, const float* X, float* Y, int6
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   __half* xh = reinterpret_cast<__half*>(wsb);
   float* partial = reinterpret_cast<float*>(wsb + plan.xhat_bytes);
-  cudaError_t e = launch_quantize_xhat(X, xh, K, N, nullptr, s);
+  cudaError_t e = launch_quantize_xhat(X, xh, K, N, plan.grid, s);
   if (e != cudaSuccess) return e;
   CUtensorMap tmW, tmX;
   if (!weight_tmap(&tmW, wtype, W, M, K) || !xhat_tmap(&tmX, xh, N, K)) {
@@ -781,7 +757,8 @@ cudaError_t launch_gemm(int wtype, const void* W, const float* X, float* Y, int6
   return e;
 }
 
-// MoE workspace: counts[E] | offsets[E+1] | tile_start[E+1] | entries[n] | src[n] | x_hat[n][K] fp16
+// MoE workspace: counts[E] | offsets[E+1] | tile_start[E+1] | entries[n] (slot of each bucket row) |
+// slot_pos[n] (bucket row of each slot) | x_hat[n][K] fp16 (bucket order)
 MoePlan plan_moe(int wtype, int64_t M, int64_t K, int64_t T, int n_experts, int top_k) {
   (void)wtype;
   MoePlan p{};
@@ -819,17 +796,17 @@ cudaError_t launch_moe(int wtype, const void* W, int n_experts, const int32_t* i
   int* offsets = reinterpret_cast<int*>(wsb + plan.off_offsets);
   int* tile_start = reinterpret_cast<int*>(wsb + plan.off_tiles);
   int* entries = reinterpret_cast<int*>(wsb + plan.off_entries);
-  int* src = reinterpret_cast<int*>(wsb + plan.off_src);
+  int* slot_pos = reinterpret_cast<int*>(wsb + plan.off_src);
   __half* xh = reinterpret_cast<__half*>(wsb + plan.off_xhat);
   const int64_t n = T * top_k;
 
-  const size_t rsmem = static_cast<size_t>(32 * n_experts + n_experts + 32) * sizeof(int);
+  const size_t rsmem = static_cast<size_t>(n_experts + 32) * sizeof(int);
   cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(moe_route_kernel), 8);
   if (e != cudaSuccess) return e;
   e = launch_pdl(moe_route_kernel, dim3(1), dim3(1024), rsmem, s, ids, static_cast<int>(n), top_k, n_experts,
-                 plan.m_tiles, MOE_BN, counts, offsets, tile_start, entries, src, Y, static_cast<int>(M), err);
+                 plan.m_tiles, MOE_BN, counts, offsets, tile_start, slot_pos, Y, static_cast<int>(M), err);
   if (e != cudaSuccess) return e;
-  e = launch_quantize_xhat(X, xh, K, n, src, s);
+  e = launch_gather_xhat(X, xh, K, n, top_k, slot_pos, entries, num_sms, s);
   if (e != cudaSuccess) return e;
 
   CUtensorMap tmW, tmX;

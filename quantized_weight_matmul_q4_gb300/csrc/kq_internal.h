@@ -11,8 +11,11 @@
 namespace kq {
 
 cudaError_t launch_quantize_q8_1(const float* X, void* Xq, int64_t K, int64_t N, cudaStream_t s);
-cudaError_t launch_quantize_xhat(const float* X, __half* Xh, int64_t K, int64_t rows, const int* src_rows,
-                                 cudaStream_t s);
+cudaError_t launch_quantize_xhat(const float* X, __half* Xh, int64_t K, int64_t rows, int num_sms, cudaStream_t s);
+// MoE: for every slot i with bucket row p = slot_pos[i] >= 0, writes the x_hat
+// of token i / top_k to row p of Xh and entries[p] = i.
+cudaError_t launch_gather_xhat(const float* X, __half* Xh, int64_t K, int64_t n_slots, int top_k,
+                               const int* slot_pos, int* entries, int num_sms, cudaStream_t s);
 cudaError_t launch_matvec(int wtype, const void* W, const float* x, float* y, int64_t M, int64_t K, int* err,
                           int num_sms, cudaStream_t s, int* status);
 

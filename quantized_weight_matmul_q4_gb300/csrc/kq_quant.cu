@@ -25,34 +25,84 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float* __restr
   }
 }
 
-// Output row p of Xh (fp16 [rows][K]) is the Q8_1 value of input row
-// src_rows[p] (or row p when src_rows is null); a negative source row gives
-// zeros. Each x_hat = fp16(d_h * q): the product is exact in fp32 and is
+// x_hat = fp16(d_h * q) of four values: the product is exact in fp32 and is
 // rounded once.
+__device__ __forceinline__ uint2 xhat4(const Q8Quad& r) {
+  const __half2 h01 = __halves2half2(__float2half_rn(__fmul_rn(r.dh, static_cast<float>(r.q[0]))),
+                                     __float2half_rn(__fmul_rn(r.dh, static_cast<float>(r.q[1]))));
+  const __half2 h23 = __halves2half2(__float2half_rn(__fmul_rn(r.dh, static_cast<float>(r.q[2]))),
+                                     __float2half_rn(__fmul_rn(r.dh, static_cast<float>(r.q[3]))));
+  return make_uint2(half2_bits(h01), half2_bits(h23));
+}
+
+constexpr int XH_UNROLL = 4;   // quads in flight per thread
+constexpr int XH_CTAS_PER_SM = 8;
+
+// Output row p of Xh (fp16 [rows][K]) is the Q8_1 value of input row p. Quads
+// (4 values) are strided over a grid of a few CTAs per SM, XH_UNROLL loads in
+// flight per thread. K / 4 is a multiple of 64 and the stride a multiple of 32,
+// so a warp's 32 quads always lie in one row and take the same path.
 __global__ void __launch_bounds__(256) quantize_xhat_kernel(const float* __restrict__ X, __half* __restrict__ Xh,
-                                                            int K, int64_t rows, const int* __restrict__ src_rows) {
+                                                            int K, int64_t rows) {
   pdl_enter();
-  const int64_t t = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;  // quad index in the output
+  const int64_t total = rows * (K >> 2);
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * 256;
+  for (int64_t t0 = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x; t0 < total; t0 += XH_UNROLL * stride) {
+    float4 v[XH_UNROLL];
+#pragma unroll
+    for (int u = 0; u < XH_UNROLL; ++u) {
+      const int64_t t = t0 + u * stride;
+      if (t < total) v[u] = __ldg(reinterpret_cast<const float4*>(X) + t);
+    }
+#pragma unroll
+    for (int u = 0; u < XH_UNROLL; ++u) {
+      const int64_t t = t0 + u * stride;
+      if (t < total) reinterpret_cast<uint2*>(Xh)[t] = xhat4(quantize_quad(v[u]));
+    }
+  }
+}
+
+// MoE gather: quad c of slot i quantises x[i / top_k][4c .. 4c+3] and writes
+// it to bucket row slot_pos[i] (skipped when negative); the first quad of a
+// slot also records entries[slot_pos[i]] = i. One quad per thread: many short
+// CTAs, so the grouped GEMM that follows can take SMs as they free up. K / 4 is
+// a multiple of 64, so a warp's quads belong to one slot and take one path.
+__global__ void __launch_bounds__(256) gather_xhat_kernel(const float* __restrict__ X, __half* __restrict__ Xh,
+                                                          int K, int64_t n_slots, int top_k,
+                                                          const int* __restrict__ slot_pos, int* __restrict__ entries) {
+  pdl_enter();
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
   const int64_t kq4 = K >> 2;
-  const int64_t row = t / kq4;
-  const int64_t col = (t - row * kq4) << 2;
-  bool valid = row < rows;
-  float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (valid) {
-    const int64_t src = src_rows ? static_cast<int64_t>(__ldg(src_rows + row)) : row;
-    if (src >= 0) v = __ldg(reinterpret_cast<const float4*>(X + src * K + col));
-  }
-  const Q8Quad r = quantize_quad(v);
-  if (valid) {
-    const __half2 h01 = __halves2half2(__float2half_rn(__fmul_rn(r.dh, static_cast<float>(r.q[0]))),
-                                       __float2half_rn(__fmul_rn(r.dh, static_cast<float>(r.q[1]))));
-    const __half2 h23 = __halves2half2(__float2half_rn(__fmul_rn(r.dh, static_cast<float>(r.q[2]))),
-                                       __float2half_rn(__fmul_rn(r.dh, static_cast<float>(r.q[3]))));
-    uint2 o;
-    o.x = half2_bits(h01);
-    o.y = half2_bits(h23);
-    *reinterpret_cast<uint2*>(Xh + row * K + col) = o;
-  }
+  const int64_t i = t / kq4;
+  const int64_t c = t - i * kq4;
+  if (i >= n_slots) return;
+  const int pos = __ldg(slot_pos + i);
+  if (pos < 0) return;
+  const float4 v = __ldg(reinterpret_cast<const float4*>(X + (i / top_k) * K) + c);
+  reinterpret_cast<uint2*>(Xh + static_cast<int64_t>(pos) * K)[c] = xhat4(quantize_quad(v));
+  if (c == 0) entries[pos] = static_cast<int>(i);
+}
+
+static unsigned xhat_grid(int64_t quads, int num_sms) {
+  const int64_t need = (quads + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(num_sms) * XH_CTAS_PER_SM;
+  return static_cast<unsigned>(need < cap ? need : cap);
+}
+
+cudaError_t launch_quantize_xhat(const float* X, __half* Xh, int64_t K, int64_t rows, int num_sms, cudaStream_t s) {
+  const int64_t quads = rows * (K / 4);
+  if (quads == 0) return cudaSuccess;
+  return launch_pdl(quantize_xhat_kernel, dim3(xhat_grid(quads, num_sms)), dim3(256), 0, s, X, Xh,
+                    static_cast<int>(K), rows);
+}
+
+cudaError_t launch_gather_xhat(const float* X, __half* Xh, int64_t K, int64_t n_slots, int top_k,
+                               const int* slot_pos, int* entries, int num_sms, cudaStream_t s) {
+  (void)num_sms;
+  const int64_t quads = n_slots * (K / 4);
+  if (quads == 0) return cudaSuccess;
+  return launch_pdl(gather_xhat_kernel, dim3(static_cast<unsigned>((quads + 255) / 256)), dim3(256), 0, s, X, Xh,
+                    static_cast<int>(K), n_slots, top_k, slot_pos, entries);
 }
 
 cudaError_t launch_quantize_q8_1(const float* X, void* Xq, int64_t K, int64_t N, cudaStream_t s) {
@@ -64,13 +114,5 @@ cudaError_t launch_quantize_q8_1(const float* X, void* Xq, int64_t K, int64_t N,
                     static_cast<uint8_t*>(Xq), nblk);
 }
 
-cudaError_t launch_quantize_xhat(const float* X, __half* Xh, int64_t K, int64_t rows, const int* src_rows,
-                                 cudaStream_t s) {
-  const int64_t threads = rows * (K / 4);
-  const int64_t grid = (threads + 255) / 256;
-  if (grid == 0) return cudaSuccess;
-  return launch_pdl(quantize_xhat_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, s, X, Xh,
-                    static_cast<int>(K), rows, src_rows);
-}
 
 }  // namespace kq
