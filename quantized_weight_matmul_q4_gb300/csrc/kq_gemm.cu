@@ -61,7 +61,11 @@ struct RawBox<KQ_Q4_K> {
 };
 template <>
 struct RawBox<KQ_Q6_K> {
-  static constexpr int BYTES = 224;  // a 16-byte aligned window covering one 210-byte Q6_K block
+  // A 16-byte aligned window covering one 210-byte Q6_K block (which starts up
+  // to 14 bytes in). 240 bytes = 60 words: the unpackers' 32-bit loads of 32
+  // consecutive rows then fall on 8 distinct banks per 8 rows (4-way at most),
+  // where a 224-byte pitch gives 8-way conflicts.
+  static constexpr int BYTES = 240;
 };
 
 struct GemmArgs {
@@ -179,30 +183,54 @@ __device__ __forceinline__ void dequant_q4k(const uint8_t* __restrict__ raw, int
   }
 }
 
+// The 8 words that start d bytes into the 48-byte window w (d even, < 16; the
+// same d for every thread of a K-block, so the branch does not diverge).
+__device__ __forceinline__ void window_words(const uint32_t (&w)[12], int d, uint32_t (&out)[8]) {
+  const int sh = (d & 3) * 8;
+  switch (d >> 2) {
+    case 0:
+#pragma unroll
+      for (int i = 0; i < 8; ++i) out[i] = __funnelshift_r(w[i], w[i + 1], sh);
+      break;
+    case 1:
+#pragma unroll
+      for (int i = 0; i < 8; ++i) out[i] = __funnelshift_r(w[i + 1], w[i + 2], sh);
+      break;
+    case 2:
+#pragma unroll
+      for (int i = 0; i < 8; ++i) out[i] = __funnelshift_r(w[i + 2], w[i + 3], sh);
+      break;
+    default:
+#pragma unroll
+      for (int i = 0; i < 8; ++i) out[i] = __funnelshift_r(w[i + 3], w[i + 4], sh);
+      break;
+  }
+}
+
 // Q6_K, K step s covers weights 64s..64s+63 of the super-block: half h = s/2,
 // quarters g = 2(s&1) and 2(s&1)+1. Half gg of the step is quarter
 // g = 2(s&1) + gg: 32 weights d*sc*(q-32), q = 4 bits of ql | 2 bits of qh.
-// The block starts `rem` bytes into the row's 16-byte aligned window.
+// The block starts `rem` bytes into the row's 16-byte aligned window; its ql
+// and qh bytes are fetched as three aligned 16-byte loads each (with the
+// 240-byte row pitch, 8 consecutive rows hit 8 distinct bank groups).
 __device__ __forceinline__ void dequant_q6k(const uint8_t* __restrict__ raw, int rem, int s, int r, int gg,
                                             uint32_t (&o)[16]) {
-  const uint8_t* blk = raw + r * RawBox<KQ_Q6_K>::BYTES + rem;
+  const uint8_t* row = raw + r * RawBox<KQ_Q6_K>::BYTES;
+  const uint8_t* blk = row + rem;
   const int h = s >> 1, g = 2 * (s & 1) + gg;
-  const int sh = (rem & 3) * 8;  // 0 or 16
-  const uint32_t* pl = reinterpret_cast<const uint32_t*>(blk - (rem & 3) + 64 * h + 32 * (g & 1));
-  const uint32_t* ph = reinterpret_cast<const uint32_t*>(blk - (rem & 3) + 128 + 32 * h);
   uint32_t ql[8], qh[8];
   {
-    uint32_t a[9], b[9];
+    const uint4* pl = reinterpret_cast<const uint4*>(row + 64 * h + 32 * (g & 1));
+    const uint4* ph = reinterpret_cast<const uint4*>(row + 128 + 32 * h);
+    uint32_t a[12], b[12];
 #pragma unroll
-    for (int i = 0; i < 9; ++i) {
-      a[i] = pl[i];
-      b[i] = ph[i];
+    for (int k = 0; k < 3; ++k) {
+      const uint4 x = pl[k], y = ph[k];
+      a[4 * k] = x.x; a[4 * k + 1] = x.y; a[4 * k + 2] = x.z; a[4 * k + 3] = x.w;
+      b[4 * k] = y.x; b[4 * k + 1] = y.y; b[4 * k + 2] = y.z; b[4 * k + 3] = y.w;
     }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      ql[i] = __funnelshift_r(a[i], a[i + 1], sh);
-      qh[i] = __funnelshift_r(b[i], b[i + 1], sh);
-    }
+    window_words(a, rem, ql);
+    window_words(b, rem, qh);
   }
   const float d = __half2float(*reinterpret_cast<const __half*>(blk + 208));
   const int8_t* scp = reinterpret_cast<const int8_t*>(blk + 192 + 8 * h + 2 * g);
