@@ -7,7 +7,7 @@ fused). A step is one decode sweep over 8 rotated weight copies of each shape
 (16 launches, 406 MB of weights: larger than the 129 MB L2, so no flush is
 needed). Extra keys report the prefill GEMMs (N = 64, 512, 2048; Q4_K and Q6_K)
 and the MoE grouped GEMM as TFLOP/s, each call timed cold (L2 flushed between
-calls).
+calls: a 256 MB write, then a 256 MB read so no dirty flush data is left).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -346,6 +346,9 @@ def run_ours(args, dist):
                     + ("" if args.eager else ", replayed as one CUDA graph"),
             "l2": "inputs larger than L2 (8 weight copies per shape, 406 MB of weights)",
             "parallelism": f"replicas x{dist.world}",
+            "sections": "prefill/MoE calls: each captured once as a CUDA graph and replayed with L2 flushed "
+                        "before every replay (256 MB written, then another 256 MB read, so the flush's dirty "
+                        "lines are written back before the timed region); ms_eager: the same call launched eagerly",
         },
         "roofline": {
             "kernel": "matvec_q4k_lanerow_kernel",
@@ -374,23 +377,51 @@ def run_ours(args, dist):
 
 
 def _timed_calls(fn, iters, warm, flush, torch, stream):
-    """Mean device time (ms) of fn() over iters calls, L2 flushed before each."""
+    """Device time (ms) of one fn() call, L2 flushed before each: the call is
+    captured once as a CUDA graph and replayed (mean, min over iters), and the
+    same is measured for eager calls (mean), which adds host launch latency."""
     for _ in range(warm):
         fn()
-    times = []
-    for _ in range(iters):
-        flush.zero_()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
+    torch.cuda.synchronize()
+
+    def timed(call):
+        times = []
+        for _ in range(iters):
+            flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(torch.cuda.current_stream())
+            call()
+            b.record(torch.cuda.current_stream())
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b))
+        return times
+
+    eager = timed(fn)
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
         fn()
-        b.record(stream)
-        torch.cuda.synchronize()
-        times.append(a.elapsed_time(b))
-    return statistics.mean(times), min(times)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        fn()
+    g.replay()
+    torch.cuda.synchronize()
+    graph = timed(g.replay)
+    return statistics.mean(graph), min(graph), statistics.mean(eager)
 
 
 def run_sections(args, kq, syn, torch, dev, stream, pk, only=None):
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # 256 MB > L2
+    # L2 flush between timed calls: write 256 MB (> L2), then read another
+    # 256 MB, so L2 holds only clean lines when the call starts (the write-back
+    # of the dirty flush data is paid before the timed region, not inside it).
+    flush_w = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush_r = torch.zeros(64 << 20, dtype=torch.int32, device=dev)
+
+    def flush():
+        flush_w.zero_()
+        flush_r.sum()
     res = {}
     iters = max(3, args.section_iters)
     gemm_names = ["prefill_q4k_4096x4096_n64", "prefill_q4k_4096x4096_n512",
@@ -408,15 +439,15 @@ def run_sections(args, kq, syn, torch, dev, stream, pk, only=None):
         Y = torch.empty((N, M), dtype=torch.float32, device=dev)
         ws = torch.empty(kq.kq_workspace_bytes(kq.KQ_OP_GEMM, wl["wtype"], M, K, N), dtype=torch.uint8, device=dev)
         fn = lambda: kq.kq_gemm(wl["wtype"], W, X, M, K, Y=Y, ws=ws)  # noqa: E731
-        ms, ms_min = _timed_calls(fn, iters, 2, flush, torch, stream)
+        ms, ms_min, ms_eager = _timed_calls(fn, iters, 2, flush, torch, stream)
         flops = 2.0 * M * N * K
         wbytes = W.numel() + X.numel() * 4 + Y.numel() * 4
         tf = flops / (ms / 1e3) / 1e12
-        res[name] = {"ms": round(ms, 4), "ms_min": round(ms_min, 4), "tflops": round(tf, 1),
+        res[name] = {"ms": round(ms, 4), "ms_min": round(ms_min, 4), "ms_eager": round(ms_eager, 4),
+                     "tflops": round(tf, 1),
                      "frac_bf16_peak": round(tf / pk["bf16_tflops"], 4),
                      "alg_gbs": round(wbytes / (ms / 1e3) / 1e9, 1),
-                     "frac_hbm_peak": round(wbytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"], 4),
-                     "launches_per_call": None}
+                     "frac_hbm_peak": round(wbytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"], 4)}
         del W, X, Y, ws
     if only is not None and only != moe_name:
         return res
@@ -428,12 +459,12 @@ def run_sections(args, kq, syn, torch, dev, stream, pk, only=None):
     Y = torch.empty((T, top_k, M), dtype=torch.float32, device=dev)
     ws = torch.empty(kq.kq_workspace_bytes(kq.KQ_OP_MOE, "q4_k", M, K, T, E, top_k), dtype=torch.uint8, device=dev)
     fn = lambda: kq.kq_moe_grouped_gemm("q4_k", W, E, ids, X, M, K, Y=Y, ws=ws)  # noqa: E731
-    ms, ms_min = _timed_calls(fn, iters, 2, flush, torch, stream)
+    ms, ms_min, ms_eager = _timed_calls(fn, iters, 2, flush, torch, stream)
     flops = 2.0 * M * K * T * top_k
     nbytes = W.numel() + X.numel() * 4 + Y.numel() * 4 + ids.numel() * 4
     tf = flops / (ms / 1e3) / 1e12
     res["moe_q4k_128x768x2048_t1024_top8"] = {
-        "ms": round(ms, 4), "ms_min": round(ms_min, 4), "tflops": round(tf, 1),
+        "ms": round(ms, 4), "ms_min": round(ms_min, 4), "ms_eager": round(ms_eager, 4), "tflops": round(tf, 1),
         "frac_bf16_peak": round(tf / pk["bf16_tflops"], 4),
         "alg_gbs": round(nbytes / (ms / 1e3) / 1e9, 1),
         "frac_hbm_peak": round(nbytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"], 4)}
