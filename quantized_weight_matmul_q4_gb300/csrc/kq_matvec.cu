@@ -308,9 +308,13 @@ __global__ void __launch_bounds__(MV_THREADS, 1) matvec_kernel(const MatvecParam
 // adds its items into one register per row group, in item order; the warps'
 // sums are added in warp order at the end (deterministic).
 // ---------------------------------------------------------------------------
-constexpr int LR_NW = 24;                    // consumer warps (plus one producer warp)
-constexpr int LR_THREADS = (LR_NW + 1) * 32;
-constexpr int LR_CT = LR_NW * 32;
+// Two builds: 24 consumer warps with all of a CTA's rows staged at once (one CTA
+// per SM), or 14 consumer warps with a ring of chunk slots in at most half of
+// an SM's shared memory (two CTAs per SM), for row ranges that do not fit
+// whole.
+constexpr int LR_NW_FULL = 24;
+constexpr int LR_NW_RING = 14;
+constexpr int LR_RING_SMEM = 113 * 1024;     // two CTAs per SM (228 KB, 1 KB reserved per CTA)
 constexpr int LR_MAX_ROWS = 128;             // rows per CTA: at most four row groups
 constexpr int LR_XT = 2;                     // 8-value activation tasks loaded per thread per round
 
@@ -323,43 +327,68 @@ struct MatvecLaneRowParams {
   int cb;           // super-blocks per chunk (odd)
   int n_chunks;     // ceil(nb / cb)
   int chunk_bytes;  // shared-memory stride of a chunk (R * cb * 144 rounded up to 128)
+  int S;            // chunk slots (== n_chunks: everything staged at once; fewer: a ring)
   uint32_t inv_per_chunk, inv_cb;  // ceil(2^32 / d) for d = n_groups * cb and d = cb
   int xq_off, xs_off, part_off, bar_off;  // shared-memory layout (bytes)
   int* err;
 };
 
-__global__ void __launch_bounds__(LR_THREADS, 1)
+template <int NW, bool RING>
+__global__ void __launch_bounds__((NW + 1) * 32, RING ? 2 : 1)
     matvec_q4k_lanerow_kernel(const __grid_constant__ CUtensorMap tmW, const MatvecLaneRowParams p) {
+  constexpr int LR_CT = NW * 32;
   extern __shared__ __align__(1024) uint8_t smem[];
   int8_t* xq = reinterpret_cast<int8_t*>(smem + p.xq_off);
   float2* xs = reinterpret_cast<float2*>(smem + p.xs_off);  // per 32-block: {d8, d8 * Sum q}
   float* part = reinterpret_cast<float*>(smem + p.part_off);  // [warp][row group][lane]
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);  // one per chunk
-  volatile int* abort = reinterpret_cast<volatile int*>(full + p.n_chunks);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);  // one per slot
+  uint64_t* empty = full + p.S;
+  volatile int* abort = reinterpret_cast<volatile int*>(empty + p.S);
 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r0 = blockIdx.x * p.R;
   const int rows = min(p.R, p.M - r0);
 
+  const int per_chunk = p.n_groups * p.cb;  // work items per chunk
   if (threadIdx.x == 0) {
-    for (int c = 0; c < p.n_chunks; ++c) mbar_init(&full[c], 1);
+    for (int sl = 0; sl < p.S; ++sl) {
+      mbar_init(&full[sl], 1);
+      if (RING) mbar_init(&empty[sl], per_chunk);  // every item of a chunk, computed or skipped, arrives once
+    }
     *abort = 0;
     fence_mbar_init();
   }
   __syncthreads();
 
-  if (warp == LR_NW) {
+  if (warp == NW) {
     if (lane == 0) {
       tma_prefetch_desc(&tmW);
       const uint32_t box = static_cast<uint32_t>(p.R * p.cb * Q4K_BYTES);
-      for (int c = 0; c < p.n_chunks; ++c) {
-        mbar_expect_tx(&full[c], box);
-        tma_load_2d(smem + static_cast<size_t>(c) * p.chunk_bytes, &tmW, &full[c], c * p.cb * (Q4K_BYTES / 4), r0);
+      if (!RING) {
+        for (int c = 0; c < p.n_chunks; ++c) {
+          mbar_expect_tx(&full[c], box);
+          tma_load_2d(smem + static_cast<size_t>(c) * p.chunk_bytes, &tmW, &full[c], c * p.cb * (Q4K_BYTES / 4), r0);
+        }
+        // Every copy lands before the CTA may exit (also when the consumers gave up).
+        for (int c = 0; c < p.n_chunks; ++c)
+          if (!mbar_wait_bounded(&full[c], 0)) report_error(p.err, ERR_WAIT_TIMEOUT);
+      } else {
+        int issued = 0;
+        for (int c = 0; c < p.n_chunks; ++c) {
+          const int sl = c % p.S;
+          if (c >= p.S && !mbar_wait(&empty[sl], ((c / p.S) - 1) & 1, abort, p.err)) break;
+          mbar_expect_tx(&full[sl], box);
+          tma_load_2d(smem + static_cast<size_t>(sl) * p.chunk_bytes, &tmW, &full[sl], c * p.cb * (Q4K_BYTES / 4),
+                      r0);
+          issued = c + 1;
+        }
+        // Every copy lands before the CTA may exit (also when the consumers gave up).
+        for (int sl = 0; sl < min(issued, p.S); ++sl) {
+          const int fills = (issued - sl + p.S - 1) / p.S;
+          if (!mbar_wait_bounded(&full[sl], (fills - 1) & 1)) report_error(p.err, ERR_WAIT_TIMEOUT);
+        }
       }
-      // Every copy lands before the CTA may exit (also when the consumers gave up).
-      for (int c = 0; c < p.n_chunks; ++c)
-        if (!mbar_wait_bounded(&full[c], 0)) report_error(p.err, ERR_WAIT_TIMEOUT);
     }
     return;
   }
@@ -396,25 +425,38 @@ __global__ void __launch_bounds__(LR_THREADS, 1)
 
   const float4* xs4 = reinterpret_cast<const float4*>(xs);
   const int pitch = p.cb * Q4K_BYTES;
-  const int per_chunk = p.n_groups * p.cb;
   const int items = p.n_chunks * per_chunk;
-  int ready = -1;  // last chunk this warp has seen land
+  int ready = -1, sl = 0;  // last chunk this warp has seen land, and its slot
   float acc[4] = {0.f, 0.f, 0.f, 0.f};  // this warp's sums for row groups 0..3
-  for (int i = warp; i < items; i += LR_NW) {
+  for (int i = warp; i < items; i += NW) {
     // i = (c * n_groups + g) * cb + j; quotients by multiply-high (exact in range)
     const int c = static_cast<int>(__umulhi(static_cast<uint32_t>(i), p.inv_per_chunk));
     const int rem = i - c * per_chunk;
     const int g = static_cast<int>(__umulhi(static_cast<uint32_t>(rem), p.inv_cb));
     const int j = rem - g * p.cb;
     const int b = c * p.cb + j;
-    if (b >= p.nb) continue;  // zero-filled tail of the last chunk
-    if (c != ready) {
-      if (!mbar_wait(&full[c], 0, abort, p.err)) break;
-      ready = c;
+    if (!RING) {
+      if (b >= p.nb) continue;  // zero-filled tail of the last chunk
+      if (c != ready) {
+        if (!mbar_wait(&full[c], 0, abort, p.err)) break;
+        ready = c;
+      }
+      sl = c;
+    } else {
+      if (c != ready) {
+        sl = c % p.S;
+        if (!mbar_wait(&full[sl], (c / p.S) & 1, abort, p.err)) break;
+        ready = c;
+      }
+      if (b >= p.nb) {  // zero-filled tail of the last chunk: release it all the same
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[sl]);
+        continue;
+      }
     }
     const int row = 32 * g + lane;
     const int srow = min(row, p.R - 1);  // lanes past the last row repeat it; their result is dropped
-    const uint8_t* blk = smem + static_cast<size_t>(c) * p.chunk_bytes + srow * pitch + j * Q4K_BYTES;
+    const uint8_t* blk = smem + static_cast<size_t>(sl) * p.chunk_bytes + srow * pitch + j * Q4K_BYTES;
     const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
     const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x & 0xFFFFu)));
     const float dmin = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x >> 16)));
@@ -465,6 +507,10 @@ __global__ void __launch_bounds__(LR_THREADS, 1)
     const float v = fmaf(-dmin, mn, d * lo);
 #pragma unroll
     for (int k = 0; k < 4; ++k) acc[k] += (g == k) ? v : 0.f;
+    if (RING) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[sl]);
+    }
   }
 #pragma unroll
   for (int k = 0; k < 4; ++k)
@@ -475,16 +521,18 @@ __global__ void __launch_bounds__(LR_THREADS, 1)
     const float* pr = part + (r >> 5) * 32 + (r & 31);
     float a = pr[0];
 #pragma unroll 8
-    for (int w = 1; w < LR_NW; ++w) a += pr[w * p.n_groups * 32];
+    for (int w = 1; w < NW; ++w) a += pr[w * p.n_groups * 32];
     p.y[r0 + r] = a;
   }
 }
 
 static inline int round_up(int v, int a) { return (v + a - 1) / a * a; }
 
-// Launch plan of the lane-row kernel; false when a CTA's rows do not fit in
-// shared memory (then the item kernel above runs).
-static bool plan_lanerow(int64_t M, int64_t K, int num_sms, MatvecLaneRowParams* p, int* grid, size_t* smem) {
+// Launch plan of the lane-row kernel with nw consumer warps in at most `budget`
+// bytes of shared memory; `ring` allows fewer chunk slots than chunks (at least
+// two). False when the rows do not fit (then the item kernel above runs).
+static bool plan_lanerow(int64_t M, int64_t K, int num_sms, int nw, int budget, bool ring, MatvecLaneRowParams* p,
+                         int* grid, size_t* smem) {
   if (K > (int64_t(1) << 20)) return false;
   p->M = static_cast<int>(M);
   p->K = static_cast<int>(K);
@@ -495,23 +543,26 @@ static bool plan_lanerow(int64_t M, int64_t K, int num_sms, MatvecLaneRowParams*
   p->R = static_cast<int>(R);
   *grid = static_cast<int>((M + R - 1) / R);
   p->n_groups = (p->R + 31) / 32;
-  const int part_bytes = LR_NW * p->n_groups * 32 * 4;
+  const int part_bytes = nw * p->n_groups * 32 * 4;
   const int fixed = round_up(p->K, 128)                 // activation codes
                     + round_up((p->K / 32) * 8, 128)    // {d8, d8 * Sum q} per 32-block
                     + part_bytes;                       // per-warp partials
   for (int cb = 7; cb >= 1; cb -= 2) {  // widest odd chunk that fits
     const int n_chunks = (p->nb + cb - 1) / cb;
     const int chunk_bytes = round_up(p->R * cb * Q4K_BYTES, 128);
-    const size_t total = static_cast<size_t>(n_chunks) * chunk_bytes + fixed + n_chunks * 8 + 16;
-    if (total > static_cast<size_t>(MV_SMEM_LIMIT)) continue;
-    p->cb = cb;
-    p->n_chunks = n_chunks;
+    int S = n_chunks;
+    auto total = [&](int slots) { return static_cast<size_t>(slots) * chunk_bytes + fixed + slots * 16 + 16; };
+    while (ring && S > 2 && total(S) > static_cast<size_t>(budget)) --S;
+    if (total(S) > static_cast<size_t>(budget)) continue;
     // i / d == umulhi(i, ceil(2^32 / d)) holds while i * d < 2^32
     if (static_cast<int64_t>(n_chunks) * p->n_groups * cb * p->n_groups * cb >= (int64_t(1) << 32)) return false;
+    p->cb = cb;
+    p->n_chunks = n_chunks;
+    p->chunk_bytes = chunk_bytes;
+    p->S = S;
     p->inv_per_chunk = static_cast<uint32_t>(((uint64_t(1) << 32) + p->n_groups * cb - 1) / (p->n_groups * cb));
     p->inv_cb = static_cast<uint32_t>(((uint64_t(1) << 32) + cb - 1) / cb);
-    p->chunk_bytes = chunk_bytes;
-    size_t off = static_cast<size_t>(n_chunks) * chunk_bytes;
+    size_t off = static_cast<size_t>(S) * chunk_bytes;
     p->xq_off = static_cast<int>(off);
     off += round_up(p->K, 128);
     p->xs_off = static_cast<int>(off);
@@ -519,7 +570,7 @@ static bool plan_lanerow(int64_t M, int64_t K, int num_sms, MatvecLaneRowParams*
     p->part_off = static_cast<int>(off);
     off += part_bytes;
     p->bar_off = static_cast<int>(off);
-    *smem = total;
+    *smem = total(S);
     return true;
   }
   return false;
@@ -528,12 +579,16 @@ static bool plan_lanerow(int64_t M, int64_t K, int num_sms, MatvecLaneRowParams*
 cudaError_t launch_matvec(int wtype, const void* W, const float* x, float* y, int64_t M, int64_t K, int* err,
                           int num_sms, cudaStream_t s, int* status) {
   *status = KQ_OK;
-  // Q4_K whose per-CTA rows fit in shared memory: the lane-row kernel.
+  // Q4_K: the lane-row kernel with all rows staged at once when they fit
+  // (measured faster at the decode sizes: the ring's refills wait for the
+  // activations and then for HBM), else its ring form.
   if (wtype == KQ_Q4_K) {
     MatvecLaneRowParams lp{};
     size_t smem = 0;
     int grid = 0;
-    if (plan_lanerow(M, K, num_sms, &lp, &grid, &smem)) {
+    const bool full = plan_lanerow(M, K, num_sms, LR_NW_FULL, MV_SMEM_LIMIT, false, &lp, &grid, &smem);
+    const bool ring = !full && plan_lanerow(M, K, num_sms, LR_NW_RING, LR_RING_SMEM, true, &lp, &grid, &smem);
+    if (full || ring) {
       CUtensorMap tmW;
       const uint64_t rs = static_cast<uint64_t>(lp.nb) * Q4K_BYTES;
       if (!encode_tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT32, W, rs / 4, static_cast<uint64_t>(M), rs,
@@ -545,9 +600,16 @@ cudaError_t launch_matvec(int wtype, const void* W, const float* x, float* y, in
       lp.x = x;
       lp.y = y;
       lp.err = err;
-      cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(matvec_q4k_lanerow_kernel), 9);
+      if (ring) {
+        cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(matvec_q4k_lanerow_kernel<LR_NW_RING, true>), 10);
+        if (e != cudaSuccess) return e;
+        return launch_pdl(matvec_q4k_lanerow_kernel<LR_NW_RING, true>, dim3(grid), dim3((LR_NW_RING + 1) * 32), smem,
+                          s, tmW, lp);
+      }
+      cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(matvec_q4k_lanerow_kernel<LR_NW_FULL, false>), 9);
       if (e != cudaSuccess) return e;
-      return launch_pdl(matvec_q4k_lanerow_kernel, dim3(grid), dim3(LR_THREADS), smem, s, tmW, lp);
+      return launch_pdl(matvec_q4k_lanerow_kernel<LR_NW_FULL, false>, dim3(grid), dim3((LR_NW_FULL + 1) * 32), smem,
+                        s, tmW, lp);
     }
   }
   MatvecParams p{};

@@ -73,3 +73,20 @@ def test_zero_activation_gives_zero():
     W = syn.q4_k_weights(np.random.default_rng(1), M, K)
     y = _run("q4_k", W, np.zeros((1, K), np.float32), M, K)
     assert np.all(y == 0)
+
+
+@pytest.mark.parametrize("M,K", [(4096, 14336), (14336, 4096)])
+def test_ring_staging_shapes_sampled_rows(M, K):
+    # Row ranges too large to stage whole take the ring form of the lane-row
+    # kernel (chunk slots refilled as they are consumed); rows at CTA range
+    # boundaries and the ragged end are among the sampled ones.
+    rng = np.random.default_rng(M + K)
+    W = syn.q4_k_weights(rng, M, K)
+    x = syn.activations(rng, K, 1)
+    y = _run("q4_k", W, x, M, K)
+    R = -(-M // 152)
+    rows = np.unique(np.concatenate([rng.choice(M, 160, replace=False), [0, R - 1, R, M - 1],
+                                     np.arange(R * 150, M)]))
+    Yr, B = ora.matmul_rows("q4_k", W, x, K, rows)
+    assert_within_bound(y[rows], Yr[0], B[0], f"ring {M}x{K}")
+    assert np.all(np.isfinite(y))
