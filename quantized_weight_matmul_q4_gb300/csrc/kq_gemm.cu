@@ -25,10 +25,16 @@
 //  * warps 16-19 drain finished accumulators (tcgen05.ld) to global memory
 //    (with two accumulators, while the next tile is being computed).
 //
-// Tiles are statically strided over a persistent grid (one CTA per SM), so
-// results do not depend on scheduling; a split K range is summed afterwards in
-// a fixed order. Every wait is bounded (ERR_WAIT_TIMEOUT, no hang).
+// The grid is persistent (one CTA per SM). The raw producer picks each CTA's
+// next tile and hands its index to the other roles through a small ring in
+// shared memory: dense tiles (all the same cost) are strided statically; MoE
+// tiles come from an atomic tile queue in the workspace ("ZINC MMQ v2",
+// Persistent kernel + atomic work queue). Every output element is computed
+// inside one tile, so results do not depend on which CTA takes which tile; a
+// split K range is summed afterwards in a fixed order. Every wait is bounded
+// (ERR_WAIT_TIMEOUT, no hang).
 #include <algorithm>
+#include <climits>
 
 #include "kq_internal.h"
 #include "kq_common.cuh"
@@ -52,6 +58,10 @@ constexpr int GM_THREADS = 23 * 32;
 constexpr int GM_TMEM_COLS = 512;     // accumulators, then the A stages
 constexpr int GM_SMEM_LIMIT = 227 * 1024;
 constexpr int MOE_MAX_EXPERTS = 512;
+constexpr int GM_TQ = 4;              // tile-index ring slots
+// Warps that read each tile index: the x_hat producer, the MMA issuer, the
+// unpackers and the epilogue (one arrival per warp on the slot's empty barrier).
+constexpr int GM_TQ_READERS = 1 + 1 + GM_DQ_WARPS + 4;
 
 template <int WT>
 struct RawBox;
@@ -86,6 +96,7 @@ struct GemmArgs {
   const int* offsets;
   const int* tile_start;
   const int* entries;
+  int* tile_queue;  // MoE: next tile index minus gridDim.x (zeroed by the routing kernel)
   int* err;
 };
 
@@ -138,6 +149,25 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs& a, int t, const int*
     T.split = 0;
   }
   return T;
+}
+
+// Next tile index from the ring (called by a whole warp, or by one lane when
+// `one_lane`). Returns INT_MAX when a wait gave up.
+__device__ __forceinline__ int tq_pop(uint64_t* full, uint64_t* empty, const int* ids, int& qi, uint32_t& qph,
+                                      bool one_lane, volatile int* abort, int* err) {
+  if (!mbar_wait(&full[qi], qph, abort, err)) return INT_MAX;
+  const int t = *reinterpret_cast<const volatile int*>(&ids[qi]);
+  if (one_lane) {
+    mbar_arrive(&empty[qi]);
+  } else {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&empty[qi]);
+  }
+  if (++qi == GM_TQ) {
+    qi = 0;
+    qph ^= 1;
+  }
+  return t;
 }
 
 // --- weight unpacking into the fp16 A operand ---------------------------------
@@ -269,7 +299,10 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
   uint64_t* k_empty = k_full + a.k_stages;
   uint64_t* acc_full = k_empty + a.k_stages;
   uint64_t* acc_empty = acc_full + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  uint64_t* tq_full = acc_empty + 2;
+  uint64_t* tq_empty = tq_full + GM_TQ;
+  int* tq_ids = reinterpret_cast<int*>(tq_empty + GM_TQ);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tq_ids + GM_TQ);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_tile_start = reinterpret_cast<int*>(tmem_slot + 4);
   int* s_counts = s_tile_start + (a.n_experts + 1);
@@ -289,6 +322,10 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], 4);
+    }
+    for (int i = 0; i < GM_TQ; ++i) {
+      mbar_init(&tq_full[i], 1);
+      mbar_init(&tq_empty[i], GM_TQ_READERS);
     }
     *abort = 0;
     fence_mbar_init();
@@ -327,10 +364,20 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
 
   if (warp == GM_RAW_WARP) {
     // ---- raw weight producer -------------------------------------------------
+    // It also picks the CTA's tiles: the first is blockIdx.x, later ones come
+    // from the MoE tile queue or, for the dense GEMM, a stride of gridDim.x.
     if (lane == 0) {
-      int st = 0;
-      uint32_t ph = 0;
-      for (int t = blockIdx.x; t < total_tiles && !*abort; t += gridDim.x) {
+      int st = 0, qi = 0;
+      uint32_t ph = 0, qph = 0;
+      for (int t = blockIdx.x;; ) {
+        if (!mbar_wait(&tq_empty[qi], qph ^ 1, abort, a.err)) break;
+        tq_ids[qi] = t;
+        mbar_arrive(&tq_full[qi]);
+        if (++qi == GM_TQ) {
+          qi = 0;
+          qph ^= 1;
+        }
+        if (t >= total_tiles || *abort) break;
         const Tile T = decode_tile<MOE>(a, t, s_tile_start, s_counts, s_offsets);
         for (int kb = T.kb0; kb < T.kb1; ++kb) {
           if (!mbar_wait(&raw_empty[st], ph ^ 1, abort, a.err)) break;
@@ -342,15 +389,18 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
             ph ^= 1;
           }
         }
+        t = MOE ? static_cast<int>(gridDim.x) + atomicAdd(a.tile_queue, 1) : t + static_cast<int>(gridDim.x);
       }
     }
   } else if (warp == GM_B_WARP) {
     // ---- activation producer -------------------------------------------------
     if (!MOE) asm volatile("griddepcontrol.wait;" ::: "memory");  // x_hat comes from the previous kernel
     if (lane == 0) {
-      int st = 0;
-      uint32_t ph = 0;
-      for (int t = blockIdx.x; t < total_tiles && !*abort; t += gridDim.x) {
+      int st = 0, qi = 0;
+      uint32_t ph = 0, qph = 0;
+      for (;;) {
+        const int t = tq_pop(tq_full, tq_empty, tq_ids, qi, qph, true, abort, a.err);
+        if (t >= total_tiles || *abort) break;
         const Tile T = decode_tile<MOE>(a, t, s_tile_start, s_counts, s_offsets);
         const int nbox = (T.ncols + GM_BBOX - 1) / GM_BBOX;
         for (int kb = T.kb0; kb < T.kb1 && !*abort; ++kb) {
@@ -372,12 +422,13 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
     // ---- tensor-core issuer --------------------------------------------------
     // The whole warp runs the loop converged, so descriptors and counters stay
     // warp-uniform; one elected lane issues the MMAs and commits.
-    int kst = 0;
-    uint32_t kph = 0;
-    int it = 0;
+    int kst = 0, qi = 0;
+    uint32_t kph = 0, qph = 0;
     const uint32_t a_tmem0 = tmem_base + a.a_col0;
     const uint64_t b_desc0 = smem_desc_sw128(smem_u32(sB));
-    for (int t = blockIdx.x; t < total_tiles && !*abort; t += gridDim.x, ++it) {
+    for (int it = 0;; ++it) {
+      const int t = tq_pop(tq_full, tq_empty, tq_ids, qi, qph, false, abort, a.err);
+      if (t >= total_tiles || *abort) break;
       const Tile T = decode_tile<MOE>(a, t, s_tile_start, s_counts, s_offsets);
       const int acc = (a.n_acc == 2) ? (it & 1) : 0;
       const uint32_t acc_ph = (a.n_acc == 2) ? ((it >> 1) & 1) : (it & 1);
@@ -418,9 +469,11 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
     // half (w / 4) % 2 of a K step, and the K steps of parity w / 8
     const int r = 32 * (warp & 3) + lane, hf = (warp >> 2) & 1, grp = warp >> 3;
     const uint32_t a_row = tmem_base + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + a.a_col0 + 16 * hf;
-    int rst = 0, ast = 0, gs = 0;
-    uint32_t rph = 0, aph = 0;
-    for (int t = blockIdx.x; t < total_tiles && !*abort; t += gridDim.x) {
+    int rst = 0, ast = 0, gs = 0, qi = 0;
+    uint32_t rph = 0, aph = 0, qph = 0;
+    for (;;) {
+      const int t = tq_pop(tq_full, tq_empty, tq_ids, qi, qph, false, abort, a.err);
+      if (t >= total_tiles || *abort) break;
       const Tile T = decode_tile<MOE>(a, t, s_tile_start, s_counts, s_offsets);
       for (int kb = T.kb0; kb < T.kb1 && !*abort; ++kb) {
         if (!mbar_wait(&raw_full[rst], rph, abort, a.err)) break;
@@ -457,8 +510,11 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
     // ---- epilogue: tensor memory -> fp32 Y -----------------------------------
     if (!MOE) asm volatile("griddepcontrol.wait;" ::: "memory");  // Y may still be read by the previous kernel
     const int wq = warp - GM_EPI_WARP0;  // == warp % 4: this warp's 32 TMEM lanes
-    int it = 0;
-    for (int t = blockIdx.x; t < total_tiles && !*abort; t += gridDim.x, ++it) {
+    int qi = 0;
+    uint32_t qph = 0;
+    for (int it = 0;; ++it) {
+      const int t = tq_pop(tq_full, tq_empty, tq_ids, qi, qph, false, abort, a.err);
+      if (t >= total_tiles || *abort) break;
       const Tile T = decode_tile<MOE>(a, t, s_tile_start, s_counts, s_offsets);
       const int acc = (a.n_acc == 2) ? (it & 1) : 0;
       const uint32_t acc_ph = (a.n_acc == 2) ? ((it >> 1) & 1) : (it & 1);
@@ -566,7 +622,8 @@ constexpr int ROUTE_IDS_PER_THREAD = 16;  // ids held in registers between the t
 
 __global__ void __launch_bounds__(1024) moe_route_kernel(const int* __restrict__ ids, int n, int top_k, int E,
                                                          int m_tiles, int bn, int* counts, int* offsets,
-                                                         int* tile_start, int* slot_pos, float* Y, int M, int* err) {
+                                                         int* tile_start, int* tile_queue, int* slot_pos, float* Y,
+                                                         int M, int* err) {
   extern __shared__ int rsm[];
   int* cnt = rsm;        // [E]: histogram, then the scatter cursor of each bucket
   int* wsum = cnt + E;   // [32]
@@ -607,6 +664,7 @@ __global__ void __launch_bounds__(1024) moe_route_kernel(const int* __restrict__
   if (threadIdx.x == 0) {
     offsets[E] = n_valid;
     tile_start[E] = n_tiles;
+    *tile_queue = 0;  // the grouped GEMM's atomic tile queue starts empty
   }
   __syncthreads();
   // pass 2: bucket positions (-1 for an invalid id, whose output row is zeroed)
@@ -673,7 +731,7 @@ static bool choose_stages(int wtype, int bn, int n_experts, GemmArgs* a, size_t*
   if (a_max < 2) return false;
   const int b_bytes = ((bn + GM_BBOX - 1) / GM_BBOX) * GM_BBOX_BYTES;
   const int raw_bytes = raw_box_bytes(wtype) * GM_BM;
-  const int tables = (n_experts > 0 ? 3 * (n_experts + 1) * 4 : 0) + 64;
+  const int tables = (n_experts > 0 ? 3 * (n_experts + 1) * 4 : 0) + 64 + GM_TQ * 20;
   const int budget = GM_SMEM_LIMIT - (1024 + tables + 512);
   auto bytes = [&](int bs, int rs) { return bs * b_bytes + rs * raw_bytes; };
   // The B ring gets priority: an x_hat stage takes ~1.4k cycles from issue to
@@ -785,7 +843,7 @@ cudaError_t launch_gemm(int wtype, const void* W, const float* X, float* Y, int6
   return e;
 }
 
-// MoE workspace: counts[E] | offsets[E+1] | tile_start[E+1] | entries[n] (slot of each bucket row) |
+// MoE workspace: counts[E] | offsets[E+1] | tile_start[E+1] | tile queue counter | entries[n] (slot of each bucket row) |
 // slot_pos[n] (bucket row of each slot) | x_hat[n][K] fp16 (bucket order)
 MoePlan plan_moe(int wtype, int64_t M, int64_t K, int64_t T, int n_experts, int top_k) {
   (void)wtype;
@@ -799,6 +857,8 @@ MoePlan plan_moe(int wtype, int64_t M, int64_t K, int64_t T, int n_experts, int 
   o += round_up64(4 * (n_experts + 1), 256);
   p.off_tiles = o;
   o += round_up64(4 * (n_experts + 1), 256);
+  p.off_queue = o;
+  o += 256;
   p.off_entries = o;
   o += round_up64(4 * n, 256);
   p.off_src = o;
@@ -823,6 +883,7 @@ cudaError_t launch_moe(int wtype, const void* W, int n_experts, const int32_t* i
   int* counts = reinterpret_cast<int*>(wsb + plan.off_counts);
   int* offsets = reinterpret_cast<int*>(wsb + plan.off_offsets);
   int* tile_start = reinterpret_cast<int*>(wsb + plan.off_tiles);
+  int* tile_queue = reinterpret_cast<int*>(wsb + plan.off_queue);
   int* entries = reinterpret_cast<int*>(wsb + plan.off_entries);
   int* slot_pos = reinterpret_cast<int*>(wsb + plan.off_src);
   __half* xh = reinterpret_cast<__half*>(wsb + plan.off_xhat);
@@ -832,7 +893,8 @@ cudaError_t launch_moe(int wtype, const void* W, int n_experts, const int32_t* i
   cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(moe_route_kernel), 8);
   if (e != cudaSuccess) return e;
   e = launch_pdl(moe_route_kernel, dim3(1), dim3(1024), rsmem, s, ids, static_cast<int>(n), top_k, n_experts,
-                 plan.m_tiles, MOE_BN, counts, offsets, tile_start, slot_pos, Y, static_cast<int>(M), err);
+                 plan.m_tiles, MOE_BN, counts, offsets, tile_start, tile_queue, slot_pos, Y, static_cast<int>(M),
+                 err);
   if (e != cudaSuccess) return e;
   e = launch_gather_xhat(X, xh, K, n, top_k, slot_pos, entries, num_sms, s);
   if (e != cudaSuccess) return e;
@@ -857,6 +919,7 @@ cudaError_t launch_moe(int wtype, const void* W, int n_experts, const int32_t* i
   a.offsets = offsets;
   a.tile_start = tile_start;
   a.entries = entries;
+  a.tile_queue = tile_queue;
   a.err = err;
   size_t smem = 0;
   if (!choose_stages(wtype, MOE_BN, n_experts, &a, &smem)) {

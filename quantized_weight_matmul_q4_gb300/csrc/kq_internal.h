@@ -31,7 +31,7 @@ cudaError_t launch_gemm(int wtype, const void* W, const float* X, float* Y, int6
 
 struct MoePlan {
   int m_tiles;
-  size_t off_counts, off_offsets, off_tiles, off_entries, off_src, off_xhat, total_bytes;
+  size_t off_counts, off_offsets, off_tiles, off_queue, off_entries, off_src, off_xhat, total_bytes;
 };
 MoePlan plan_moe(int wtype, int64_t M, int64_t K, int64_t T, int n_experts, int top_k);
 cudaError_t launch_moe(int wtype, const void* W, int n_experts, const int32_t* ids, int top_k, const float* X,
