@@ -35,6 +35,7 @@
 // (ERR_WAIT_TIMEOUT, no hang).
 #include <algorithm>
 #include <climits>
+#include <mutex>
 
 #include "kq_internal.h"
 #include "kq_common.cuh"
@@ -111,15 +112,18 @@ struct Tile {
   int nbase;   // entries index of column 0 (MoE)
 };
 
-template <bool MOE>
-__device__ __forceinline__ Tile decode_tile(const GemmArgs& a, int t, const int* s_tile_start, const int* s_counts,
-                                            const int* s_offsets) {
+// Dense tiles: t = (m_tile * n_tiles + n_tile) * splits + split. A CTA pair
+// takes 256 weight rows (m_tiles counts pairs of 128-row tiles); the CTA of
+// rank r computes rows 128 r .. 128 r + 127 of them.
+template <bool MOE, bool PAIR>
+__device__ __forceinline__ Tile decode_tile(const GemmArgs& a, int t, int rank, const int* s_tile_start,
+                                            const int* s_counts, const int* s_offsets) {
   Tile T;
   if (!MOE) {
     const int split = t % a.splits;
     const int mn = t / a.splits;
     const int nt = mn % a.n_tiles, mt = mn / a.n_tiles;
-    T.m0 = mt * GM_BM;
+    T.m0 = (PAIR ? 2 * mt + rank : mt) * GM_BM;
     T.wrow0 = T.m0;
     T.xrow0 = nt * a.bn;
     T.ncols = min(a.bn, a.N - T.xrow0);
@@ -172,20 +176,21 @@ __device__ __forceinline__ int tq_pop(uint64_t* full, uint64_t* empty, const int
 
 // --- weight unpacking into the fp16 A operand ---------------------------------
 // A stage: 128 rows (tensor-memory lanes) x 64 K of fp16, two per 32-bit
-// column, lower k in the low half. The thread of row r and half hf produces the
-// 32 weights k = 32hf .. 32hf+31 of the step as o[0..15] (columns 16hf + i).
+// column, lower k in the low half. The thread of row r and half hf produces
+// the 32 weights k = 16hf .. 16hf+15 (columns 8hf .. 8hf+7, lo[]) and
+// k = 32+16hf .. 32+16hf+15 (columns 16+8hf .. 16+8hf+7, hi[]) of the step,
+// so that each byte of the weight codes is read from shared memory once.
 
-// Q4_K, K step s (0..3) of a super-block covers sub-blocks 2s (low nibbles of
-// qs[32s..32s+31]) and 2s+1 (high nibbles): half hf is sub-block 2s + hf, 32
-// weights w = d*sc*nib - dmin*m computed as one fp16 fma on the exact nibble.
-__device__ __forceinline__ void dequant_q4k(const uint8_t* __restrict__ raw, int s, int r, int hf,
-                                            uint32_t (&o)[16]) {
-  const uint8_t* blk = raw + r * Q4K_BYTES;
-  const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
-  const uint4 q0 = *reinterpret_cast<const uint4*>(blk + 16 + 32 * s);
-  const uint4 q1 = *reinterpret_cast<const uint4*>(blk + 32 + 32 * s);
-  const int j = 2 * s + hf;
-  uint32_t scw, mw;
+// Q4_K, K step s (0..3) of a super-block covers sub-blocks 2s (the low
+// nibbles of qs[32s..32s+31]) and 2s+1 (their high nibbles). Half hf reads the
+// 16 bytes qs[32s+16hf ..]: their low nibbles are weights 16hf.. of sub-block
+// 2s, their high nibbles weights 16hf.. of sub-block 2s+1. Every weight
+// w = d*sc*nib - dmin*m is one fp16 fma on the exact nibble. hdr is the
+// block's first 16 bytes (d, dmin, packed 6-bit scales and mins).
+__device__ __forceinline__ void dequant_q4k(const uint4& hdr, const uint8_t* __restrict__ raw, int s, int r, int hf,
+                                            uint32_t (&lo)[8], uint32_t (&hi)[8]) {
+  const uint4 q = *reinterpret_cast<const uint4*>(raw + r * Q4K_BYTES + 16 + 32 * s + 16 * hf);
+  uint32_t scw, mw;  // 6-bit scales / mins of sub-blocks 0-3 (s < 2) or 4-7, one per byte
   if (s < 2) {
     scw = hdr.y & 0x3F3F3F3Fu;
     mw = hdr.z & 0x3F3F3F3Fu;
@@ -193,97 +198,112 @@ __device__ __forceinline__ void dequant_q4k(const uint8_t* __restrict__ raw, int
     scw = (hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u);
     mw = ((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u);
   }
-  const int bi = (j & 3) * 8;
-  const float sc = static_cast<float>((scw >> bi) & 0xFFu);
-  const float mn = static_cast<float>((mw >> bi) & 0xFFu);
+  const int b0 = (s & 1) * 16;  // byte of sub-block 2s; 2s+1 is the next byte
   const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x & 0xFFFFu)));
   const float dmin = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x >> 16)));
-  const __half2 scale2 = __float2half2_rn(d * sc);
-  const __half2 negmin2 = __float2half2_rn(-(dmin * mn));
+  const __half2 sc_lo = __float2half2_rn(d * static_cast<float>((scw >> b0) & 0xFFu));
+  const __half2 mn_lo = __float2half2_rn(-(dmin * static_cast<float>((mw >> b0) & 0xFFu)));
+  const __half2 sc_hi = __float2half2_rn(d * static_cast<float>((scw >> (b0 + 8)) & 0xFFu));
+  const __half2 mn_hi = __float2half2_rn(-(dmin * static_cast<float>((mw >> (b0 + 8)) & 0xFFu)));
   const __half2 k1024 = __float2half2_rn(1024.f);
-  const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint32_t src = hf ? (w[i] >> 4) : w[i];
-    // bytes 0,1 (and 2,3) -> fp16 (1024 + nibble) pairs
-    const uint32_t t0 = __byte_perm(src, 0x64646464u, 0x5140) & 0xFF0FFF0Fu;
-    const uint32_t t1 = __byte_perm(src, 0x64646464u, 0x7362) & 0xFF0FFF0Fu;
-    o[2 * i] = half2_bits(__hfma2(__hsub2(bits_half2(t0), k1024), scale2, negmin2));
-    o[2 * i + 1] = half2_bits(__hfma2(__hsub2(bits_half2(t1), k1024), scale2, negmin2));
+  for (int i = 0; i < 4; ++i) {
+    // bytes 0,1 (and 2,3) -> fp16 (1024 + nibble) pairs, low then high nibbles
+    const uint32_t l0 = __byte_perm(w[i], 0x64646464u, 0x5140) & 0xFF0FFF0Fu;
+    const uint32_t l1 = __byte_perm(w[i], 0x64646464u, 0x7362) & 0xFF0FFF0Fu;
+    const uint32_t h0 = __byte_perm(w[i] >> 4, 0x64646464u, 0x5140) & 0xFF0FFF0Fu;
+    const uint32_t h1 = __byte_perm(w[i] >> 4, 0x64646464u, 0x7362) & 0xFF0FFF0Fu;
+    lo[2 * i] = half2_bits(__hfma2(__hsub2(bits_half2(l0), k1024), sc_lo, mn_lo));
+    lo[2 * i + 1] = half2_bits(__hfma2(__hsub2(bits_half2(l1), k1024), sc_lo, mn_lo));
+    hi[2 * i] = half2_bits(__hfma2(__hsub2(bits_half2(h0), k1024), sc_hi, mn_hi));
+    hi[2 * i + 1] = half2_bits(__hfma2(__hsub2(bits_half2(h1), k1024), sc_hi, mn_hi));
   }
 }
 
-// The 8 words that start d bytes into the 48-byte window w (d even, < 16; the
+// The 4 words that start d bytes into the 32-byte window w (d even, < 16; the
 // same d for every thread of a K-block, so the branch does not diverge).
-__device__ __forceinline__ void window_words(const uint32_t (&w)[12], int d, uint32_t (&out)[8]) {
+__device__ __forceinline__ void window4(const uint4& a, const uint4& b, int d, uint32_t (&out)[4]) {
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
   const int sh = (d & 3) * 8;
   switch (d >> 2) {
     case 0:
 #pragma unroll
-      for (int i = 0; i < 8; ++i) out[i] = __funnelshift_r(w[i], w[i + 1], sh);
+      for (int i = 0; i < 4; ++i) out[i] = __funnelshift_r(w[i], w[i + 1], sh);
       break;
     case 1:
 #pragma unroll
-      for (int i = 0; i < 8; ++i) out[i] = __funnelshift_r(w[i + 1], w[i + 2], sh);
+      for (int i = 0; i < 4; ++i) out[i] = __funnelshift_r(w[i + 1], w[i + 2], sh);
       break;
     case 2:
 #pragma unroll
-      for (int i = 0; i < 8; ++i) out[i] = __funnelshift_r(w[i + 2], w[i + 3], sh);
+      for (int i = 0; i < 4; ++i) out[i] = __funnelshift_r(w[i + 2], w[i + 3], sh);
       break;
     default:
 #pragma unroll
-      for (int i = 0; i < 8; ++i) out[i] = __funnelshift_r(w[i + 3], w[i + 4], sh);
+      for (int i = 0; i < 4; ++i) out[i] = __funnelshift_r(w[i + 3], w[i + 4], sh);
       break;
   }
 }
 
-// Q6_K, K step s covers weights 64s..64s+63 of the super-block: half h = s/2,
-// quarters g = 2(s&1) and 2(s&1)+1. Half gg of the step is quarter
-// g = 2(s&1) + gg: 32 weights d*sc*(q-32), q = 4 bits of ql | 2 bits of qh.
-// The block starts `rem` bytes into the row's 16-byte aligned window; its ql
-// and qh bytes are fetched as three aligned 16-byte loads each (with the
-// 240-byte row pitch, 8 consecutive rows hit 8 distinct bank groups).
-__device__ __forceinline__ void dequant_q6k(const uint8_t* __restrict__ raw, int rem, int s, int r, int gg,
-                                            uint32_t (&o)[16]) {
+// Q6_K half h (weights 128h .. 128h+127) of a block, for the 16 positions
+// l = 16hf .. 16hf+15 of its four quarters: ql[64h + l] (quarters 0 and 2),
+// ql[64h + 32 + l] (quarters 1 and 3) and qh[32h + l] (2 bits of each
+// quarter). The block starts `rem` bytes into the row's 16-byte aligned window,
+// so each 16 bytes come from two aligned 16-byte loads.
+struct Q6Half {
+  uint32_t qa[4], qb[4], qh[4];
+};
+__device__ __forceinline__ void load_q6k_half(const uint8_t* __restrict__ raw, int rem, int h, int r, int hf,
+                                              Q6Half& q) {
   const uint8_t* row = raw + r * RawBox<KQ_Q6_K>::BYTES;
-  const uint8_t* blk = row + rem;
-  const int h = s >> 1, g = 2 * (s & 1) + gg;
-  uint32_t ql[8], qh[8];
-  {
-    const uint4* pl = reinterpret_cast<const uint4*>(row + 64 * h + 32 * (g & 1));
-    const uint4* ph = reinterpret_cast<const uint4*>(row + 128 + 32 * h);
-    uint32_t a[12], b[12];
-#pragma unroll
-    for (int k = 0; k < 3; ++k) {
-      const uint4 x = pl[k], y = ph[k];
-      a[4 * k] = x.x; a[4 * k + 1] = x.y; a[4 * k + 2] = x.z; a[4 * k + 3] = x.w;
-      b[4 * k] = y.x; b[4 * k + 1] = y.y; b[4 * k + 2] = y.z; b[4 * k + 3] = y.w;
-    }
-    window_words(a, rem, ql);
-    window_words(b, rem, qh);
-  }
+  const uint4* pa = reinterpret_cast<const uint4*>(row + 64 * h + 16 * hf);
+  const uint4* pb = reinterpret_cast<const uint4*>(row + 64 * h + 32 + 16 * hf);
+  const uint4* ph = reinterpret_cast<const uint4*>(row + 128 + 32 * h + 16 * hf);
+  window4(pa[0], pa[1], rem, q.qa);
+  window4(pb[0], pb[1], rem, q.qb);
+  window4(ph[0], ph[1], rem, q.qh);
+}
+
+// Q6_K K step s: half h = s/2, quarters g0 = 2(s&1) (k = l of the step) and
+// g0+1 (k = 32 + l). Weight d*sc*(q-32), q = 4 bits of ql | 2 bits of qh, sc the
+// int8 scale of the 16 positions l = 16hf.. of the quarter.
+__device__ __forceinline__ void dequant_q6k(const uint8_t* __restrict__ raw, int rem, const Q6Half& q, int s, int r,
+                                            int hf, uint32_t (&lo)[8], uint32_t (&hi)[8]) {
+  const uint8_t* blk = raw + r * RawBox<KQ_Q6_K>::BYTES + rem;
+  const int h = s >> 1, g0 = 2 * (s & 1);
   const float d = __half2float(*reinterpret_cast<const __half*>(blk + 208));
-  const int8_t* scp = reinterpret_cast<const int8_t*>(blk + 192 + 8 * h + 2 * g);
-  const __half2 s0 = __float2half2_rn(d * static_cast<float>(scp[0]));
-  const __half2 s1 = __float2half2_rn(d * static_cast<float>(scp[1]));
+  const int8_t* scp = reinterpret_cast<const int8_t*>(blk + 192 + 8 * h + hf);
+  const __half2 s0 = __float2half2_rn(d * static_cast<float>(scp[2 * g0]));
+  const __half2 s1 = __float2half2_rn(d * static_cast<float>(scp[2 * g0 + 2]));
   const __half2 k1056 = __float2half2_rn(1056.f);
   const bool low = (s & 1) == 0;  // quarters 0,1 use low nibbles, 2,3 high
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint32_t lo = low ? (ql[i] & 0x0F0F0F0Fu) : ((ql[i] >> 4) & 0x0F0F0F0Fu);
-    const uint32_t q = lo | (((qh[i] >> (2 * g)) & 0x03030303u) << 4);
-    const uint32_t t0 = __byte_perm(q, 0x64646464u, 0x5140);
-    const uint32_t t1 = __byte_perm(q, 0x64646464u, 0x7362);
-    const __half2 sc2 = (i < 4) ? s0 : s1;
-    o[2 * i] = half2_bits(__hmul2(__hsub2(bits_half2(t0), k1056), sc2));
-    o[2 * i + 1] = half2_bits(__hmul2(__hsub2(bits_half2(t1), k1056), sc2));
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t la = low ? (q.qa[i] & 0x0F0F0F0Fu) : ((q.qa[i] >> 4) & 0x0F0F0F0Fu);
+    const uint32_t lb = low ? (q.qb[i] & 0x0F0F0F0Fu) : ((q.qb[i] >> 4) & 0x0F0F0F0Fu);
+    const uint32_t va = la | (((q.qh[i] >> (2 * g0)) & 0x03030303u) << 4);
+    const uint32_t vb = lb | (((q.qh[i] >> (2 * g0 + 2)) & 0x03030303u) << 4);
+    lo[2 * i] = half2_bits(__hmul2(__hsub2(bits_half2(__byte_perm(va, 0x64646464u, 0x5140)), k1056), s0));
+    lo[2 * i + 1] = half2_bits(__hmul2(__hsub2(bits_half2(__byte_perm(va, 0x64646464u, 0x7362)), k1056), s0));
+    hi[2 * i] = half2_bits(__hmul2(__hsub2(bits_half2(__byte_perm(vb, 0x64646464u, 0x5140)), k1056), s1));
+    hi[2 * i + 1] = half2_bits(__hmul2(__hsub2(bits_half2(__byte_perm(vb, 0x64646464u, 0x7362)), k1056), s1));
   }
 }
 
-template <int WT, bool MOE>
+// PAIR (dense only): the kernel runs in clusters of two CTAs on neighbouring
+// SMs. Both CTAs stream and unpack their own 128 weight rows into their own
+// tensor memory and load half of the tile's x_hat rows; one thread of the even
+// CTA issues M = 256 MMAs (cta_group::2) that read both CTAs' operands and
+// write each CTA's accumulator. Each SM then holds, and pulls from L2, only
+// half of every B stage. Barrier roles in a pair: k_full and acc_empty of the
+// even CTA collect both CTAs' arrivals (and both x_hat halves' bytes); the MMA
+// commits arrive on k_empty and acc_full of both CTAs.
+template <int WT, bool MOE, bool PAIR>
 __global__ void __launch_bounds__(GM_THREADS, 1)
     kq_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const GemmArgs a) {
+  static_assert(!(MOE && PAIR), "the MoE kernel runs unpaired");
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
   constexpr int RAW_BYTES = RawBox<WT>::BYTES * GM_BM;
@@ -309,6 +329,9 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
   int* s_offsets = s_counts + a.n_experts;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
+  const int tile0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int tile_stride = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < a.raw_stages; ++i) {
@@ -316,12 +339,12 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
       mbar_init(&raw_empty[i], GM_DQ_WARPS);
     }
     for (int i = 0; i < a.k_stages; ++i) {
-      mbar_init(&k_full[i], 1 + GM_DQ_GROUP);
+      mbar_init(&k_full[i], 1 + (PAIR ? 2 : 1) * GM_DQ_GROUP);
       mbar_init(&k_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 4);
+      mbar_init(&acc_empty[i], PAIR ? 8 : 4);
     }
     for (int i = 0; i < GM_TQ; ++i) {
       mbar_init(&tq_full[i], 1);
@@ -331,8 +354,13 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
     fence_mbar_init();
   }
   if (warp == GM_MMA_WARP) {
-    tmem_alloc(tmem_slot, GM_TMEM_COLS);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(tmem_slot, GM_TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, GM_TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   if (warp == GM_RAW_WARP && lane == 0) {
     tma_prefetch_desc(&tmW);
@@ -355,6 +383,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();  // the other CTA's barriers and tensor memory are ready too
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   if (MOE)
@@ -364,12 +393,12 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
 
   if (warp == GM_RAW_WARP) {
     // ---- raw weight producer -------------------------------------------------
-    // It also picks the CTA's tiles: the first is blockIdx.x, later ones come
-    // from the MoE tile queue or, for the dense GEMM, a stride of gridDim.x.
+    // It also picks the CTA's tiles: the first is its CTA (pair) index, later
+    // ones come from the MoE tile queue or, for the dense GEMM, a fixed stride.
     if (lane == 0) {
       int st = 0, qi = 0;
       uint32_t ph = 0, qph = 0;
-      for (int t = blockIdx.x;; ) {
+      for (int t = tile0;;) {
         if (!mbar_wait(&tq_empty[qi], qph ^ 1, abort, a.err)) break;
         tq_ids[qi] = t;
         mbar_arrive(&tq_full[qi]);
@@ -378,7 +407,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
           qph ^= 1;
         }
         if (t >= total_tiles || *abort) break;
-        const Tile T = decode_tile<MOE>(a, t, s_tile_start, s_counts, s_offsets);
+        const Tile T = decode_tile<MOE, PAIR>(a, t, rank, s_tile_start, s_counts, s_offsets);
         for (int kb = T.kb0; kb < T.kb1; ++kb) {
           if (!mbar_wait(&raw_empty[st], ph ^ 1, abort, a.err)) break;
           mbar_expect_tx(&raw_full[st], RAW_BYTES);
@@ -389,7 +418,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
             ph ^= 1;
           }
         }
-        t = MOE ? static_cast<int>(gridDim.x) + atomicAdd(a.tile_queue, 1) : t + static_cast<int>(gridDim.x);
+        t = MOE ? static_cast<int>(gridDim.x) + atomicAdd(a.tile_queue, 1) : t + tile_stride;
       }
     }
   } else if (warp == GM_B_WARP) {
@@ -401,15 +430,38 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
       for (;;) {
         const int t = tq_pop(tq_full, tq_empty, tq_ids, qi, qph, true, abort, a.err);
         if (t >= total_tiles || *abort) break;
-        const Tile T = decode_tile<MOE>(a, t, s_tile_start, s_counts, s_offsets);
-        const int nbox = (T.ncols + GM_BBOX - 1) / GM_BBOX;
+        const Tile T = decode_tile<MOE, PAIR>(a, t, rank, s_tile_start, s_counts, s_offsets);
+        // Boxes of 64 token rows that hold at least one valid token. A pair
+        // splits the tile's bn rows in halves; the even CTA's barrier expects
+        // the bytes of both halves.
+        int nbox, xrow, expect;
+        if (PAIR) {
+          const int hb = a.bn / (2 * GM_BBOX);
+          const int n0 = min(hb, (T.ncols + GM_BBOX - 1) / GM_BBOX);
+          const int n1 = max(0, min(hb, (T.ncols - hb * GM_BBOX + GM_BBOX - 1) / GM_BBOX));
+          nbox = rank ? n1 : n0;
+          xrow = T.xrow0 + rank * hb * GM_BBOX;
+          expect = (n0 + n1) * GM_BBOX_BYTES;
+        } else {
+          nbox = (T.ncols + GM_BBOX - 1) / GM_BBOX;
+          xrow = T.xrow0;
+          expect = nbox * GM_BBOX_BYTES;
+        }
         for (int kb = T.kb0; kb < T.kb1 && !*abort; ++kb) {
           for (int s = 0; s < 4; ++s) {
             if (!mbar_wait(&k_empty[st], ph ^ 1, abort, a.err)) break;
-            mbar_expect_tx(&k_full[st], nbox * GM_BBOX_BYTES);
-            for (int j = 0; j < nbox; ++j)
-              tma_load_2d(sB + st * a.b_stage_bytes + j * GM_BBOX_BYTES, &tmX, &k_full[st],
-                          kb * QK_K + s * GM_BK, T.xrow0 + j * GM_BBOX);
+            if (PAIR) {
+              const uint32_t full_cl = mapa_shared(&k_full[st], 0);
+              if (rank == 0) mbar_expect_tx(&k_full[st], expect);
+              for (int j = 0; j < nbox; ++j)
+                tma_load_2d_pair(sB + st * a.b_stage_bytes + j * GM_BBOX_BYTES, &tmX, full_cl,
+                                 kb * QK_K + s * GM_BK, xrow + j * GM_BBOX);
+            } else {
+              mbar_expect_tx(&k_full[st], expect);
+              for (int j = 0; j < nbox; ++j)
+                tma_load_2d(sB + st * a.b_stage_bytes + j * GM_BBOX_BYTES, &tmX, &k_full[st],
+                            kb * QK_K + s * GM_BK, xrow + j * GM_BBOX);
+            }
             if (++st == a.k_stages) {
               st = 0;
               ph ^= 1;
@@ -417,6 +469,26 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
           }
         }
       }
+      // A pair's MMA commits arrive on this CTA's k_empty from the other SM:
+      // wait until every stage filled here has been released, so that none is
+      // still in flight when the CTA exits.
+      if (PAIR && !*abort) {
+        for (int i = 0; i < a.k_stages; ++i) {
+          if (!mbar_wait_bounded(&k_empty[st], ph ^ 1)) break;
+          if (++st == a.k_stages) {
+            st = 0;
+            ph ^= 1;
+          }
+        }
+      }
+    }
+  } else if (warp == GM_MMA_WARP && PAIR && rank != 0) {
+    // The odd CTA of a pair issues no MMAs: this warp only follows the tile ring.
+    int qi = 0;
+    uint32_t qph = 0;
+    for (;;) {
+      const int t = tq_pop(tq_full, tq_empty, tq_ids, qi, qph, false, abort, a.err);
+      if (t >= total_tiles || *abort) break;
     }
   } else if (warp == GM_MMA_WARP) {
     // ---- tensor-core issuer --------------------------------------------------
@@ -426,16 +498,19 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
     uint32_t kph = 0, qph = 0;
     const uint32_t a_tmem0 = tmem_base + a.a_col0;
     const uint64_t b_desc0 = smem_desc_sw128(smem_u32(sB));
-    for (int it = 0;; ++it) {
+    int it = 0;
+    for (;; ++it) {
       const int t = tq_pop(tq_full, tq_empty, tq_ids, qi, qph, false, abort, a.err);
       if (t >= total_tiles || *abort) break;
-      const Tile T = decode_tile<MOE>(a, t, s_tile_start, s_counts, s_offsets);
+      const Tile T = decode_tile<MOE, PAIR>(a, t, rank, s_tile_start, s_counts, s_offsets);
       const int acc = (a.n_acc == 2) ? (it & 1) : 0;
       const uint32_t acc_ph = (a.n_acc == 2) ? ((it >> 1) & 1) : (it & 1);
       if (!mbar_wait(&acc_empty[acc], acc_ph ^ 1, abort, a.err)) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * a.acc_cols;
-      const uint32_t idesc = idesc_f16_f32(GM_BM, (T.ncols + 15) & ~15);
+      // a pair always multiplies the full bn rows of B (each CTA holds bn / 2)
+      const uint32_t idesc =
+          PAIR ? idesc_f16_f32(2 * GM_BM, a.bn) : idesc_f16_f32(GM_BM, (T.ncols + 15) & ~15);
       const int nsteps = (T.kb1 - T.kb0) * 4;
       bool ok = true;
       for (int ks = 0; ks < nsteps; ++ks) {
@@ -449,9 +524,16 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
         const uint64_t bd = b_desc0 + static_cast<uint64_t>((kst * a.b_stage_bytes) >> 4);
         if (elect_one()) {
 #pragma unroll
-          for (int k = 0; k < GM_BK / 16; ++k)  // +32 bytes per K=16 step inside the 128-byte row
-            umma_f16_ta(d_tmem, at + 8 * k, bd + 2 * k, idesc, (ks == 0 && k == 0) ? 0u : 1u);
-          umma_commit(&k_empty[kst]);
+          for (int k = 0; k < GM_BK / 16; ++k) {  // +32 bytes per K=16 step inside the 128-byte row
+            if (PAIR)
+              umma_f16_ta_pair(d_tmem, at + 8 * k, bd + 2 * k, idesc, (ks == 0 && k == 0) ? 0u : 1u);
+            else
+              umma_f16_ta(d_tmem, at + 8 * k, bd + 2 * k, idesc, (ks == 0 && k == 0) ? 0u : 1u);
+          }
+          if (PAIR)
+            umma_commit_pair(&k_empty[kst], 0x3);
+          else
+            umma_commit(&k_empty[kst]);
         }
         __syncwarp();
         if (++kst == a.k_stages) {
@@ -459,39 +541,69 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
           kph ^= 1;
         }
       }
-      if (elect_one()) umma_commit(&acc_full[acc]);
+      if (elect_one()) {
+        if (PAIR)
+          umma_commit_pair(&acc_full[acc], 0x3);
+        else
+          umma_commit(&acc_full[acc]);
+      }
       __syncwarp();
       if (!ok) break;
     }
+    // A pair: the other CTA's epilogue arrives on acc_empty here; wait for the
+    // releases of the last accumulators before the CTA exits.
+    if (PAIR && !*abort) {
+      for (int j = 0; j < a.n_acc; ++j, ++it) {
+        const int acc = (a.n_acc == 2) ? (it & 1) : 0;
+        const uint32_t acc_ph = (a.n_acc == 2) ? ((it >> 1) & 1) : (it & 1);
+        if (!mbar_wait_bounded(&acc_empty[acc], acc_ph ^ 1)) break;
+      }
+    }
   } else if (warp < GM_DQ_WARPS) {
     // ---- weight unpackers ----------------------------------------------------
-    // warp w owns tensor-memory lanes 32 (w % 4) .. +31 (rows of the tile), the
-    // half (w / 4) % 2 of a K step, and the K steps of parity w / 8
+    // warp w owns tensor-memory lanes 32 (w % 4) .. +31 (rows of the tile) and
+    // the half (w / 4) % 2 of each K step; the two groups of eight warps
+    // (w / 8) take alternate steps of a super-block (Q4_K: steps 0, 2 and 1, 3;
+    // Q6_K: the two steps of one half of the block, which share their loads)
     const int r = 32 * (warp & 3) + lane, hf = (warp >> 2) & 1, grp = warp >> 3;
-    const uint32_t a_row = tmem_base + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + a.a_col0 + 16 * hf;
-    int rst = 0, ast = 0, gs = 0, qi = 0;
+    const uint32_t a_lane = tmem_base + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + a.a_col0;
+    int rst = 0, ast = 0, qi = 0;
     uint32_t rph = 0, aph = 0, qph = 0;
     for (;;) {
       const int t = tq_pop(tq_full, tq_empty, tq_ids, qi, qph, false, abort, a.err);
       if (t >= total_tiles || *abort) break;
-      const Tile T = decode_tile<MOE>(a, t, s_tile_start, s_counts, s_offsets);
+      const Tile T = decode_tile<MOE, PAIR>(a, t, rank, s_tile_start, s_counts, s_offsets);
       for (int kb = T.kb0; kb < T.kb1 && !*abort; ++kb) {
         if (!mbar_wait(&raw_full[rst], rph, abort, a.err)) break;
         const uint8_t* raw = sRaw + rst * RAW_BYTES;
-        for (int s = 0; s < 4; ++s, ++gs) {
-          if ((gs & 1) == grp) {
+        const int rem = (WT == KQ_Q6_K) ? ((kb * Q6K_BYTES) & 15) : 0;
+        uint4 hdr = make_uint4(0u, 0u, 0u, 0u);
+        Q6Half q6;
+        for (int s = 0; s < 4; ++s) {
+          const bool mine = (WT == KQ_Q4_K) ? ((s & 1) == grp) : ((s >> 1) == grp);
+          if (mine) {
             if (!mbar_wait(&k_empty[ast], aph ^ 1, abort, a.err)) break;
             tc_fence_after();
-            uint32_t o[16];
-            if (WT == KQ_Q4_K)
-              dequant_q4k(raw, s, r, hf, o);
-            else
-              dequant_q6k(raw, (kb * Q6K_BYTES) & 15, s, r, hf, o);
-            tmem_st_32x32b_x16(a_row + ast * GM_A_COLS, o);
+            uint32_t lo[8], hi[8];
+            if (WT == KQ_Q4_K) {
+              if (s < 2) hdr = *reinterpret_cast<const uint4*>(raw + r * Q4K_BYTES);
+              dequant_q4k(hdr, raw, s, r, hf, lo, hi);
+            } else {
+              if ((s & 1) == 0) load_q6k_half(raw, rem, s >> 1, r, hf, q6);
+              dequant_q6k(raw, rem, q6, s, r, hf, lo, hi);
+            }
+            const uint32_t col = a_lane + ast * GM_A_COLS + 8 * hf;
+            tmem_st_32x32b_x8(col, lo);
+            tmem_st_32x32b_x8(col + 16, hi);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&k_full[ast]);
+            if (lane == 0) {
+              if (PAIR)
+                mbar_arrive_cluster(mapa_shared(&k_full[ast], 0));
+              else
+                mbar_arrive(&k_full[ast]);
+            }
           }
           if (++ast == a.k_stages) {
             ast = 0;
@@ -515,7 +627,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
     for (int it = 0;; ++it) {
       const int t = tq_pop(tq_full, tq_empty, tq_ids, qi, qph, false, abort, a.err);
       if (t >= total_tiles || *abort) break;
-      const Tile T = decode_tile<MOE>(a, t, s_tile_start, s_counts, s_offsets);
+      const Tile T = decode_tile<MOE, PAIR>(a, t, rank, s_tile_start, s_counts, s_offsets);
       const int acc = (a.n_acc == 2) ? (it & 1) : 0;
       const uint32_t acc_ph = (a.n_acc == 2) ? ((it >> 1) & 1) : (it & 1);
       if (!mbar_wait(&acc_full[acc], acc_ph, abort, a.err)) break;
@@ -544,15 +656,24 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+      if (lane == 0) {
+        if (PAIR)
+          mbar_arrive_cluster(mapa_shared(&acc_empty[acc], 0));
+        else
+          mbar_arrive(&acc_empty[acc]);
+      }
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();  // no CTA of the pair frees its memory while the other may still use it
   if (warp == GM_MMA_WARP) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, GM_TMEM_COLS);
+    if (PAIR)
+      tmem_dealloc_pair(tmem_base, GM_TMEM_COLS);
+    else
+      tmem_dealloc(tmem_base, GM_TMEM_COLS);
   }
 }
 
@@ -722,14 +843,15 @@ static int raw_box_bytes(int wtype) { return wtype == KQ_Q4_K ? RawBox<KQ_Q4_K>:
 // 64-K A stages of 32 columns. Shared memory: the x_hat (B) ring, whose L2 ->
 // shared memory round trip (1-2k cycles) the stages in flight must cover, and
 // the raw weight ring (each super-block feeds four K steps; they come from HBM).
-static bool choose_stages(int wtype, int bn, int n_experts, GemmArgs* a, size_t* smem) {
+static bool choose_stages(int wtype, int bn, int n_experts, bool pair, GemmArgs* a, size_t* smem) {
   const int acc_cols = (bn + 15) & ~15;
   a->n_acc = (2 * acc_cols + 4 * GM_A_COLS <= GM_TMEM_COLS) ? 2 : 1;
   a->acc_cols = acc_cols;
   a->a_col0 = a->n_acc * acc_cols;
   const int a_max = std::min(GM_A_MAX_STAGES, (GM_TMEM_COLS - a->a_col0) / GM_A_COLS);
   if (a_max < 2) return false;
-  const int b_bytes = ((bn + GM_BBOX - 1) / GM_BBOX) * GM_BBOX_BYTES;
+  // a CTA of a pair holds half of the bn x_hat rows of a stage
+  const int b_bytes = (pair ? bn / (2 * GM_BBOX) : (bn + GM_BBOX - 1) / GM_BBOX) * GM_BBOX_BYTES;
   const int raw_bytes = raw_box_bytes(wtype) * GM_BM;
   const int tables = (n_experts > 0 ? 3 * (n_experts + 1) * 4 : 0) + 64 + GM_TQ * 20;
   const int budget = GM_SMEM_LIMIT - (1024 + tables + 512);
@@ -748,24 +870,28 @@ static bool choose_stages(int wtype, int bn, int n_experts, GemmArgs* a, size_t*
   return true;
 }
 
+// CTA pairs need bn = 128 or 256 (two whole 64-row x_hat boxes per half or
+// one) and an even number of 128-row tiles (no pair half lies wholly past M).
 GemmPlan plan_gemm(int wtype, int64_t M, int64_t K, int64_t N, int num_sms) {
   (void)wtype;
   GemmPlan p{};
-  const int bn = static_cast<int>(N >= GM_BNMAX ? GM_BNMAX : round_up64(N, GM_BBOX));
+  p.bn = static_cast<int>(N >= GM_BNMAX ? GM_BNMAX : round_up64(N, GM_BBOX));
   p.m_tiles = static_cast<int>((M + GM_BM - 1) / GM_BM);
-  p.n_tiles = static_cast<int>((N + bn - 1) / bn);
+  p.n_tiles = static_cast<int>((N + p.bn - 1) / p.bn);
+  p.pair = (p.bn == 128 || p.bn == 256) && p.m_tiles % 2 == 0 && num_sms >= 2;
   const int nb = static_cast<int>(K / QK_K);
-  const int tiles = p.m_tiles * p.n_tiles;
+  const int slots = p.pair ? num_sms / 2 : num_sms;
+  const int tiles = (p.pair ? p.m_tiles / 2 : p.m_tiles) * p.n_tiles;
   int splits = 1;
-  if (tiles < num_sms) {
-    splits = num_sms / tiles;
+  if (tiles < slots) {
+    splits = slots / tiles;
     if (splits > nb) splits = nb;
     if (splits > 16) splits = 16;
     if (splits < 1) splits = 1;
   }
   p.splits = splits;
-  const int64_t total = static_cast<int64_t>(tiles) * splits;
-  p.grid = static_cast<int>(total < num_sms ? total : num_sms);
+  const int64_t units = static_cast<int64_t>(p.m_tiles) * p.n_tiles * splits;
+  p.grid = static_cast<int>(units < num_sms ? units : num_sms);
   p.xhat_bytes = static_cast<size_t>(round_up64(N * K * 2, 1024));
   p.partial_bytes = splits > 1 ? static_cast<size_t>(round_up64(static_cast<int64_t>(splits) * N * M * 4, 1024)) : 0;
   p.total_bytes = p.xhat_bytes + p.partial_bytes;
@@ -775,9 +901,63 @@ GemmPlan plan_gemm(int wtype, int64_t M, int64_t K, int64_t N, int num_sms) {
 template <int WT, bool MOE>
 static cudaError_t launch_kernel(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmArgs& a, int grid,
                                  size_t smem, cudaStream_t s) {
-  cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(kq_gemm_kernel<WT, MOE>), 2 + 2 * WT + (MOE ? 1 : 0));
+  cudaError_t e =
+      allow_max_smem(reinterpret_cast<const void*>(kq_gemm_kernel<WT, MOE, false>), 2 + 2 * WT + (MOE ? 1 : 0));
   if (e != cudaSuccess) return e;
-  return launch_pdl(kq_gemm_kernel<WT, MOE>, dim3(grid), dim3(GM_THREADS), smem, s, tmW, tmX, a);
+  return launch_pdl(kq_gemm_kernel<WT, MOE, false>, dim3(grid), dim3(GM_THREADS), smem, s, tmW, tmX, a);
+}
+
+// Clusters of two CTAs (one per SM) that can be resident at once on the
+// current device, looked up once per device and weight type; 0 when pairs
+// cannot run.
+template <int WT>
+static int pair_clusters(cudaLaunchConfig_t cfg) {
+  static std::mutex mu;
+  static int cached[2][64];
+  static bool known[2][64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  const int w = WT == KQ_Q4_K ? 0 : 1;
+  if (!known[w][dev]) {
+    int n = 0;
+    cfg.gridDim = dim3(2);
+    if (cudaOccupancyMaxActiveClusters(&n, kq_gemm_kernel<WT, false, true>, &cfg) != cudaSuccess) {
+      (void)cudaGetLastError();
+      n = 0;
+    }
+    cached[w][dev] = n;
+    known[w][dev] = true;
+  }
+  return cached[w][dev];
+}
+
+// Launches the paired dense kernel over `units` pair tiles; *launched = false
+// (and nothing queued) when the device cannot run CTA pairs.
+template <int WT>
+static cudaError_t launch_pair(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmArgs& a, int units,
+                               size_t smem, cudaStream_t s, bool* launched) {
+  *launched = false;
+  cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(kq_gemm_kernel<WT, false, true>), 11 + WT);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(GM_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  const int clusters = pair_clusters<WT>(cfg);
+  if (clusters < 1) return cudaSuccess;
+  cfg.gridDim = dim3(2 * std::min(units, clusters));
+  *launched = true;
+  return cudaLaunchKernelEx(&cfg, kq_gemm_kernel<WT, false, true>, tmW, tmX, a);
 }
 
 static cudaError_t dispatch(int wtype, bool moe, const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmArgs& a,
@@ -819,21 +999,35 @@ cudaError_t launch_gemm(int wtype, const void* W, const float* X, float* Y, int6
   a.M = static_cast<int>(M);
   a.N = static_cast<int>(N);
   a.nb = static_cast<int>(K / QK_K);
-  a.m_tiles = plan.m_tiles;
   a.n_tiles = plan.n_tiles;
   a.splits = plan.splits;
-  a.bn = static_cast<int>(N >= GM_BNMAX ? GM_BNMAX : round_up64(N, GM_BBOX));
+  a.bn = plan.bn;
   a.Y = Y;
   a.partial = partial;
   a.n_experts = 0;
   a.err = err;
-  size_t smem = 0;
-  if (!choose_stages(wtype, a.bn, 0, &a, &smem)) {
-    *status = KQ_ERR_SHAPE;
-    return cudaSuccess;
+  bool launched = false;
+  if (plan.pair) {
+    GemmArgs ap = a;
+    ap.m_tiles = plan.m_tiles / 2;
+    size_t smem = 0;
+    if (choose_stages(wtype, plan.bn, 0, true, &ap, &smem)) {
+      const int units = ap.m_tiles * plan.n_tiles * plan.splits;
+      e = wtype == KQ_Q4_K ? launch_pair<KQ_Q4_K>(tmW, tmX, ap, units, smem, s, &launched)
+                           : launch_pair<KQ_Q6_K>(tmW, tmX, ap, units, smem, s, &launched);
+      if (e != cudaSuccess) return e;
+    }
   }
-  e = dispatch(wtype, false, tmW, tmX, a, plan.grid, smem, s);
-  if (e != cudaSuccess) return e;
+  if (!launched) {
+    a.m_tiles = plan.m_tiles;
+    size_t smem = 0;
+    if (!choose_stages(wtype, plan.bn, 0, false, &a, &smem)) {
+      *status = KQ_ERR_SHAPE;
+      return cudaSuccess;
+    }
+    e = dispatch(wtype, false, tmW, tmX, a, plan.grid, smem, s);
+    if (e != cudaSuccess) return e;
+  }
   if (plan.splits > 1) {
     const int64_t n = N * M;
     const int64_t threads = (n + 3) / 4;
@@ -922,7 +1116,7 @@ cudaError_t launch_moe(int wtype, const void* W, int n_experts, const int32_t* i
   a.tile_queue = tile_queue;
   a.err = err;
   size_t smem = 0;
-  if (!choose_stages(wtype, MOE_BN, n_experts, &a, &smem)) {
+  if (!choose_stages(wtype, MOE_BN, n_experts, false, &a, &smem)) {
     *status = KQ_ERR_SHAPE;
     return cudaSuccess;
   }

@@ -19,10 +19,14 @@ cudaError_t launch_gather_xhat(const float* X, __half* Xh, int64_t K, int64_t n_
 cudaError_t launch_matvec(int wtype, const void* W, const float* x, float* y, int64_t M, int64_t K, int* err,
                           int num_sms, cudaStream_t s, int* status);
 
-// Dense prefill GEMM plan: tiles of 128 weight rows x up to 256 tokens, with
-// the K range optionally split across CTAs (fixed-order reduction after).
+// Dense prefill GEMM plan: tiles of 128 weight rows x up to bn = 256 tokens
+// (256 rows for a CTA pair), with the K range optionally split across CTAs
+// (fixed-order reduction after).
 struct GemmPlan {
-  int m_tiles, n_tiles, splits, grid;
+  int m_tiles;  // 128-row tiles
+  int n_tiles, bn, splits;
+  bool pair;    // run as CTA pairs (2-SM MMAs) when the device allows it
+  int grid;     // CTAs of an unpaired launch
   size_t xhat_bytes, partial_bytes, total_bytes;
 };
 GemmPlan plan_gemm(int wtype, int64_t M, int64_t K, int64_t N, int num_sms);

@@ -27,6 +27,11 @@ def _run(wtype, W, X, M, K):
     ("q4_k", 1, 256, 1),
     ("q6_k", 136, 2048, 40),
     ("q6_k", 256, 4096, 257),
+    # CTA pairs (even number of 128-row tiles, token tile of 128 or 256)
+    ("q4_k", 512, 1024, 128),      # bn = 128: one 64-row x_hat box per CTA
+    ("q4_k", 500, 512, 200),       # bn = 256, ragged M and ragged second half
+    ("q6_k", 512, 2048, 96),       # bn = 128, second half partly past N
+    ("q4_k", 256, 4096, 256),      # one pair tile, K split 16 ways
 ])
 def test_small_shapes_full_parity(wtype, M, K, N):
     rng = np.random.default_rng(M + 3 * K + 7 * N)
