@@ -32,6 +32,7 @@ def _run(wtype, W, X, M, K):
     ("q4_k", 500, 512, 200),       # bn = 256, ragged M and ragged second half
     ("q6_k", 512, 2048, 96),       # bn = 128, second half partly past N
     ("q4_k", 256, 4096, 256),      # one pair tile, K split 16 ways
+    ("q4_k", 20480, 256, 100),     # 80 pair tiles: some pairs take two, alternating accumulators
 ])
 def test_small_shapes_full_parity(wtype, M, K, N):
     rng = np.random.default_rng(M + 3 * K + 7 * N)

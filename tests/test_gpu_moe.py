@@ -34,6 +34,8 @@ def test_workload_full_parity():
     ("q4_k", 3, 128, 256, 300, 2),     # buckets larger than one 128-token tile
     ("q4_k", 16, 64, 1024, 9, 1),      # most experts get no token
     ("q6_k", 4, 136, 2048, 50, 2),
+    ("q4_k", 6, 256, 512, 300, 2),     # buckets of more than one 128-token tile
+    ("q6_k", 3, 512, 2048, 70, 3),
 ])
 def test_small_shapes_full_parity(wtype, E, M, K, T, top_k):
     rng = np.random.default_rng(E * 100 + T)
@@ -45,8 +47,9 @@ def test_small_shapes_full_parity(wtype, E, M, K, T, top_k):
     assert_within_bound(Y, Yr, B, f"moe {wtype} E={E} T={T}")
 
 
-def test_all_tokens_to_one_expert():
-    E, M, K, T = 4, 128, 512, 260
+@pytest.mark.parametrize("M", [128, 256])
+def test_all_tokens_to_one_expert(M):
+    E, K, T = 4, 512, 260
     rng = np.random.default_rng(9)
     W = syn.q4_k_weights(rng, E * M, K)
     X = syn.activations(rng, K, T)
@@ -56,8 +59,9 @@ def test_all_tokens_to_one_expert():
     assert_within_bound(Y, Yr, B, "one expert")
 
 
-def test_out_of_range_expert_id_is_reported_and_zeroed():
-    E, M, K, T, top_k = 4, 128, 256, 10, 2
+@pytest.mark.parametrize("M", [128, 256])
+def test_out_of_range_expert_id_is_reported_and_zeroed(M):
+    E, K, T, top_k = 4, 256, 10, 2
     rng = np.random.default_rng(4)
     W = syn.q4_k_weights(rng, E * M, K)
     X = syn.activations(rng, K, T)
