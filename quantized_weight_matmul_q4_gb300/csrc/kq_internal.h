@@ -14,8 +14,10 @@ cudaError_t launch_quantize_q8_1(const float* X, void* Xq, int64_t K, int64_t N,
 cudaError_t launch_quantize_xhat(const float* X, __half* Xh, int64_t K, int64_t rows, int num_sms, cudaStream_t s);
 // MoE: for every slot i with bucket row p = slot_pos[i] >= 0, writes the x_hat
 // of token i / top_k to row p of Xh and entries[p] = i.
-cudaError_t launch_gather_xhat(const float* X, __half* Xh, int64_t K, int64_t n_slots, int top_k,
-                               const int* slot_pos, int* entries, int num_sms, cudaStream_t s);
+// Bucket row slot_pos[i] of Xh <- row i / top_k of Xtok (x_hat per token);
+// entries[slot_pos[i]] = i. Negative positions are skipped.
+cudaError_t launch_gather_rows(const __half* Xtok, __half* Xh, int64_t K, int64_t n_slots, int top_k,
+                               const int* slot_pos, int* entries, cudaStream_t s);
 cudaError_t launch_matvec(int wtype, const void* W, const float* x, float* y, int64_t M, int64_t K, int* err,
                           int num_sms, cudaStream_t s, int* status);
 
@@ -35,7 +37,7 @@ cudaError_t launch_gemm(int wtype, const void* W, const float* X, float* Y, int6
 
 struct MoePlan {
   int m_tiles;
-  size_t off_counts, off_offsets, off_tiles, off_queue, off_entries, off_src, off_xhat, total_bytes;
+  size_t off_counts, off_offsets, off_tiles, off_queue, off_entries, off_src, off_xtok, off_xhat, total_bytes;
 };
 MoePlan plan_moe(int wtype, int64_t M, int64_t K, int64_t T, int n_experts, int top_k);
 cudaError_t launch_moe(int wtype, const void* W, int n_experts, const int32_t* ids, int top_k, const float* X,

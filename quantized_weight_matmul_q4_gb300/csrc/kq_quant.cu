@@ -62,25 +62,37 @@ __global__ void __launch_bounds__(256) quantize_xhat_kernel(const float* __restr
   }
 }
 
-// MoE gather: quad c of slot i quantises x[i / top_k][4c .. 4c+3] and writes
-// it to bucket row slot_pos[i] (skipped when negative); the first quad of a
-// slot also records entries[slot_pos[i]] = i. One quad per thread: many short
-// CTAs, so the grouped GEMM that follows can take SMs as they free up. K / 4 is
-// a multiple of 64, so a warp's quads belong to one slot and take one path.
-__global__ void __launch_bounds__(256) gather_xhat_kernel(const float* __restrict__ X, __half* __restrict__ Xh,
-                                                          int K, int64_t n_slots, int top_k,
-                                                          const int* __restrict__ slot_pos, int* __restrict__ entries) {
+// MoE gather: bucket row slot_pos[i] of Xh is the x_hat row of slot i's token
+// (row i / top_k of Xtok, quantised once per token); slots with a negative
+// position are skipped. One warp per slot, each lane moving 16-byte pieces of
+// the row with GR_UNROLL loads in flight; lane 0 also records
+// entries[slot_pos[i]] = i. K * 2 bytes is a multiple of 512, so every lane
+// moves whole rounds of 32 x 16 bytes.
+constexpr int GR_WARPS = 8;
+constexpr int GR_UNROLL = 8;
+__global__ void __launch_bounds__(GR_WARPS * 32) gather_rows_kernel(const __half* __restrict__ Xtok,
+                                                                    __half* __restrict__ Xh, int K, int64_t n_slots,
+                                                                    int top_k, const int* __restrict__ slot_pos,
+                                                                    int* __restrict__ entries) {
   pdl_enter();
-  const int64_t t = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
-  const int64_t kq4 = K >> 2;
-  const int64_t i = t / kq4;
-  const int64_t c = t - i * kq4;
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * GR_WARPS + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
   if (i >= n_slots) return;
   const int pos = __ldg(slot_pos + i);
   if (pos < 0) return;
-  const float4 v = __ldg(reinterpret_cast<const float4*>(X + (i / top_k) * K) + c);
-  reinterpret_cast<uint2*>(Xh + static_cast<int64_t>(pos) * K)[c] = xhat4(quantize_quad(v));
-  if (c == 0) entries[pos] = static_cast<int>(i);
+  const uint4* src = reinterpret_cast<const uint4*>(Xtok + (i / top_k) * static_cast<int64_t>(K));
+  uint4* dst = reinterpret_cast<uint4*>(Xh + static_cast<int64_t>(pos) * K);
+  const int n16 = K / 8;  // 16-byte pieces per row
+  for (int c0 = lane; c0 < n16; c0 += 32 * GR_UNROLL) {
+    uint4 v[GR_UNROLL];
+#pragma unroll
+    for (int u = 0; u < GR_UNROLL; ++u)
+      if (c0 + 32 * u < n16) v[u] = __ldg(src + c0 + 32 * u);
+#pragma unroll
+    for (int u = 0; u < GR_UNROLL; ++u)
+      if (c0 + 32 * u < n16) dst[c0 + 32 * u] = v[u];
+  }
+  if (lane == 0) entries[pos] = static_cast<int>(i);
 }
 
 static unsigned xhat_grid(int64_t quads, int num_sms) {
@@ -96,13 +108,11 @@ cudaError_t launch_quantize_xhat(const float* X, __half* Xh, int64_t K, int64_t 
                     static_cast<int>(K), rows);
 }
 
-cudaError_t launch_gather_xhat(const float* X, __half* Xh, int64_t K, int64_t n_slots, int top_k,
-                               const int* slot_pos, int* entries, int num_sms, cudaStream_t s) {
-  (void)num_sms;
-  const int64_t quads = n_slots * (K / 4);
-  if (quads == 0) return cudaSuccess;
-  return launch_pdl(gather_xhat_kernel, dim3(static_cast<unsigned>((quads + 255) / 256)), dim3(256), 0, s, X, Xh,
-                    static_cast<int>(K), n_slots, top_k, slot_pos, entries);
+cudaError_t launch_gather_rows(const __half* Xtok, __half* Xh, int64_t K, int64_t n_slots, int top_k,
+                               const int* slot_pos, int* entries, cudaStream_t s) {
+  if (n_slots == 0) return cudaSuccess;
+  return launch_pdl(gather_rows_kernel, dim3(static_cast<unsigned>((n_slots + GR_WARPS - 1) / GR_WARPS)),
+                    dim3(GR_WARPS * 32), 0, s, Xtok, Xh, static_cast<int>(K), n_slots, top_k, slot_pos, entries);
 }
 
 cudaError_t launch_quantize_q8_1(const float* X, void* Xq, int64_t K, int64_t N, cudaStream_t s) {
