@@ -115,6 +115,12 @@ KQ_API kq_status kq_matvec(int wtype, const void* W, const float* x, float* y, i
  * architecture; [GAP] T1). X is quantised to Q8_1 (as x_hat = fp16(d_h * q))
  * into the workspace once per call; weight super-blocks are staged by TMA and
  * unpacked to fp16 into tensor memory; tcgen05 MMAs accumulate in tensor memory.
+ * A few tokens are a decode rather than a GEMM: Q4_K with 2 <= N <= 5 runs on
+ * the decode matvec path instead ([MMVQ] §2: dp4a on the Q8_1 codes, the min
+ * term from the block sums; the tokens' codes are made once into the
+ * workspace, the weights are read once for all tokens). Both paths meet the
+ * accuracy bound above; a token's result may differ in the last bits with the
+ * number of tokens in the call (the partial sums are grouped differently).
  * W: M x K weights; X: fp32 [N][K]; Y: fp32 [N][M], written.
  * ws: device workspace of at least kq_workspace_bytes(KQ_OP_GEMM, ...) bytes.
  * Q6_K needs K % 2048 == 0 (rows whose byte length is a multiple of 16).

@@ -892,6 +892,7 @@ GemmPlan plan_gemm(int wtype, int64_t M, int64_t K, int64_t N, int num_sms) {
   p.splits = splits;
   const int64_t units = static_cast<int64_t>(p.m_tiles) * p.n_tiles * splits;
   p.grid = static_cast<int>(units < num_sms ? units : num_sms);
+  p.num_sms = num_sms;
   p.xhat_bytes = static_cast<size_t>(round_up64(N * K * 2, 1024));
   p.partial_bytes = splits > 1 ? static_cast<size_t>(round_up64(static_cast<int64_t>(splits) * N * M * 4, 1024)) : 0;
   p.total_bytes = p.xhat_bytes + p.partial_bytes;
@@ -985,6 +986,14 @@ static bool xhat_tmap(CUtensorMap* tm, const void* Xh, int64_t rows, int64_t K) 
 cudaError_t launch_gemm(int wtype, const void* W, const float* X, float* Y, int64_t M, int64_t K, int64_t N,
                         void* ws, const GemmPlan& plan, int* err, cudaStream_t s, int* status) {
   *status = KQ_OK;
+  // A few tokens are a decode, not a GEMM: the tensor-core tiles would be
+  // nearly empty, so Q4_K runs on the matvec path, which streams the weights
+  // once and multiplies each staged block with every token.
+  if (wtype == KQ_Q4_K && N <= LR_TOKENS_MAX) {
+    bool handled = false;
+    cudaError_t e = launch_matvec_tokens(W, X, Y, M, K, N, ws, plan.xhat_bytes, err, plan.num_sms, s, &handled);
+    if (e != cudaSuccess || handled) return e;
+  }
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   __half* xh = reinterpret_cast<__half*>(wsb);
   float* partial = reinterpret_cast<float*>(wsb + plan.xhat_bytes);

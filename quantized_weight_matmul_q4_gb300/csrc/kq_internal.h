@@ -21,6 +21,16 @@ cudaError_t launch_gather_rows(const __half* Xtok, __half* Xh, int64_t K, int64_
 cudaError_t launch_matvec(int wtype, const void* W, const float* x, float* y, int64_t M, int64_t K, int* err,
                           int num_sms, cudaStream_t s, int* status);
 
+// Several tokens (Q4_K, 2 <= N <= LR_TOKENS_MAX) on the decode matvec path:
+// Y[N][M] = dequant(W) . X[N][K], the tokens' Q8_1 codes made once into
+// `scratch` (device memory; at most ~1.25 N K + 256 N bytes are used);
+// *handled = false when the shape or the scratch does not suit it (nothing
+// queued).
+constexpr int LR_TOKENS_MAX = 5;  // measured crossover with the tensor-core GEMM at the decode shapes
+cudaError_t launch_matvec_tokens(const void* W, const float* X, float* Y, int64_t M, int64_t K, int64_t N,
+                                 void* scratch, size_t scratch_bytes, int* err, int num_sms, cudaStream_t s,
+                                 bool* handled);
+
 // Dense prefill GEMM plan: tiles of 128 weight rows x up to bn = 256 tokens
 // (256 rows for a CTA pair), with the K range optionally split across CTAs
 // (fixed-order reduction after).
@@ -29,6 +39,7 @@ struct GemmPlan {
   int n_tiles, bn, splits;
   bool pair;    // run as CTA pairs (2-SM MMAs) when the device allows it
   int grid;     // CTAs of an unpaired launch
+  int num_sms;
   size_t xhat_bytes, partial_bytes, total_bytes;
 };
 GemmPlan plan_gemm(int wtype, int64_t M, int64_t K, int64_t N, int num_sms);

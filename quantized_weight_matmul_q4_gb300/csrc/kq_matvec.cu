@@ -317,10 +317,13 @@ constexpr int LR_NW_RING = 14;
 constexpr int LR_RING_SMEM = 113 * 1024;     // two CTAs per SM (228 KB, 1 KB reserved per CTA)
 constexpr int LR_MAX_ROWS = 128;             // rows per CTA: at most four row groups
 constexpr int LR_XT = 2;                     // 8-value activation tasks loaded per thread per round
+constexpr int LR_NT = 4;                     // tokens per pass of the several-token kernel (else 2 when
+                                             // four tokens' activations do not fit beside the weights)
 
 struct MatvecLaneRowParams {
-  const float* x;
-  float* y;
+  const float* x;   // [n_tok][K]
+  float* y;         // [n_tok][M]
+  int n_tok;        // tokens (1 for the decode matvec)
   int M, K, nb;
   int R;            // rows per CTA
   int n_groups;     // ceil(R / 32)
@@ -330,6 +333,9 @@ struct MatvecLaneRowParams {
   int S;            // chunk slots (== n_chunks: everything staged at once; fewer: a ring)
   uint32_t inv_per_chunk, inv_cb;  // ceil(2^32 / d) for d = n_groups * cb and d = cb
   int xq_off, xs_off, part_off, bar_off;  // shared-memory layout (bytes)
+  int xq_tok, xs_tok;                     // bytes of one token's codes and of its {d8, s} pairs
+  const uint8_t* xq_g;                    // several tokens: codes [n_tok][xq_tok], quantised beforehand
+  const uint8_t* xs_g;                    // several tokens: {d8, s} pairs [n_tok][xs_tok]
   int* err;
 };
 
@@ -526,13 +532,164 @@ __global__ void __launch_bounds__((NW + 1) * 32, RING ? 2 : 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// The lane-row kernel for a few tokens (the small-N decode: 2 .. LR_TOKENS_MAX
+// tokens, e.g. several sequences or speculative tokens at once). Same staging
+// and arithmetic as the kernel above (staged form only); y is [n_tok][M]. The
+// tokens' Q8_1 codes and {d8, s} pairs are made once per call by
+// quantize_split_kernel (below) in exactly the shared-memory layout, and a pass
+// pulls up to NT tokens of them with two bulk copies. Warp w serves token
+// w % tn of the pass and takes every (24 / tn)-th work item of the CTA, so each
+// token's items are spread over several warps and a warp keeps one set of
+// row-group sums, as in the one-token kernel. The weights are read from HBM once
+// whatever the number of tokens; later passes reuse them.
+// ---------------------------------------------------------------------------
+template <int NT>
+__global__ void __launch_bounds__((LR_NW_FULL + 1) * 32, 1)
+    matvec_q4k_lanerow_tokens_kernel(const __grid_constant__ CUtensorMap tmW, const MatvecLaneRowParams p) {
+  constexpr int NW = LR_NW_FULL;  // divisible by 1, 2, 3 and 4
+  static_assert(NT >= 1 && NT <= 4 && NW % 12 == 0, "token split of the warps");
+  constexpr int LR_CT = NW * 32;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  int8_t* xq = reinterpret_cast<int8_t*>(smem + p.xq_off);           // [NT][xq_tok]
+  uint8_t* xsb = smem + p.xs_off;                                     // [NT][xs_tok]: per 32-block {d8, d8 * Sum q}
+  float* part = reinterpret_cast<float*>(smem + p.part_off);         // [warp][row group][lane]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);    // one per chunk
+  uint64_t* x_full = full + p.S;                                     // the activations of a pass
+  volatile int* abort = reinterpret_cast<volatile int*>(x_full + 1);
+
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r0 = blockIdx.x * p.R;
+  const int rows = min(p.R, p.M - r0);
+  const int per_chunk = p.n_groups * p.cb;  // work items per chunk
+  if (threadIdx.x == 0) {
+    for (int c = 0; c < p.n_chunks; ++c) mbar_init(&full[c], 1);
+    mbar_init(x_full, 1);
+    *abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == NW) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmW);
+      const uint32_t box = static_cast<uint32_t>(p.R * p.cb * Q4K_BYTES);
+      for (int c = 0; c < p.n_chunks; ++c) {
+        mbar_expect_tx(&full[c], box);
+        tma_load_2d(smem + static_cast<size_t>(c) * p.chunk_bytes, &tmW, &full[c], c * p.cb * (Q4K_BYTES / 4), r0);
+      }
+      // Every copy lands before the CTA may exit (also when the consumers gave up).
+      for (int c = 0; c < p.n_chunks; ++c)
+        if (!mbar_wait_bounded(&full[c], 0)) report_error(p.err, ERR_WAIT_TIMEOUT);
+    }
+    return;
+  }
+
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // x may come from the previous kernel
+
+  const int pitch = p.cb * Q4K_BYTES;
+  const int items = p.n_chunks * per_chunk;
+  for (int t0 = 0, pass = 0; t0 < p.n_tok; t0 += NT, ++pass) {
+    const int tn = min(NT, p.n_tok - t0);  // tokens of this pass
+    if (t0 > 0) asm volatile("bar.sync 1, %0;" ::"r"(LR_CT) : "memory");  // the last pass's reads are done
+    if (threadIdx.x == 0) {
+      fence_proxy_async_smem();  // those reads come before the copies' writes
+      mbar_expect_tx(x_full, static_cast<uint32_t>(tn * (p.xq_tok + p.xs_tok)));
+      bulk_g2s(xq, p.xq_g + static_cast<size_t>(t0) * p.xq_tok, static_cast<uint32_t>(tn * p.xq_tok), x_full);
+      bulk_g2s(xsb, p.xs_g + static_cast<size_t>(t0) * p.xs_tok, static_cast<uint32_t>(tn * p.xs_tok), x_full);
+    }
+    if (!mbar_wait(x_full, pass & 1, abort, p.err)) break;
+
+    const int wpt = NW / tn;          // warps per token
+    const int tt = warp % tn, wi = warp / tn;
+    const int8_t* xqt = xq + tt * p.xq_tok;
+    const float4* xs4 = reinterpret_cast<const float4*>(xsb + tt * p.xs_tok);
+    int ready = -1;                       // last chunk this warp has seen land (later passes: at once)
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};  // this warp's sums for row groups 0..3
+    for (int i = wi; i < items; i += wpt) {
+      const int c = static_cast<int>(__umulhi(static_cast<uint32_t>(i), p.inv_per_chunk));
+      const int rem = i - c * per_chunk;
+      const int g = static_cast<int>(__umulhi(static_cast<uint32_t>(rem), p.inv_cb));
+      const int j = rem - g * p.cb;
+      const int b = c * p.cb + j;
+      if (b >= p.nb) continue;  // zero-filled tail of the last chunk
+      if (c != ready) {
+        if (!mbar_wait(&full[c], 0, abort, p.err)) break;
+        ready = c;
+      }
+      const int srow = min(32 * g + lane, p.R - 1);  // lanes past the last row repeat it; dropped
+      const uint8_t* blk = smem + static_cast<size_t>(c) * p.chunk_bytes + srow * pitch + j * Q4K_BYTES;
+      const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
+      const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x & 0xFFFFu)));
+      const float dmin = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x >> 16)));
+      const uint32_t sc_lo = hdr.y & 0x3F3F3F3Fu, m_lo = hdr.z & 0x3F3F3F3Fu;
+      const uint32_t sc_hi = (hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u);
+      const uint32_t m_hi = ((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u);
+      const int8_t* xb = xqt + (b << 8);
+      float lo = 0.f, mn = 0.f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 qa = *reinterpret_cast<const uint4*>(blk + 16 + 32 * q);
+        const uint4 qb = *reinterpret_cast<const uint4*>(blk + 32 + 32 * q);
+        const int4 x0 = *reinterpret_cast<const int4*>(xb + 64 * q);
+        const int4 x1 = *reinterpret_cast<const int4*>(xb + 64 * q + 16);
+        const int4 x2 = *reinterpret_cast<const int4*>(xb + 64 * q + 32);
+        const int4 x3 = *reinterpret_cast<const int4*>(xb + 64 * q + 48);
+        const float4 ds = xs4[(b << 2) + q];  // {d8, s} of sub-blocks 2q and 2q+1
+        int a0 = __dp4a(static_cast<int>(qa.x & 0x0F0F0F0Fu), x0.x, 0);
+        int a1 = __dp4a(static_cast<int>(qb.x & 0x0F0F0F0Fu), x1.x, 0);
+        int h0 = dp4a_us(qa.x & 0xF0F0F0F0u, x2.x, 0);
+        int h1 = dp4a_us(qb.x & 0xF0F0F0F0u, x3.x, 0);
+        a0 = __dp4a(static_cast<int>(qa.y & 0x0F0F0F0Fu), x0.y, a0);
+        a1 = __dp4a(static_cast<int>(qb.y & 0x0F0F0F0Fu), x1.y, a1);
+        h0 = dp4a_us(qa.y & 0xF0F0F0F0u, x2.y, h0);
+        h1 = dp4a_us(qb.y & 0xF0F0F0F0u, x3.y, h1);
+        a0 = __dp4a(static_cast<int>(qa.z & 0x0F0F0F0Fu), x0.z, a0);
+        a1 = __dp4a(static_cast<int>(qb.z & 0x0F0F0F0Fu), x1.z, a1);
+        h0 = dp4a_us(qa.z & 0xF0F0F0F0u, x2.z, h0);
+        h1 = dp4a_us(qb.z & 0xF0F0F0F0u, x3.z, h1);
+        a0 = __dp4a(static_cast<int>(qa.w & 0x0F0F0F0Fu), x0.w, a0);
+        a1 = __dp4a(static_cast<int>(qb.w & 0x0F0F0F0Fu), x1.w, a1);
+        h0 = dp4a_us(qa.w & 0xF0F0F0F0u, x2.w, h0);
+        h1 = dp4a_us(qb.w & 0xF0F0F0F0u, x3.w, h1);
+        const uint32_t scw = (q < 2) ? sc_lo : sc_hi;
+        const uint32_t mw = (q < 2) ? m_lo : m_hi;
+        const int sh = (q & 1) * 16;
+        const int scA = (scw >> sh) & 0xFF, scB = (scw >> (sh + 8)) & 0xFF;
+        const int mA = (mw >> sh) & 0xFF, mB = (mw >> (sh + 8)) & 0xFF;
+        lo = fmaf(ds.x, i2f(scA * (a0 + a1)), lo);
+        lo = fmaf(ds.z, i2f(scB * ((h0 + h1) >> 4)), lo);
+        mn = fmaf(ds.y, i2f(mA), mn);
+        mn = fmaf(ds.w, i2f(mB), mn);
+      }
+      const float v = fmaf(-dmin, mn, d * lo);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc[k] += (g == k) ? v : 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      if (k < p.n_groups) part[(warp * p.n_groups + k) * 32 + lane] = acc[k];
+    asm volatile("bar.sync 1, %0;" ::"r"(LR_CT) : "memory");
+    // y[token][row] = Sum over the token's warps, in warp order
+    for (int u = threadIdx.x; u < tn * rows; u += LR_CT) {
+      const int t = u / rows, r = u - t * rows;
+      const float* pr = part + (r >> 5) * 32 + (r & 31);
+      float a = pr[t * p.n_groups * 32];
+      for (int w = t + tn; w < NW; w += tn) a += pr[w * p.n_groups * 32];
+      p.y[static_cast<int64_t>(t0 + t) * p.M + r0 + r] = a;
+    }
+  }
+}
+
 static inline int round_up(int v, int a) { return (v + a - 1) / a * a; }
 
-// Launch plan of the lane-row kernel with nw consumer warps in at most `budget`
-// bytes of shared memory; `ring` allows fewer chunk slots than chunks (at least
-// two). False when the rows do not fit (then the item kernel above runs).
-static bool plan_lanerow(int64_t M, int64_t K, int num_sms, int nw, int budget, bool ring, MatvecLaneRowParams* p,
-                         int* grid, size_t* smem) {
+// Launch plan of the lane-row kernel with nw consumer warps and room for the
+// activations of nt tokens in at most `budget` bytes of shared memory; `ring`
+// allows fewer chunk slots than chunks (at least two). False when the rows do
+// not fit (then the item kernel above runs).
+static bool plan_lanerow(int64_t M, int64_t K, int num_sms, int nw, int nt, int budget, bool ring,
+                         MatvecLaneRowParams* p, int* grid, size_t* smem) {
   if (K > (int64_t(1) << 20)) return false;
   p->M = static_cast<int>(M);
   p->K = static_cast<int>(K);
@@ -544,10 +701,12 @@ static bool plan_lanerow(int64_t M, int64_t K, int num_sms, int nw, int budget, 
   *grid = static_cast<int>((M + R - 1) / R);
   p->n_groups = (p->R + 31) / 32;
   const int part_bytes = nw * p->n_groups * 32 * 4;
-  const int fixed = round_up(p->K, 128)                 // activation codes
-                    + round_up((p->K / 32) * 8, 128)    // {d8, d8 * Sum q} per 32-block
-                    + part_bytes;                       // per-warp partials
-  for (int cb = 7; cb >= 1; cb -= 2) {  // widest odd chunk that fits
+  p->xq_tok = round_up(p->K, 128);                      // activation codes of a token
+  p->xs_tok = round_up((p->K / 32) * 8, 128);           // {d8, d8 * Sum q} per 32-block
+  const int fixed = nt * (p->xq_tok + p->xs_tok) + part_bytes;  // + per-warp partials
+  // Widest odd chunk that fits. cb >= 3 keeps both divisors of the item index
+  // (cb and n_groups * cb) at least 3, so their reciprocals fit in 32 bits.
+  for (int cb = 7; cb >= 3; cb -= 2) {
     const int n_chunks = (p->nb + cb - 1) / cb;
     const int chunk_bytes = round_up(p->R * cb * Q4K_BYTES, 128);
     int S = n_chunks;
@@ -564,9 +723,9 @@ static bool plan_lanerow(int64_t M, int64_t K, int num_sms, int nw, int budget, 
     p->inv_cb = static_cast<uint32_t>(((uint64_t(1) << 32) + cb - 1) / cb);
     size_t off = static_cast<size_t>(S) * chunk_bytes;
     p->xq_off = static_cast<int>(off);
-    off += round_up(p->K, 128);
+    off += static_cast<size_t>(nt) * p->xq_tok;
     p->xs_off = static_cast<int>(off);
-    off += round_up((p->K / 32) * 8, 128);
+    off += static_cast<size_t>(nt) * p->xs_tok;
     p->part_off = static_cast<int>(off);
     off += part_bytes;
     p->bar_off = static_cast<int>(off);
@@ -586,8 +745,8 @@ cudaError_t launch_matvec(int wtype, const void* W, const float* x, float* y, in
     MatvecLaneRowParams lp{};
     size_t smem = 0;
     int grid = 0;
-    const bool full = plan_lanerow(M, K, num_sms, LR_NW_FULL, MV_SMEM_LIMIT, false, &lp, &grid, &smem);
-    const bool ring = !full && plan_lanerow(M, K, num_sms, LR_NW_RING, LR_RING_SMEM, true, &lp, &grid, &smem);
+    const bool full = plan_lanerow(M, K, num_sms, LR_NW_FULL, 1, MV_SMEM_LIMIT, false, &lp, &grid, &smem);
+    const bool ring = !full && plan_lanerow(M, K, num_sms, LR_NW_RING, 1, LR_RING_SMEM, true, &lp, &grid, &smem);
     if (full || ring) {
       CUtensorMap tmW;
       const uint64_t rs = static_cast<uint64_t>(lp.nb) * Q4K_BYTES;
@@ -599,6 +758,7 @@ cudaError_t launch_matvec(int wtype, const void* W, const float* x, float* y, in
       }
       lp.x = x;
       lp.y = y;
+      lp.n_tok = 1;
       lp.err = err;
       if (ring) {
         cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(matvec_q4k_lanerow_kernel<LR_NW_RING, true>), 10);
@@ -660,6 +820,83 @@ cudaError_t launch_matvec(int wtype, const void* W, const float* x, float* y, in
     e = launch_pdl(matvec_kernel<KQ_Q6_K>, dim3(G), dim3(MV_THREADS), smem, s, p);
   }
   return e;
+}
+
+// Q8_1 of n_tok tokens in the layout the several-token kernel copies into
+// shared memory: codes [n_tok][xq_tok] (x's order) and per 32-block
+// {d8, d8 * Sum q} [n_tok][xs_tok]; the arithmetic of the one-token kernel's own
+// quantiser (quantize_oct), so the codes are the same. Task t quantises eight
+// values of token t / (K / 8); a warp's 32 tasks share one token.
+__global__ void __launch_bounds__(256) quantize_split_kernel(const float* __restrict__ X, int n_tok, int K, int xq_tok,
+                                                             int xs_tok, uint8_t* __restrict__ xq_g,
+                                                             uint8_t* __restrict__ xs_g) {
+  pdl_enter();
+  const int nt = K >> 3;
+  const int64_t total = static_cast<int64_t>(n_tok) * nt;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x; t < total;
+       t += static_cast<int64_t>(gridDim.x) * 256) {
+    const int tok = static_cast<int>(t / nt), tl = static_cast<int>(t - static_cast<int64_t>(tok) * nt);
+    const float4* src = reinterpret_cast<const float4*>(X + static_cast<int64_t>(tok) * K) + 2 * tl;
+    const float4 a = __ldg(src), c = __ldg(src + 1);
+    const float v[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+    const Q8Oct r = quantize_oct(v);
+    *reinterpret_cast<uint2*>(xq_g + static_cast<int64_t>(tok) * xq_tok + 8 * tl) = make_uint2(r.q[0], r.q[1]);
+    if ((threadIdx.x & 3) == 0)
+      reinterpret_cast<float2*>(xs_g + static_cast<int64_t>(tok) * xs_tok)[tl >> 2] =
+          make_float2(r.dh, __fmul_rn(r.dh, static_cast<float>(r.sumq)));  // exact
+  }
+}
+
+// Q4_K for N = 2 .. LR_TOKENS_MAX tokens: the staged lane-row kernel with
+// LR_NT (else two) tokens per pass. *handled = false (nothing queued) when the
+// rows do not fit staged next to the activations of two tokens.
+cudaError_t launch_matvec_tokens(const void* W, const float* X, float* Y, int64_t M, int64_t K, int64_t N,
+                                 void* scratch, size_t scratch_bytes, int* err, int num_sms, cudaStream_t s,
+                                 bool* handled) {
+  *handled = false;
+  if (N < 2 || N > LR_TOKENS_MAX) return cudaSuccess;
+  MatvecLaneRowParams lp{};
+  size_t smem = 0;
+  int grid = 0;
+  int nt = LR_NT;
+  if (!plan_lanerow(M, K, num_sms, LR_NW_FULL, nt, MV_SMEM_LIMIT, false, &lp, &grid, &smem)) {
+    nt = 2;
+    if (!plan_lanerow(M, K, num_sms, LR_NW_FULL, nt, MV_SMEM_LIMIT, false, &lp, &grid, &smem)) return cudaSuccess;
+  }
+  CUtensorMap tmW;
+  const uint64_t rs = static_cast<uint64_t>(lp.nb) * Q4K_BYTES;
+  if (!encode_tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT32, W, rs / 4, static_cast<uint64_t>(M), rs,
+                      static_cast<uint32_t>(lp.cb * Q4K_BYTES / 4), static_cast<uint32_t>(lp.R),
+                      CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaSuccess;
+  const size_t xq_bytes = static_cast<size_t>(N) * lp.xq_tok, xs_bytes = static_cast<size_t>(N) * lp.xs_tok;
+  if (xq_bytes + xs_bytes > scratch_bytes) return cudaSuccess;
+  uint8_t* xq_g = static_cast<uint8_t*>(scratch);
+  uint8_t* xs_g = xq_g + xq_bytes;  // xq_tok is a multiple of 128: 16-byte aligned
+  lp.x = X;
+  lp.y = Y;
+  lp.n_tok = static_cast<int>(N);
+  lp.xq_g = xq_g;
+  lp.xs_g = xs_g;
+  lp.err = err;
+  smem += 16;  // the activations' barrier
+  *handled = true;
+  {
+    const int64_t tasks = N * (K / 8);
+    const int64_t blocks = std::min<int64_t>((tasks + 255) / 256, static_cast<int64_t>(num_sms) * 4);
+    cudaError_t e = launch_pdl(quantize_split_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, X,
+                               static_cast<int>(N), static_cast<int>(K), lp.xq_tok, lp.xs_tok, xq_g, xs_g);
+    if (e != cudaSuccess) return e;
+  }
+  if (nt == LR_NT) {
+    cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(matvec_q4k_lanerow_tokens_kernel<LR_NT>), 11);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(matvec_q4k_lanerow_tokens_kernel<LR_NT>, dim3(grid), dim3((LR_NW_FULL + 1) * 32), smem, s,
+                      tmW, lp);
+  }
+  cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(matvec_q4k_lanerow_tokens_kernel<2>), 14);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(matvec_q4k_lanerow_tokens_kernel<2>, dim3(grid), dim3((LR_NW_FULL + 1) * 32), smem, s, tmW, lp);
 }
 
 }  // namespace kq

@@ -105,6 +105,7 @@ WORKLOADS = {
     "matvec_q4k_512x2048": dict(kind="matvec", wtype="q4_k", M=512, K=2048, N=1, seed=0),
     "decode_q4k_4096x11008": dict(kind="matvec", wtype="q4_k", M=4096, K=11008, N=1, seed=1),
     "decode_q4k_11008x4096": dict(kind="matvec", wtype="q4_k", M=11008, K=4096, N=1, seed=1),
+    "smalln_q4k_4096x11008_n4": dict(kind="gemm", wtype="q4_k", M=4096, K=11008, N=4, seed=5),
     "prefill_q4k_4096x4096_n64": dict(kind="gemm", wtype="q4_k", M=4096, K=4096, N=64, seed=2),
     "prefill_q4k_4096x4096_n512": dict(kind="gemm", wtype="q4_k", M=4096, K=4096, N=512, seed=2),
     "prefill_q4k_14336x4096_n2048": dict(kind="gemm", wtype="q4_k", M=14336, K=4096, N=2048, seed=3),
