@@ -28,7 +28,8 @@ Sources (page title, section):
         What they do right (Q8_1 activations, 1 byte per element), MoE routing
         (fused gather), Correctness gate (CPU dequant + matmul reference).
 [GAP]   "Prefill Gap Closure Plan — ZINC CUDA vs llama.cpp": T2 (gather by
-        expert: histogram, prefix sum, scatter of token-slot ids).
+        expert: histogram, prefix sum, scatter of token-slot ids; "scatter
+        back" to the tokens).
 
 Where the pages leave a step open, the reading taken is stated at the function.
 The two bit layouts the pages elide (the Q4_K 6-bit scale/min packing and the
@@ -337,6 +338,47 @@ def moe(wtype: str, W_experts: np.ndarray, expert_ids: np.ndarray, X: np.ndarray
         Y[t_idx, j_idx] = xh[t_idx] @ w.T
         B[t_idx, j_idx] = np.abs(xh[t_idx]) @ np.abs(w).T
     return Y, B
+
+
+# ----------------------------------------------------------------------------
+# The steps next to the matmul: the producer of the activations before it and
+# the MoE combine after it
+# ----------------------------------------------------------------------------
+def rms_norm(X: np.ndarray, gamma: np.ndarray, eps: float) -> np.ndarray:
+    """RMSNorm of every token row, the producer whose output the activation
+    quantiser takes when it is fused into it ([MMVQ] §3.2 Key code: the Q8_1
+    quantisation body moved into the RMSNorm and SwiGLU producers). The pages
+    name the producer without its formula; the reading taken is the usual one,
+    x / sqrt(mean(x^2) + eps) * gamma, in fp64.
+
+    ``X``: [N, K]; ``gamma``: [K]. Returns fp64 [N, K]."""
+    X = np.asarray(X, dtype=np.float64)
+    ms = np.mean(X * X, axis=1, keepdims=True)
+    return X / np.sqrt(ms + eps) * np.asarray(gamma, dtype=np.float64)[None, :]
+
+
+def swiglu(G: np.ndarray, U: np.ndarray) -> np.ndarray:
+    """SwiGLU, the other producer named in [MMVQ] §3.2 Key code; reading taken:
+    silu(g) * u with silu(g) = g / (1 + exp(-g)), element-wise in fp64."""
+    G = np.asarray(G, dtype=np.float64)
+    return G / (1.0 + np.exp(-G)) * np.asarray(U, dtype=np.float64)
+
+
+def matmul_from(wtype: str, W: np.ndarray, Xp: np.ndarray, M: int, K: int):
+    """``matmul`` for activations made by a producer (``rms_norm``, ``swiglu``):
+    they are rounded to fp32 (the precision the quantiser receives them in),
+    then quantised to Q8_1 and multiplied as in ``matmul``."""
+    return matmul(wtype, W, np.asarray(Xp, dtype=np.float32), M, K)
+
+
+def moe_combine(Y: np.ndarray, probs: np.ndarray) -> np.ndarray:
+    """The step after the expert matmul: the slots' rows go back to their token
+    ([GAP] T2, "scatter back"), read as the usual MoE combine weighted by the
+    router probabilities: out[t, :] = Sum_j probs[t, j] * Y[t, j, :], in fp64.
+    The probabilities are inputs (no normalisation here).
+
+    ``Y``: [T, top_k, M]; ``probs``: [T, top_k]. Returns fp64 [T, M]."""
+    return np.einsum("tj,tjm->tm", np.asarray(probs, dtype=np.float64), np.asarray(Y, dtype=np.float64))
 
 
 def tolerance(B: np.ndarray) -> np.ndarray:

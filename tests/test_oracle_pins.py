@@ -354,3 +354,74 @@ def test_moe_equals_dense_per_slot():
             e = ids[t, j]
             Yd, Bd = ora.matmul("q4_k", W[e * M:(e + 1) * M], X[t:t + 1], M, K)
             assert np.array_equal(Y[t, j], Yd[0]) and np.array_equal(B[t, j], Bd[0])
+
+
+# ----------------------------------------------------------------------------
+# Producers (RMSNorm, SwiGLU) and the MoE combine
+# ----------------------------------------------------------------------------
+def test_rms_norm_constant_row_and_unit_mean_square():
+    K = 64
+    gamma = np.linspace(0.5, 2.0, K)
+    # a constant row c: mean square c^2, so the result is c / sqrt(c^2 + eps) * gamma
+    y = ora.rms_norm(np.full((1, K), -3.0), gamma, 0.0)
+    assert np.allclose(y[0], -gamma, rtol=0, atol=1e-15)
+    y = ora.rms_norm(np.full((1, K), 2.0), gamma, 5.0)
+    assert np.allclose(y[0], 2.0 / 3.0 * gamma, rtol=0, atol=1e-15)
+    # with gamma = 1 and eps = 0 every row has mean square exactly 1 (up to rounding)
+    rng = np.random.default_rng(71)
+    X = rng.standard_normal((5, 257)) * rng.uniform(0.1, 10.0, size=(5, 1))
+    y = ora.rms_norm(X, np.ones(257), 0.0)
+    assert np.allclose(np.mean(y * y, axis=1), 1.0, rtol=1e-13)
+
+
+def test_rms_norm_is_scale_invariant_and_row_wise():
+    rng = np.random.default_rng(72)
+    X = rng.standard_normal((3, 96))
+    g = rng.standard_normal(96)
+    a = ora.rms_norm(X, g, 0.0)
+    assert np.allclose(ora.rms_norm(7.5 * X, g, 0.0), a, rtol=1e-13)
+    assert np.allclose(ora.rms_norm(X[1:2], g, 0.0), a[1:2], rtol=0, atol=0)
+
+
+def test_swiglu_special_values_and_odd_part():
+    g = np.array([0.0, 40.0, -40.0, 1.0])
+    u = np.array([3.0, 2.0, 5.0, 1.0])
+    y = ora.swiglu(g, u)
+    assert y[0] == 0.0
+    assert abs(y[1] - 80.0) < 1e-12 and abs(y[2]) < 1e-15
+    assert abs(y[3] - 1.0 / (1.0 + math.exp(-1.0))) < 1e-15
+    # silu(g) - silu(-g) = g for every g (sigma(g) + sigma(-g) = 1)
+    rng = np.random.default_rng(73)
+    g = rng.standard_normal(1000) * 5
+    ones = np.ones_like(g)
+    assert np.allclose(ora.swiglu(g, ones) - ora.swiglu(-g, ones), g, rtol=1e-12, atol=1e-12)
+
+
+def test_moe_combine_one_hot_mean_and_linearity():
+    rng = np.random.default_rng(74)
+    T, top_k, M = 6, 4, 9
+    Y = rng.standard_normal((T, top_k, M))
+    pick = rng.integers(0, top_k, size=T)
+    onehot = np.eye(top_k)[pick]
+    assert np.array_equal(ora.moe_combine(Y, onehot), Y[np.arange(T), pick])
+    assert np.allclose(ora.moe_combine(Y, np.full((T, top_k), 1.0 / top_k)), Y.mean(axis=1), rtol=1e-14)
+    p1, p2 = rng.uniform(size=(T, top_k)), rng.uniform(size=(T, top_k))
+    assert np.allclose(ora.moe_combine(Y, p1 + p2), ora.moe_combine(Y, p1) + ora.moe_combine(Y, p2), rtol=1e-13)
+
+
+def test_moe_combine_equals_matmul_with_the_weighted_weights():
+    # Sum_j p_j (W_{e_j} . x_hat) = (Sum_j p_j W_{e_j}) . x_hat
+    E, M, K, T, top_k = 4, 3, 256, 5, 2
+    W = _q4k_random(75, E * M, K)
+    X = _rand_x(76, T, K)
+    rng = np.random.default_rng(77)
+    ids = np.stack([rng.permutation(E)[:top_k] for _ in range(T)]).astype(np.int32)
+    probs = rng.uniform(size=(T, top_k))
+    Y, _ = ora.moe("q4_k", W, ids, X, E, M, K)
+    out = ora.moe_combine(Y, probs)
+    w = ora.dequant("q4_k", W, K).reshape(E, M, K)
+    q, d_h, _ = ora.quantize_q8_1(X)
+    xh = ora.q8_1_dequant(q, d_h)
+    for t in range(T):
+        weff = sum(probs[t, j] * w[ids[t, j]] for j in range(top_k))
+        assert np.allclose(out[t], weff @ xh[t], rtol=1e-12, atol=1e-12)
