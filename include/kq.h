@@ -111,6 +111,25 @@ KQ_API kq_status kq_matvec(int wtype, const void* W, const float* x, float* y, i
                            kq_stream_t stream);
 
 /*
+ * kq_matvec_swiglu, kq_matvec_rmsnorm — kq_matvec with the producer of its
+ * activations fused into the Q8_1 quantiser ([MMVQ] §3.2 Key code: the
+ * quantisation body moved into the RMSNorm and SwiGLU producers), so the
+ * produced activations never go to memory:
+ *   swiglu:  x[k] = silu(gate[k]) * up[k],  silu(g) = g / (1 + exp(-g));
+ *   rmsnorm: x[k] = x_in[k] * r * gamma[k], r = 1 / sqrt(Sum_k x_in[k]^2 / K + eps)
+ *            (eps >= 0; the sum of squares is taken in a fixed order).
+ * gate, up, x_in, gamma: fp32 [K], 16-byte aligned. The producers compute in
+ * fp32; the Q8_1 codes are then made from those fp32 values exactly as in
+ * kq_matvec, and Y meets the accuracy bound against the exact product of the
+ * dequantised weights with the Q8_1 codes of the produced activations.
+ * Otherwise as kq_matvec (wtype, layouts, W streamed before the dependency wait).
+ */
+KQ_API kq_status kq_matvec_swiglu(int wtype, const void* W, const float* gate, const float* up, float* y, int64_t M,
+                                  int64_t K, kq_stream_t stream);
+KQ_API kq_status kq_matvec_rmsnorm(int wtype, const void* W, const float* x, const float* gamma, float eps, float* y,
+                                   int64_t M, int64_t K, kq_stream_t stream);
+
+/*
  * kq_gemm — prefill GEMM Y = dequant(W) . X for N tokens ([MMQv2] Kernel
  * architecture; [GAP] T1). X is quantised to Q8_1 (as x_hat = fp16(d_h * q))
  * into the workspace once per call; weight super-blocks are staged by TMA and
@@ -179,6 +198,19 @@ KQ_API kq_status kq_gemm_noalloc(int wtype, const void* W, const float* X, float
 KQ_API kq_status kq_moe_grouped_gemm(int wtype, const void* W_experts, int32_t n_experts, const int32_t* expert_ids,
                               int32_t top_k, const float* X, float* Y, int64_t M, int64_t K, int64_t T, void* ws,
                               size_t ws_bytes, kq_stream_t stream);
+
+/*
+ * kq_moe_combine — the step after kq_moe_grouped_gemm: each token's slot rows
+ * go back to the token, weighted by the router probabilities ([GAP] T2,
+ * "scatter back"; read as the usual weighted MoE combine):
+ *   out[t][m] = Sum_{j < top_k} probs[t][j] * Y[t][j][m],
+ * summed in fp32 in slot order with one fused multiply-add per slot
+ * (deterministic). Y: fp32 [T][top_k][M] (as kq_moe_grouped_gemm writes it);
+ * probs: fp32 [T][top_k]; out: fp32 [T][M], written. 1 <= top_k <= 512.
+ * Needs no workspace; out must not overlap Y or probs.
+ */
+KQ_API kq_status kq_moe_combine(const float* Y, const float* probs, float* out, int64_t M, int64_t T, int32_t top_k,
+                                kq_stream_t stream);
 
 /*
  * kq_workspace_bytes — device workspace needed by an operation (0 for

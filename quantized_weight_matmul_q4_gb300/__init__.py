@@ -16,8 +16,9 @@ from ._native import (KQ_DEVERR_EXPERT_ID, KQ_DEVERR_NONE, KQ_DEVERR_WAIT_TIMEOU
 __all__ = [
     "KQ_Q4_K", "KQ_Q6_K", "KQ_OP_MATVEC", "KQ_OP_GEMM", "KQ_OP_MOE", "KQError",
     "KQ_DEVERR_NONE", "KQ_DEVERR_WAIT_TIMEOUT", "KQ_DEVERR_EXPERT_ID",
-    "KQ_GEMM_STATIC_WS_BYTES", "kq_quantize_q8_1", "kq_matvec", "kq_gemm", "kq_gemm_noalloc",
-    "kq_moe_grouped_gemm", "kq_workspace_bytes", "kq_get_device_error", "block_bytes", "row_bytes",
+    "KQ_GEMM_STATIC_WS_BYTES", "kq_quantize_q8_1", "kq_matvec", "kq_matvec_swiglu", "kq_matvec_rmsnorm",
+    "kq_gemm", "kq_gemm_noalloc", "kq_moe_grouped_gemm", "kq_moe_combine", "kq_workspace_bytes",
+    "kq_get_device_error", "block_bytes", "row_bytes",
 ]
 
 _BLOCK_BYTES = {KQ_Q4_K: 144, KQ_Q6_K: 210}
@@ -79,6 +80,39 @@ def kq_matvec(wtype, W, x, M: int, K: int, y=None, stream=None):
     check(lib().kq_matvec(_wt(wtype), _dev(W, "W", torch.uint8), _dev(x, "x", torch.float32),
                           _dev(y, "y", torch.float32), M, K, _stream(stream)), "kq_matvec")
     return y
+
+
+def kq_matvec_swiglu(wtype, W, gate, up, M: int, K: int, y=None, stream=None):
+    """y[M] = dequant(W) . Q8_1(silu(gate) * up); gate, up fp32 [K]."""
+    torch = _torch()
+    if y is None:
+        y = torch.empty(M, dtype=torch.float32, device=gate.device)
+    check(lib().kq_matvec_swiglu(_wt(wtype), _dev(W, "W", torch.uint8), _dev(gate, "gate", torch.float32),
+                                 _dev(up, "up", torch.float32), _dev(y, "y", torch.float32), M, K,
+                                 _stream(stream)), "kq_matvec_swiglu")
+    return y
+
+
+def kq_matvec_rmsnorm(wtype, W, x, gamma, eps: float, M: int, K: int, y=None, stream=None):
+    """y[M] = dequant(W) . Q8_1(x / sqrt(mean(x^2) + eps) * gamma); x, gamma fp32 [K]."""
+    torch = _torch()
+    if y is None:
+        y = torch.empty(M, dtype=torch.float32, device=x.device)
+    check(lib().kq_matvec_rmsnorm(_wt(wtype), _dev(W, "W", torch.uint8), _dev(x, "x", torch.float32),
+                                  _dev(gamma, "gamma", torch.float32), float(eps), _dev(y, "y", torch.float32),
+                                  M, K, _stream(stream)), "kq_matvec_rmsnorm")
+    return y
+
+
+def kq_moe_combine(Y, probs, out=None, stream=None):
+    """out[T, M] = Sum_j probs[:, j] * Y[:, j, :] for Y fp32 [T, top_k, M], probs fp32 [T, top_k]."""
+    torch = _torch()
+    T, top_k, M = Y.shape
+    if out is None:
+        out = torch.empty((T, M), dtype=torch.float32, device=Y.device)
+    check(lib().kq_moe_combine(_dev(Y, "Y", torch.float32), _dev(probs, "probs", torch.float32),
+                               _dev(out, "out", torch.float32), M, T, top_k, _stream(stream)), "kq_moe_combine")
+    return out
 
 
 def kq_workspace_bytes(op: int, wtype, M: int, K: int, N_or_T: int, n_experts: int = 0, top_k: int = 0) -> int:

@@ -40,6 +40,9 @@ _sz = ctypes.c_size_t
 SIGNATURES = {
     "kq_quantize_q8_1": (ctypes.c_int, [_vp, _vp, _i64, _i64, _vp]),
     "kq_matvec": (ctypes.c_int, [ctypes.c_int, _vp, _vp, _vp, _i64, _i64, _vp]),
+    "kq_matvec_swiglu": (ctypes.c_int, [ctypes.c_int, _vp, _vp, _vp, _vp, _i64, _i64, _vp]),
+    "kq_matvec_rmsnorm": (ctypes.c_int, [ctypes.c_int, _vp, _vp, _vp, ctypes.c_float, _vp, _i64, _i64, _vp]),
+    "kq_moe_combine": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, _i32, _vp]),
     "kq_gemm": (ctypes.c_int, [ctypes.c_int, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _sz, _vp]),
     "kq_gemm_noalloc": (ctypes.c_int, [ctypes.c_int, _vp, _vp, _vp, _i64, _i64, _i64, _vp]),
     "kq_moe_grouped_gemm": (ctypes.c_int, [ctypes.c_int, _vp, _i32, _vp, _i32, _vp, _vp, _i64, _i64, _i64,

@@ -107,18 +107,49 @@ kq_status kq_quantize_q8_1(const float* X, void* Xq, int64_t K, int64_t N, kq_st
   return finish(launch_quantize_q8_1(X, Xq, K, N, reinterpret_cast<cudaStream_t>(stream)), KQ_OK);
 }
 
-kq_status kq_matvec(int wtype, const void* W, const float* x, float* y, int64_t M, int64_t K, kq_stream_t stream) {
+static kq_status matvec_entry(int wtype, const void* W, const float* x, const float* aux, float eps, int prod,
+                              float* y, int64_t M, int64_t K, kq_stream_t stream) {
   if (!valid_wtype(wtype)) return KQ_ERR_TYPE;
-  if (!W || !x || !y) return KQ_ERR_NULL;
+  if (!W || !x || !y || (prod != PROD_X && !aux)) return KQ_ERR_NULL;
   if (M <= 0 || K <= 0 || K % QK_K != 0 || M > kMaxDim || K > kMaxDim) return KQ_ERR_SHAPE;
-  if (!aligned16(W) || !aligned16(x) || !aligned16(y)) return KQ_ERR_ALIGN;
+  if (prod == PROD_RMSNORM && !(eps >= 0.f && eps < 1e30f)) return KQ_ERR_SHAPE;  // also rejects NaN
+  if (!aligned16(W) || !aligned16(x) || !aligned16(y) || (prod != PROD_X && !aligned16(aux))) return KQ_ERR_ALIGN;
   int dev, sms;
   int* err;
   cudaError_t e = device_state(&dev, &sms, &err);
   if (e != cudaSuccess) return KQ_ERR_CUDA;
   int status = KQ_OK;
-  e = launch_matvec(wtype, W, x, y, M, K, err, sms, reinterpret_cast<cudaStream_t>(stream), &status);
+  e = launch_matvec(wtype, W, x, aux, eps, prod, y, M, K, err, sms, reinterpret_cast<cudaStream_t>(stream), &status);
   return finish(e, status);
+}
+
+kq_status kq_matvec(int wtype, const void* W, const float* x, float* y, int64_t M, int64_t K, kq_stream_t stream) {
+  return matvec_entry(wtype, W, x, nullptr, 0.f, PROD_X, y, M, K, stream);
+}
+
+kq_status kq_matvec_swiglu(int wtype, const void* W, const float* gate, const float* up, float* y, int64_t M,
+                           int64_t K, kq_stream_t stream) {
+  return matvec_entry(wtype, W, gate, up, 0.f, PROD_SWIGLU, y, M, K, stream);
+}
+
+kq_status kq_matvec_rmsnorm(int wtype, const void* W, const float* x, const float* gamma, float eps, float* y,
+                            int64_t M, int64_t K, kq_stream_t stream) {
+  return matvec_entry(wtype, W, x, gamma, eps, PROD_RMSNORM, y, M, K, stream);
+}
+
+kq_status kq_moe_combine(const float* Y, const float* probs, float* out, int64_t M, int64_t T, int32_t top_k,
+                         kq_stream_t stream) {
+  if (!Y || !probs || !out) return KQ_ERR_NULL;
+  if (M <= 0 || T <= 0 || top_k <= 0 || top_k > 512 || M > kMaxDim || T * top_k > kMaxDim ||
+      T * top_k * M > (int64_t(1) << 40))
+    return KQ_ERR_SHAPE;
+  if (!aligned16(Y) || !aligned16(probs) || !aligned16(out)) return KQ_ERR_ALIGN;
+  int dev, sms;
+  int* err;
+  cudaError_t e = device_state(&dev, &sms, &err);
+  if (e != cudaSuccess) return KQ_ERR_CUDA;
+  e = launch_moe_combine(Y, probs, out, M, T, top_k, sms, reinterpret_cast<cudaStream_t>(stream));
+  return finish(e, KQ_OK);
 }
 
 size_t kq_workspace_bytes(int op, int wtype, int64_t M, int64_t K, int64_t N_or_T, int32_t n_experts,

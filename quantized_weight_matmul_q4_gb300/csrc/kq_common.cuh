@@ -129,6 +129,28 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
+// Waits until *counter > c, where the counter is a shared-memory word that one
+// thread raises (the number of ring chunks a producer has issued). A consumer
+// that waits for this before waiting on the chunk's slot barrier never takes
+// an older phase of the same parity for its chunk, however far ahead of the
+// other consumers it runs. Bounded like mbar_wait.
+__device__ __forceinline__ bool wait_counter_above(const volatile int* counter, int c, volatile int* abort, int* err) {
+  if (*counter > c) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(64);
+    if (*counter > c) return true;
+    if ((it & 7) == 0) {
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+        report_error(err, ERR_WAIT_TIMEOUT);
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Thread-block clusters (CTA pairs)
 // ---------------------------------------------------------------------------

@@ -12,14 +12,19 @@ namespace kq {
 
 cudaError_t launch_quantize_q8_1(const float* X, void* Xq, int64_t K, int64_t N, cudaStream_t s);
 cudaError_t launch_quantize_xhat(const float* X, __half* Xh, int64_t K, int64_t rows, int num_sms, cudaStream_t s);
-// MoE: for every slot i with bucket row p = slot_pos[i] >= 0, writes the x_hat
-// of token i / top_k to row p of Xh and entries[p] = i.
-// Bucket row slot_pos[i] of Xh <- row i / top_k of Xtok (x_hat per token);
-// entries[slot_pos[i]] = i. Negative positions are skipped.
+// MoE gather: bucket row slot_pos[i] of Xh <- row i / top_k of Xtok (x_hat
+// per token); entries[slot_pos[i]] = i. Negative positions are skipped.
 cudaError_t launch_gather_rows(const __half* Xtok, __half* Xh, int64_t K, int64_t n_slots, int top_k,
                                const int* slot_pos, int* entries, cudaStream_t s);
-cudaError_t launch_matvec(int wtype, const void* W, const float* x, float* y, int64_t M, int64_t K, int* err,
-                          int num_sms, cudaStream_t s, int* status);
+
+// Producer of the decode matvec's activations (fused into its quantiser):
+// x itself; silu(x) * aux (SwiGLU, x the gate, aux the up projection);
+// x / sqrt(mean(x^2) + eps) * aux (RMSNorm, aux = gamma).
+constexpr int PROD_X = 0;
+constexpr int PROD_SWIGLU = 1;
+constexpr int PROD_RMSNORM = 2;
+cudaError_t launch_matvec(int wtype, const void* W, const float* x, const float* aux, float eps, int prod, float* y,
+                          int64_t M, int64_t K, int* err, int num_sms, cudaStream_t s, int* status);
 
 // Several tokens (Q4_K, 2 <= N <= LR_TOKENS_MAX) on the decode matvec path:
 // Y[N][M] = dequant(W) . X[N][K], the tokens' Q8_1 codes made once into
@@ -55,6 +60,10 @@ cudaError_t launch_moe(int wtype, const void* W, int n_experts, const int32_t* i
                        float* Y, int64_t M, int64_t K, int64_t T, void* ws, const MoePlan& plan, int* err,
                        int num_sms, cudaStream_t s, int* status);
 
+// out[t][m] = Sum_j probs[t][j] * Y[t][j][m] (the MoE combine), fp32, slot order.
+cudaError_t launch_moe_combine(const float* Y, const float* probs, float* out, int64_t M, int64_t T, int top_k,
+                               int num_sms, cudaStream_t s);
+
 // Current device, its SM count and the device address of its error word
 // (looked up once per device).
 cudaError_t device_context(int* dev, int* num_sms, int** err);
@@ -62,7 +71,7 @@ cudaError_t device_context(int* dev, int* num_sms, int** err);
 // Raises a kernel's dynamic shared-memory limit to the 227 KB maximum, once per
 // device (later calls only read a flag, so launches stay cheap and capturable).
 cudaError_t allow_max_smem(const void* kernel, int slot);
-constexpr int kSmemSlots = 16;
+constexpr int kSmemSlots = 24;
 
 // Launches `kernel` on `s` with programmatic stream serialization allowed (the
 // kernel calls pdl_enter() before its first global memory access).

@@ -35,7 +35,9 @@ constexpr int MV_MAX_RING = 14;
 
 struct MatvecParams {
   const uint8_t* W;
-  const float* x;
+  const float* x;       // x, or the gate of SwiGLU
+  const float* aux;     // SwiGLU: up; RMSNorm: gamma
+  float eps;            // RMSNorm
   float* y;
   int M, K, nb;
   int bb;               // bytes per block (144 or 210)
@@ -65,6 +67,47 @@ __device__ __forceinline__ int xds_q4k(int b, int c) { return 4 * b + (c ^ ((b >
 __device__ __forceinline__ int xds_q6k(int b, int g8) { return 8 * b + (g8 ^ (b & 7)); }
 
 __device__ __forceinline__ float i2f(int v) { return static_cast<float>(v); }
+
+// The producer of the activations that the quantiser takes, fused into the
+// matvec ("06 · 8e/8e② — decode MMVQ", §3.2 Key code: the Q8_1 quantisation
+// moved into the RMSNorm and SwiGLU producers): PROD_X reads x; PROD_SWIGLU
+// makes silu(g) * u from gate g = x and up u = aux; PROD_RMSNORM makes
+// x * inv_rms * gamma with gamma = aux. All in fp32.
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+
+// Activations k .. k+3 (k a multiple of 4).
+template <int PROD>
+__device__ __forceinline__ float4 produce4(const float* __restrict__ x, const float* __restrict__ aux, int k,
+                                           float inv_rms) {
+  const float4 a = __ldg(reinterpret_cast<const float4*>(x + k));
+  if (PROD == PROD_X) return a;
+  const float4 b = __ldg(reinterpret_cast<const float4*>(aux + k));
+  if (PROD == PROD_SWIGLU)
+    return make_float4(silu_f(a.x) * b.x, silu_f(a.y) * b.y, silu_f(a.z) * b.z, silu_f(a.w) * b.w);
+  return make_float4(a.x * inv_rms * b.x, a.y * inv_rms * b.y, a.z * inv_rms * b.z, a.w * inv_rms * b.w);
+}
+
+// RMSNorm's 1 / sqrt(mean(x^2) + eps) over x[0 .. K), computed by the nthreads
+// consumer threads of the CTA (named barrier 1) in a fixed order: each thread
+// sums its quads, warps reduce by shuffles, then every thread adds the warp sums
+// in warp order. red: nthreads / 32 floats of shared memory.
+__device__ __forceinline__ float rms_inv(const float* __restrict__ x, int K, float eps, float* red, int nthreads) {
+  float ss = 0.f;
+  for (int q = threadIdx.x; q < (K >> 2); q += nthreads) {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(x) + q);
+    ss = fmaf(v.x, v.x, ss);
+    ss = fmaf(v.y, v.y, ss);
+    ss = fmaf(v.z, v.z, ss);
+    ss = fmaf(v.w, v.w, ss);
+  }
+  ss = warp_sum_f(ss);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+  float tot = 0.f;
+  for (int w = 0; w < (nthreads >> 5); ++w) tot += red[w];
+  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");  // red is free again
+  return rsqrtf(tot / static_cast<float>(K) + eps);
+}
 
 // Sum over one Q4_K super-block (256 weights) of w * x_hat, by the min-term
 // identity: d * Sum_sub d8*sc*dot(nib, q) - dmin * Sum_sub d8*m*Sum(q).
@@ -163,7 +206,7 @@ __device__ __forceinline__ float block_dot_q6k(const uint8_t* __restrict__ blk, 
   return d * acc;
 }
 
-template <int WT>
+template <int WT, int PROD>
 __global__ void __launch_bounds__(MV_THREADS, 1) matvec_kernel(const MatvecParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* xq = smem;
@@ -173,6 +216,7 @@ __global__ void __launch_bounds__(MV_THREADS, 1) matvec_kernel(const MatvecParam
   uint64_t* full = reinterpret_cast<uint64_t*>(ring + static_cast<size_t>(p.n_ring) * p.slot_bytes);
   uint64_t* empty = full + p.n_ring;
   volatile int* abort = reinterpret_cast<volatile int*>(empty + p.n_ring);
+  volatile int* issued = abort + 1;  // chunks the producer has issued
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t u0 = static_cast<int64_t>(blockIdx.x) * p.n_units / gridDim.x;
@@ -188,6 +232,7 @@ __global__ void __launch_bounds__(MV_THREADS, 1) matvec_kernel(const MatvecParam
       mbar_init(&empty[i], p.chunk_blocks);
     }
     *abort = 0;
+    *issued = 0;
     fence_mbar_init();
   }
   pdl_enter();
@@ -208,19 +253,27 @@ __global__ void __launch_bounds__(MV_THREADS, 1) matvec_kernel(const MatvecParam
         for (uint32_t i = main_bytes; i < bytes; ++i) dst[i] = base[off + i];  // ragged end of W (< 16 B)
         mbar_expect_tx(&full[slot], main_bytes);
         if (main_bytes) bulk_g2s(dst, base + off, main_bytes, &full[slot]);
+        *issued = c + 1;
+      }
+      // Every copy lands before the CTA may exit (also when the consumers gave up).
+      const int done = *issued;
+      for (int sl = 0; sl < min(done, p.n_ring); ++sl) {
+        const int fills = (done - sl + p.n_ring - 1) / p.n_ring;
+        if (!mbar_wait_bounded(&full[sl], (fills - 1) & 1)) report_error(p.err, ERR_WAIT_TIMEOUT);
       }
     }
     return;
   }
 
   // Consumers: quantise x to Q8_1 in shared memory while the first chunks land.
+  const float inv_rms = (PROD == PROD_RMSNORM) ? rms_inv(p.x, p.K, p.eps, part, MV_CTHREADS) : 0.f;
   const int nq = p.K >> 2;
   for (int base = 0; base < nq; base += 4 * MV_CTHREADS) {
     float4 xv[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int qd = base + i * MV_CTHREADS + threadIdx.x;
-      xv[i] = qd < nq ? __ldg(reinterpret_cast<const float4*>(p.x) + qd) : make_float4(0.f, 0.f, 0.f, 0.f);
+      xv[i] = qd < nq ? produce4<PROD>(p.x, p.aux, 4 * qd, inv_rms) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -258,7 +311,9 @@ __global__ void __launch_bounds__(MV_THREADS, 1) matvec_kernel(const MatvecParam
     for (int it = g0 + threadIdx.x; it < g1; it += MV_CTHREADS) {
       const int c = it / p.chunk_blocks;
       const int slot = c % p.n_ring;
-      if (!mbar_wait(&full[slot], (c / p.n_ring) & 1, abort, p.err)) {
+      // chunk c issued: the slot's completed fills are c / n_ring or one more,
+      // so the parity wait below is unambiguous
+      if (!wait_counter_above(issued, c, abort, p.err) || !mbar_wait(&full[slot], (c / p.n_ring) & 1, abort, p.err)) {
         ok = false;
         break;
       }
@@ -321,7 +376,9 @@ constexpr int LR_NT = 4;                     // tokens per pass of the several-t
                                              // four tokens' activations do not fit beside the weights)
 
 struct MatvecLaneRowParams {
-  const float* x;   // [n_tok][K]
+  const float* x;   // [n_tok][K]; one token: x, or the gate of SwiGLU
+  const float* aux; // one token: SwiGLU up, or RMSNorm gamma
+  float eps;        // RMSNorm
   float* y;         // [n_tok][M]
   int n_tok;        // tokens (1 for the decode matvec)
   int M, K, nb;
@@ -339,7 +396,7 @@ struct MatvecLaneRowParams {
   int* err;
 };
 
-template <int NW, bool RING>
+template <int NW, bool RING, int PROD>
 __global__ void __launch_bounds__((NW + 1) * 32, RING ? 2 : 1)
     matvec_q4k_lanerow_kernel(const __grid_constant__ CUtensorMap tmW, const MatvecLaneRowParams p) {
   constexpr int LR_CT = NW * 32;
@@ -350,6 +407,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, RING ? 2 : 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);  // one per slot
   uint64_t* empty = full + p.S;
   volatile int* abort = reinterpret_cast<volatile int*>(empty + p.S);
+  volatile int* chunks_issued = abort + 1;  // ring form: chunks the producer has issued
 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -363,6 +421,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, RING ? 2 : 1)
       if (RING) mbar_init(&empty[sl], per_chunk);  // every item of a chunk, computed or skipped, arrives once
     }
     *abort = 0;
+    *chunks_issued = 0;
     fence_mbar_init();
   }
   __syncthreads();
@@ -388,6 +447,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, RING ? 2 : 1)
           tma_load_2d(smem + static_cast<size_t>(sl) * p.chunk_bytes, &tmW, &full[sl], c * p.cb * (Q4K_BYTES / 4),
                       r0);
           issued = c + 1;
+          *chunks_issued = issued;
         }
         // Every copy lands before the CTA may exit (also when the consumers gave up).
         for (int sl = 0; sl < min(issued, p.S); ++sl) {
@@ -404,6 +464,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, RING ? 2 : 1)
   // x -> Q8_1 in shared memory: task t quantises x[8t .. 8t+8); the four tasks
   // of a 32-block sit on four consecutive lanes. nt is a multiple of 32, so a
   // warp's tasks are all in range or all out of range.
+  const float inv_rms = (PROD == PROD_RMSNORM) ? rms_inv(p.x, p.K, p.eps, part, LR_CT) : 0.f;
   const int nt = p.K >> 3;
   for (int t0 = 0; t0 < nt; t0 += LR_CT * LR_XT) {
     float v[LR_XT][8];
@@ -411,8 +472,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, RING ? 2 : 1)
     for (int i = 0; i < LR_XT; ++i) {
       const int t = t0 + threadIdx.x + i * LR_CT;
       if (t < nt) {
-        const float4* src = reinterpret_cast<const float4*>(p.x) + 2 * t;
-        const float4 a = __ldg(src), c = __ldg(src + 1);
+        const float4 a = produce4<PROD>(p.x, p.aux, 8 * t, inv_rms);
+        const float4 c = produce4<PROD>(p.x, p.aux, 8 * t + 4, inv_rms);
         v[i][0] = a.x; v[i][1] = a.y; v[i][2] = a.z; v[i][3] = a.w;
         v[i][4] = c.x; v[i][5] = c.y; v[i][6] = c.z; v[i][7] = c.w;
       }
@@ -451,7 +512,9 @@ __global__ void __launch_bounds__((NW + 1) * 32, RING ? 2 : 1)
     } else {
       if (c != ready) {
         sl = c % p.S;
-        if (!mbar_wait(&full[sl], (c / p.S) & 1, abort, p.err)) break;
+        // chunk c issued first: the parity wait cannot take an older fill of the slot
+        if (!wait_counter_above(chunks_issued, c, abort, p.err) || !mbar_wait(&full[sl], (c / p.S) & 1, abort, p.err))
+          break;
         ready = c;
       }
       if (b >= p.nb) {  // zero-filled tail of the last chunk: release it all the same
@@ -735,8 +798,12 @@ static bool plan_lanerow(int64_t M, int64_t K, int num_sms, int nw, int nt, int 
   return false;
 }
 
-cudaError_t launch_matvec(int wtype, const void* W, const float* x, float* y, int64_t M, int64_t K, int* err,
-                          int num_sms, cudaStream_t s, int* status) {
+// Shared-memory attribute slot of a kernel instantiation (allow_max_smem).
+constexpr int smem_slot(int base_x, int base_prod, int prod) { return prod == PROD_X ? base_x : base_prod + prod - 1; }
+
+template <int PROD>
+static cudaError_t launch_matvec_p(int wtype, const void* W, const float* x, const float* aux, float eps, float* y,
+                                   int64_t M, int64_t K, int* err, int num_sms, cudaStream_t s, int* status) {
   *status = KQ_OK;
   // Q4_K: the lane-row kernel with all rows staged at once when they fit
   // (measured faster at the decode sizes: the ring's refills wait for the
@@ -757,24 +824,30 @@ cudaError_t launch_matvec(int wtype, const void* W, const float* x, float* y, in
         return cudaSuccess;
       }
       lp.x = x;
+      lp.aux = aux;
+      lp.eps = eps;
       lp.y = y;
       lp.n_tok = 1;
       lp.err = err;
       if (ring) {
-        cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(matvec_q4k_lanerow_kernel<LR_NW_RING, true>), 10);
+        cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(matvec_q4k_lanerow_kernel<LR_NW_RING, true, PROD>),
+                                       smem_slot(10, 18, PROD));
         if (e != cudaSuccess) return e;
-        return launch_pdl(matvec_q4k_lanerow_kernel<LR_NW_RING, true>, dim3(grid), dim3((LR_NW_RING + 1) * 32), smem,
+        return launch_pdl(matvec_q4k_lanerow_kernel<LR_NW_RING, true, PROD>, dim3(grid), dim3((LR_NW_RING + 1) * 32), smem,
                           s, tmW, lp);
       }
-      cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(matvec_q4k_lanerow_kernel<LR_NW_FULL, false>), 9);
+      cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(matvec_q4k_lanerow_kernel<LR_NW_FULL, false, PROD>),
+                                     smem_slot(9, 16, PROD));
       if (e != cudaSuccess) return e;
-      return launch_pdl(matvec_q4k_lanerow_kernel<LR_NW_FULL, false>, dim3(grid), dim3((LR_NW_FULL + 1) * 32), smem,
+      return launch_pdl(matvec_q4k_lanerow_kernel<LR_NW_FULL, false, PROD>, dim3(grid), dim3((LR_NW_FULL + 1) * 32), smem,
                         s, tmW, lp);
     }
   }
   MatvecParams p{};
   p.W = static_cast<const uint8_t*>(W);
   p.x = x;
+  p.aux = aux;
+  p.eps = eps;
   p.y = y;
   p.M = static_cast<int>(M);
   p.K = static_cast<int>(K);
@@ -808,18 +881,30 @@ cudaError_t launch_matvec(int wtype, const void* W, const float* x, float* y, in
   if (n_ring > need) n_ring = static_cast<int>(need < 1 ? 1 : need);
   p.n_ring = n_ring;
   const size_t smem = static_cast<size_t>(p.xq_bytes + p.xds_bytes + MV_PART_MAX * 4) +
-                      static_cast<size_t>(n_ring) * p.slot_bytes + 2 * n_ring * sizeof(uint64_t) + 16;
+                      static_cast<size_t>(n_ring) * p.slot_bytes + 2 * n_ring * sizeof(uint64_t) + 16;  // + abort, issued
   cudaError_t e;
   if (wtype == KQ_Q4_K) {
-    e = allow_max_smem(reinterpret_cast<const void*>(matvec_kernel<KQ_Q4_K>), 0);
+    e = allow_max_smem(reinterpret_cast<const void*>(matvec_kernel<KQ_Q4_K, PROD>), smem_slot(0, 20, PROD));
     if (e != cudaSuccess) return e;
-    e = launch_pdl(matvec_kernel<KQ_Q4_K>, dim3(G), dim3(MV_THREADS), smem, s, p);
+    e = launch_pdl(matvec_kernel<KQ_Q4_K, PROD>, dim3(G), dim3(MV_THREADS), smem, s, p);
   } else {
-    e = allow_max_smem(reinterpret_cast<const void*>(matvec_kernel<KQ_Q6_K>), 1);
+    e = allow_max_smem(reinterpret_cast<const void*>(matvec_kernel<KQ_Q6_K, PROD>), smem_slot(1, 22, PROD));
     if (e != cudaSuccess) return e;
-    e = launch_pdl(matvec_kernel<KQ_Q6_K>, dim3(G), dim3(MV_THREADS), smem, s, p);
+    e = launch_pdl(matvec_kernel<KQ_Q6_K, PROD>, dim3(G), dim3(MV_THREADS), smem, s, p);
   }
   return e;
+}
+
+cudaError_t launch_matvec(int wtype, const void* W, const float* x, const float* aux, float eps, int prod, float* y,
+                          int64_t M, int64_t K, int* err, int num_sms, cudaStream_t s, int* status) {
+  switch (prod) {
+    case PROD_SWIGLU:
+      return launch_matvec_p<PROD_SWIGLU>(wtype, W, x, aux, eps, y, M, K, err, num_sms, s, status);
+    case PROD_RMSNORM:
+      return launch_matvec_p<PROD_RMSNORM>(wtype, W, x, aux, eps, y, M, K, err, num_sms, s, status);
+    default:
+      return launch_matvec_p<PROD_X>(wtype, W, x, aux, eps, y, M, K, err, num_sms, s, status);
+  }
 }
 
 // Q8_1 of n_tok tokens in the layout the several-token kernel copies into

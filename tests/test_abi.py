@@ -16,8 +16,9 @@ def L():
 
 def test_header_declares_the_boundary():
     names = nat.header_symbols()
-    assert {"kq_quantize_q8_1", "kq_matvec", "kq_gemm", "kq_moe_grouped_gemm", "kq_workspace_bytes",
-            "kq_get_device_error", "kq_status_str"} <= set(names)
+    assert {"kq_quantize_q8_1", "kq_matvec", "kq_matvec_swiglu", "kq_matvec_rmsnorm", "kq_gemm",
+            "kq_moe_grouped_gemm", "kq_moe_combine", "kq_workspace_bytes", "kq_get_device_error",
+            "kq_status_str"} <= set(names)
 
 
 def test_every_declared_symbol_is_exported(L):
@@ -52,6 +53,26 @@ def test_matvec_argument_checks(L):
     assert L.kq_matvec(nat.KQ_Q4_K, A, A, A, 16, 300, NUL) == nat.KQ_ERR_SHAPE
     assert L.kq_matvec(nat.KQ_Q6_K, A, A, A, 0, 256, NUL) == nat.KQ_ERR_SHAPE
     assert L.kq_matvec(nat.KQ_Q4_K, A, U, A, 16, 256, NUL) == nat.KQ_ERR_ALIGN
+
+
+def test_fused_matvec_argument_checks(L):
+    f = ctypes.c_float
+    assert L.kq_matvec_swiglu(nat.KQ_Q4_K, A, A, NUL, A, 16, 256, NUL) == nat.KQ_ERR_NULL
+    assert L.kq_matvec_swiglu(nat.KQ_Q4_K, A, A, U, A, 16, 256, NUL) == nat.KQ_ERR_ALIGN
+    assert L.kq_matvec_swiglu(nat.KQ_Q6_K, A, A, A, A, 16, 100, NUL) == nat.KQ_ERR_SHAPE
+    assert L.kq_matvec_rmsnorm(nat.KQ_Q4_K, A, A, NUL, f(1e-6), A, 16, 256, NUL) == nat.KQ_ERR_NULL
+    assert L.kq_matvec_rmsnorm(nat.KQ_Q4_K, A, A, A, f(-1.0), A, 16, 256, NUL) == nat.KQ_ERR_SHAPE
+    assert L.kq_matvec_rmsnorm(nat.KQ_Q4_K, A, A, A, f(float("nan")), A, 16, 256, NUL) == nat.KQ_ERR_SHAPE
+    assert L.kq_matvec_rmsnorm(nat.KQ_Q4_K, A, A, U, f(1e-6), A, 16, 256, NUL) == nat.KQ_ERR_ALIGN
+    assert L.kq_matvec_rmsnorm(5, A, A, A, f(1e-6), A, 16, 256, NUL) == nat.KQ_ERR_TYPE
+
+
+def test_moe_combine_argument_checks(L):
+    assert L.kq_moe_combine(NUL, A, A, 16, 4, 2, NUL) == nat.KQ_ERR_NULL
+    assert L.kq_moe_combine(A, A, A, 0, 4, 2, NUL) == nat.KQ_ERR_SHAPE
+    assert L.kq_moe_combine(A, A, A, 16, 4, 0, NUL) == nat.KQ_ERR_SHAPE
+    assert L.kq_moe_combine(A, A, A, 16, 4, 513, NUL) == nat.KQ_ERR_SHAPE
+    assert L.kq_moe_combine(A, U, A, 16, 4, 2, NUL) == nat.KQ_ERR_ALIGN
 
 
 def test_gemm_argument_checks(L):

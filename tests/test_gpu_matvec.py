@@ -90,3 +90,22 @@ def test_ring_staging_shapes_sampled_rows(M, K):
     Yr, B = ora.matmul_rows("q4_k", W, x, K, rows)
     assert_within_bound(y[rows], Yr[0], B[0], f"ring {M}x{K}")
     assert np.all(np.isfinite(y))
+
+
+@pytest.mark.parametrize("wtype,M,K", [
+    ("q4_k", 256, 102400),    # item kernel, 3 ring slots for up to 8 chunks per CTA
+    ("q6_k", 304, 102400),    # item kernel, 3 slots, 8-row units
+    ("q4_k", 4560, 49152),    # lane-row ring form with 2 slots of 5-block chunks
+])
+def test_shallow_rings_sampled_rows(wtype, M, K):
+    # Rings much shallower than the distance the consumers can run ahead: a
+    # consumer must never take an older fill of its chunk's slot (same barrier
+    # parity) for its chunk, and no copy may still be in flight when a CTA ends.
+    rng = np.random.default_rng(M + K)
+    W = syn.weights(wtype, rng, M, K)
+    x = syn.activations(rng, K, 1)
+    y = _run(wtype, W, x, M, K)
+    rows = np.unique(np.concatenate([rng.choice(M, 128, replace=False), [0, 1, M - 2, M - 1]]))
+    Yr, B = ora.matmul_rows(wtype, W, x, K, rows)
+    assert_within_bound(y[rows], Yr[0], B[0], f"shallow ring {wtype} {M}x{K}")
+    assert np.all(np.isfinite(y))
