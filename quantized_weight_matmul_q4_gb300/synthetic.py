@@ -20,6 +20,13 @@ Distributions follow the workloads of the k-quant matmul pages:
   ``scales[16]`` uniform on [-64, 63] at byte 192 and fp16 ``d`` at byte 208
   (the generator bug described in "06 · 8e/8e②", §3.3 Pitfalls, put d at byte
   0; it sits at 208). ``d`` is drawn like the Q4_K ``d``.
+* TQ4_1S block (32 weights, 20 bytes; "TQ4_1S Weight Kernel Optimization",
+  Block Layout): fp16 ``d0`` at byte 0 and ``d1`` at byte 2, each drawn as
+  0.02 * exp(0.25 * N(0, 1)) (positive half-block scales of the size of a
+  7B model's weights), then 16 bytes of 4-bit centroid indices, element j in
+  byte j / 2 (low nibble for even j). The indices are floor(8 + 3 z) clipped to
+  [0, 15] with z ~ N(0, 1): symmetric and bell-shaped like the occupancy of
+  the Lloyd-Max cells of N(0, 1), without the centroid table.
 * Activations X: fp32 N(0, 1), token-major (K contiguous per token).
 * MoE routing: for every token, the top-k experts of softmax(N(0,1) logits),
   ordered by descending probability, ties to the lower expert index.
@@ -32,6 +39,8 @@ QK_K = 256            # weights per k-quant super-block
 Q4_K_BYTES = 144      # bytes per Q4_K super-block
 Q6_K_BYTES = 210      # bytes per Q6_K super-block
 Q8_1_BYTES = 36       # bytes per 32-element Q8_1 activation block
+QK_TQ = 32            # weights per TQ4_1S block
+TQ4_1S_BYTES = 20     # bytes per TQ4_1S block
 QK8_1 = 32            # activations per Q8_1 block
 
 
@@ -74,7 +83,22 @@ def q6_k_weights(rng: np.random.Generator, M: int, K: int) -> np.ndarray:
     return w.reshape(M, nb * Q6_K_BYTES)
 
 
+def tq4_1s_weights(rng: np.random.Generator, M: int, K: int) -> np.ndarray:
+    """Random TQ4_1S matrix: uint8 array of shape [M, (K/32)*20], row-major."""
+    if K % QK_TQ:
+        raise ValueError("K must be a multiple of 32")
+    nb = K // QK_TQ
+    w = np.empty((M, nb, TQ4_1S_BYTES), dtype=np.uint8)
+    d = (0.02 * np.exp(0.25 * rng.standard_normal((M, nb, 2)))).astype(np.float16)
+    w[:, :, 0:4] = d.view(np.uint8).reshape(M, nb, 4)
+    idx = np.clip(np.floor(8 + 3 * rng.standard_normal((M, nb, QK_TQ))), 0, 15).astype(np.uint8)
+    w[:, :, 4:20] = idx[..., 0::2] | (idx[..., 1::2] << 4)
+    return w.reshape(M, nb * TQ4_1S_BYTES)
+
+
 def weights(wtype: str, rng: np.random.Generator, M: int, K: int) -> np.ndarray:
+    if wtype == "tq4_1s":
+        return tq4_1s_weights(rng, M, K)
     if wtype == "q4_k":
         return q4_k_weights(rng, M, K)
     if wtype == "q6_k":
@@ -99,12 +123,15 @@ def expert_ids(rng: np.random.Generator, T: int, n_experts: int, top_k: int) -> 
     return np.ascontiguousarray(order[:, :top_k].astype(np.int32))
 
 
-# Seeded workloads with the shapes of the k-quant matmul pages. Seeds: the
-# 512x2048 matvec uses seed 0; the others use 1..4 in the order listed.
+# Seeded workloads with the shapes of the pages. Seeds: the 512x2048 matvec
+# uses seed 0; the others use 1..6. The TQ4_1S shapes are the FFN matvecs of the
+# 7B model the TQ4_1S page decodes (hidden 3584, intermediate 18944).
 WORKLOADS = {
     "matvec_q4k_512x2048": dict(kind="matvec", wtype="q4_k", M=512, K=2048, N=1, seed=0),
     "decode_q4k_4096x11008": dict(kind="matvec", wtype="q4_k", M=4096, K=11008, N=1, seed=1),
     "decode_q4k_11008x4096": dict(kind="matvec", wtype="q4_k", M=11008, K=4096, N=1, seed=1),
+    "decode_tq4_1s_18944x3584": dict(kind="matvec", wtype="tq4_1s", M=18944, K=3584, N=1, seed=6),
+    "decode_tq4_1s_3584x18944": dict(kind="matvec", wtype="tq4_1s", M=3584, K=18944, N=1, seed=6),
     "smalln_q4k_4096x11008_n4": dict(kind="gemm", wtype="q4_k", M=4096, K=11008, N=4, seed=5),
     "prefill_q4k_4096x4096_n64": dict(kind="gemm", wtype="q4_k", M=4096, K=4096, N=64, seed=2),
     "prefill_q4k_4096x4096_n512": dict(kind="gemm", wtype="q4_k", M=4096, K=4096, N=512, seed=2),

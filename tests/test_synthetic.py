@@ -35,6 +35,20 @@ def test_q6k_generator_fields_and_d_offset():
     assert not (0.005 < np.abs(lead[np.isfinite(lead)]).mean() < 0.011)
 
 
+def test_tq4_1s_generator_fields():
+    W = syn.tq4_1s_weights(np.random.default_rng(3), 32, 4096)
+    assert W.shape == (32, 128 * 20) and W.dtype == np.uint8
+    blk = W.reshape(32, 128, 20)
+    d = _f16(blk[..., 0:4].reshape(32, 128, 2, 2)).ravel()
+    assert np.all(d > 0) and 0.018 < np.median(d) < 0.022            # 0.02 * exp(0.25 N(0,1))
+    lo, hi = blk[..., 4:20] & 0xF, blk[..., 4:20] >> 4
+    idx = np.concatenate([lo.ravel(), hi.ravel()])
+    counts = np.bincount(idx, minlength=16)
+    assert np.all(counts > 0)                                        # every index occurs
+    assert counts[7] + counts[8] > 5 * (counts[0] + counts[15])      # bell-shaped, symmetric
+    assert abs(int(counts[:8].sum()) - int(counts[8:].sum())) < 0.02 * idx.size
+
+
 def test_activations_and_ids():
     X = syn.activations(np.random.default_rng(2), 4096, 8)
     assert X.shape == (8, 4096) and X.dtype == np.float32
