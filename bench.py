@@ -412,6 +412,65 @@ def _timed_calls(fn, iters, warm, flush, torch, stream):
     return statistics.mean(graph), min(graph), statistics.mean(eager)
 
 
+# Decode sweeps of other weight formats: name -> (workloads, weight copies).
+# Copies of each matrix make the swept weights larger than L2.
+DECODE_SECTIONS = {
+    "decode_tq4_1s_18944x3584_3584x18944": (("decode_tq4_1s_18944x3584", "decode_tq4_1s_3584x18944"), 4),
+    "decode_q6k_4096x11008_11008x4096": (("decode_q6k_4096x11008", "decode_q6k_11008x4096"), 4),
+}
+
+
+def _decode_sweep(kq, syn, torch, dev, stream, names, copies, reps, pk):
+    """One kq_matvec per weight copy and shape, captured as a CUDA graph and
+    replayed `reps` times back to back (weights larger than L2, so no flush).
+    Returns the section's numbers: algorithmic GB/s = (weights + x + y bytes)
+    / device time."""
+    sets = []
+    for name in names:
+        wl = syn.make_workload(name, copies=copies)
+        Ws = [torch.from_numpy(w).to(dev) for w in wl["W"]]
+        x = torch.from_numpy(wl["X"][0]).to(dev)
+        y = torch.empty(wl["M"], dtype=torch.float32, device=dev)
+        sets.append((wl["wtype"], wl["M"], wl["K"], Ws, x, y))
+
+    def step():
+        for c in range(copies):
+            for (wt, M, K, Ws, x, y) in sets:
+                kq.kq_matvec(wt, Ws[c], x, M, K, y=y)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        step()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        step()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        g.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / reps
+    nbytes = sum(copies * (Ws[0].numel() + 4 * K + 4 * M) for (_, M, K, Ws, _, _) in sets)
+    launches = copies * len(sets)
+    gbs = nbytes / (ms / 1e3) / 1e9
+    if kq.kq_get_device_error():
+        raise RuntimeError("device error during a decode section")
+    return {"ms_per_sweep": round(ms, 4), "launches_per_sweep": launches,
+            "us_per_launch": round(1e3 * ms / launches, 2),
+            "weight_mb_per_sweep": round(sum(copies * Ws[0].numel() for (_, _, _, Ws, _, _) in sets) / 1e6, 1),
+            "gbs": round(gbs, 1), "frac_hbm_peak": round(gbs / pk["hbm_gbs"], 4)}
+
+
 def run_sections(args, kq, syn, torch, dev, stream, pk, only=None):
     # L2 flush between timed calls: write 256 MB (> L2), then read another
     # 256 MB, so L2 holds only clean lines when the call starts (the write-back
@@ -423,12 +482,17 @@ def run_sections(args, kq, syn, torch, dev, stream, pk, only=None):
         flush_w.zero_()
         flush_r.sum()
     res = {}
+    for name, (names, copies) in DECODE_SECTIONS.items():
+        if only is None or only == name:
+            res[name] = _decode_sweep(kq, syn, torch, dev, stream, names, copies, 20, pk)
+    if only in DECODE_SECTIONS:
+        return res
     iters = max(3, args.section_iters)
     gemm_names = ["smalln_q4k_4096x11008_n4", "prefill_q4k_4096x4096_n64", "prefill_q4k_4096x4096_n512",
                   "prefill_q4k_14336x4096_n2048", "prefill_q6k_4096x14336_n2048"]
     moe_name = "moe_q4k_128x768x2048_t1024_top8"
     if only is not None:
-        if only not in gemm_names + [moe_name]:
+        if only not in gemm_names + [moe_name] + list(DECODE_SECTIONS):
             raise SystemExit(f"unknown section {only!r}")
         gemm_names = [n for n in gemm_names if n == only]
     for name in gemm_names:

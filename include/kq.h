@@ -4,7 +4,9 @@
  *   Y[M, N] = dequant(W)[M, K] . X[K, N]
  *
  * W holds 4-bit Q4_K or 6-bit Q6_K super-blocks; X is fp32 and is quantised to
- * Q8_1 (int8 codes with an fp16 scale per 32 values) inside every call.
+ * Q8_1 (int8 codes with an fp16 scale per 32 values) inside every call. The
+ * decode matvec also takes TQ4_1S weights (WHT-rotated 4-bit Lloyd-Max codes),
+ * which it multiplies with the fp32 activations directly.
  *
  * Sources (page title, section):
  *  [MMVQ]  "06 · 8e/8e② — decode MMVQ: dp4a integer dot products + the llama.cpp
@@ -17,6 +19,9 @@
  *  [GAP]   "Prefill Gap Closure Plan — ZINC CUDA vs llama.cpp": T1 (fused dequant
  *          tensor-core GEMM), T2 (grouped MoE expert GEMM: histogram, prefix sum,
  *          scatter, per-expert GEMM).
+ *  [TQ]    "TQ4_1S Weight Kernel Optimization": Architecture Overview (rotated
+ *          4-bit weights, dequant = centroid[index] * half-block scale, inverse
+ *          WHT, pre-rotated activation), Block Layout, Centroid Table.
  *
  * Conventions for every entry point
  *  - Pointers are device pointers owned by the caller (cudaMalloc / a framework
@@ -27,13 +32,15 @@
  *      W : M rows x (K/256) super-blocks; a Q4_K block is 144 bytes
  *          [fp16 d][fp16 dmin][12 B packed 6-bit scales/mins][128 B nibbles],
  *          a Q6_K block is 210 bytes [ql 128][qh 64][int8 scales 16][fp16 d].
+ *          TQ4_1S: M rows x (K/32) blocks of 20 bytes [fp16 d0][fp16 d1][qs 16],
+ *          element j's centroid index in qs[j/2], low nibble for even j.
  *          For MoE the experts' matrices are concatenated, expert-major.
  *      X : fp32, token-major: token n occupies X[n*K .. n*K+K-1].
  *      Y : fp32, token-major: Y[n*M + m].
  *      Xq: N x (K/32) Q8_1 blocks of 36 bytes [fp16 d][fp16 s][int8 q[32]].
  *  - Alignment: W, X, Y, Xq and ws must be 16-byte aligned.
- *  - Sizes: K must be a multiple of 256 (32 for kq_quantize_q8_1); M, N, T >= 1;
- *    all sizes below 2^31.
+ *  - Sizes: K must be a multiple of 256 (32 for kq_quantize_q8_1 and for TQ4_1S);
+ *    M, N, T >= 1; all sizes below 2^31.
  *  - Work is queued on `stream` (a cudaStream_t; NULL = legacy default stream).
  *    A status other than KQ_OK means nothing was queued, except KQ_ERR_CUDA
  *    after a failed launch.
@@ -74,7 +81,9 @@ typedef enum kq_status {
   KQ_ERR_DEVICE = 7     /* a kernel recorded an error; see kq_get_device_error */
 } kq_status;
 
-typedef enum kq_wtype { KQ_Q4_K = 1, KQ_Q6_K = 2 } kq_wtype;
+/* KQ_TQ4_1S is taken by kq_matvec only; the other entry points return
+ * KQ_ERR_TYPE for it. */
+typedef enum kq_wtype { KQ_Q4_K = 1, KQ_Q6_K = 2, KQ_TQ4_1S = 3 } kq_wtype;
 
 typedef enum kq_op { KQ_OP_MATVEC = 1, KQ_OP_GEMM = 2, KQ_OP_MOE = 3 } kq_op;
 
@@ -106,6 +115,17 @@ KQ_API kq_status kq_quantize_q8_1(const float* X, void* Xq, int64_t K, int64_t N
  * call starts, i.e. by a preceding kernel that allows programmatic dependent
  * launch. (A preceding ordinary kernel, copy or event is always complete.)
  * A Q6_K row whose byte length is not a multiple of 16 must have K <= 15360.
+ *
+ * wtype KQ_TQ4_1S ([TQ]): W holds rotated weights r_b[j] = c[idx_j] * d_h(j)
+ * per 32-block b (c the page's 16-entry centroid table, d0 for j < 16, d1
+ * otherwise), and y[m] = Sum_b w_b . x_b with w_b = H^-1 r_b, H the orthonormal
+ * 32-point Walsh-Hadamard transform in natural order (H[i][j] =
+ * (-1)^popcount(i & j) / sqrt(32), its own inverse). The call rotates x once
+ * (x_r = H x_b, fp32) and computes Sum_b r_b . x_r in fp32; no Q8_1 step.
+ * K must be a multiple of 32 (multiples of 128 take the TMA-staged kernel).
+ * Accuracy: |y - y_ref| <= 1e-3 * Sum_b Sum_j Sum_k |r_b[j] H[j][k] x_b[k]| + 1e-5,
+ * y_ref the exact product. Weight streaming starts before the dependency wait,
+ * as above.
  */
 KQ_API kq_status kq_matvec(int wtype, const void* W, const float* x, float* y, int64_t M, int64_t K,
                            kq_stream_t stream);
@@ -122,7 +142,8 @@ KQ_API kq_status kq_matvec(int wtype, const void* W, const float* x, float* y, i
  * fp32; the Q8_1 codes are then made from those fp32 values exactly as in
  * kq_matvec, and Y meets the accuracy bound against the exact product of the
  * dequantised weights with the Q8_1 codes of the produced activations.
- * Otherwise as kq_matvec (wtype, layouts, W streamed before the dependency wait).
+ * Otherwise as kq_matvec (wtype, layouts, W streamed before the dependency wait);
+ * KQ_TQ4_1S is not taken here (KQ_ERR_TYPE).
  */
 KQ_API kq_status kq_matvec_swiglu(int wtype, const void* W, const float* gate, const float* up, float* y, int64_t M,
                                   int64_t K, kq_stream_t stream);

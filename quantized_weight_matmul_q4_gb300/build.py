@@ -18,7 +18,7 @@ OUT_DIR = os.path.join(PKG_DIR, "_lib")
 LIB_PATH = os.path.join(OUT_DIR, "libkq.so")
 INCLUDE = os.path.join(ROOT, "include")
 
-SOURCES = ["kq_api.cu", "kq_quant.cu", "kq_matvec.cu", "kq_gemm.cu", "kq_gemm_noalloc.cu", "kq_combine.cu"]
+SOURCES = ["kq_api.cu", "kq_quant.cu", "kq_matvec.cu", "kq_gemm.cu", "kq_gemm_noalloc.cu", "kq_combine.cu", "kq_tq4.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", f"-I{INCLUDE}"]

@@ -109,6 +109,18 @@ kq_status kq_quantize_q8_1(const float* X, void* Xq, int64_t K, int64_t N, kq_st
 
 static kq_status matvec_entry(int wtype, const void* W, const float* x, const float* aux, float eps, int prod,
                               float* y, int64_t M, int64_t K, kq_stream_t stream) {
+  if (wtype == KQ_TQ4_1S && prod == PROD_X) {
+    if (!W || !x || !y) return KQ_ERR_NULL;
+    if (M <= 0 || K <= 0 || K % 32 != 0 || M > kMaxDim || K > kMaxDim) return KQ_ERR_SHAPE;
+    if (!aligned16(W) || !aligned16(x) || !aligned16(y)) return KQ_ERR_ALIGN;
+    int dev, sms;
+    int* err;
+    cudaError_t e = device_state(&dev, &sms, &err);
+    if (e != cudaSuccess) return KQ_ERR_CUDA;
+    int status = KQ_OK;
+    e = launch_tq4_matvec(W, x, y, M, K, err, sms, reinterpret_cast<cudaStream_t>(stream), &status);
+    return finish(e, status);
+  }
   if (!valid_wtype(wtype)) return KQ_ERR_TYPE;
   if (!W || !x || !y || (prod != PROD_X && !aux)) return KQ_ERR_NULL;
   if (M <= 0 || K <= 0 || K % QK_K != 0 || M > kMaxDim || K > kMaxDim) return KQ_ERR_SHAPE;

@@ -26,6 +26,10 @@ constexpr int PROD_RMSNORM = 2;
 cudaError_t launch_matvec(int wtype, const void* W, const float* x, const float* aux, float eps, int prod, float* y,
                           int64_t M, int64_t K, int* err, int num_sms, cudaStream_t s, int* status);
 
+// TQ4_1S decode matvec y = W . x (K a multiple of 32; W 16-byte aligned).
+cudaError_t launch_tq4_matvec(const void* W, const float* x, float* y, int64_t M, int64_t K, int* err, int num_sms,
+                              cudaStream_t s, int* status);
+
 // Several tokens (Q4_K, 2 <= N <= LR_TOKENS_MAX) on the decode matvec path:
 // Y[N][M] = dequant(W) . X[N][K], the tokens' Q8_1 codes made once into
 // `scratch` (device memory; at most ~1.25 N K + 256 N bytes are used);
@@ -71,7 +75,7 @@ cudaError_t device_context(int* dev, int* num_sms, int** err);
 // Raises a kernel's dynamic shared-memory limit to the 227 KB maximum, once per
 // device (later calls only read a flag, so launches stay cheap and capturable).
 cudaError_t allow_max_smem(const void* kernel, int slot);
-constexpr int kSmemSlots = 24;
+constexpr int kSmemSlots = 26;
 
 // Launches `kernel` on `s` with programmatic stream serialization allowed (the
 // kernel calls pdl_enter() before its first global memory access).

@@ -130,6 +130,8 @@ WORKLOADS = {
     "matvec_q4k_512x2048": dict(kind="matvec", wtype="q4_k", M=512, K=2048, N=1, seed=0),
     "decode_q4k_4096x11008": dict(kind="matvec", wtype="q4_k", M=4096, K=11008, N=1, seed=1),
     "decode_q4k_11008x4096": dict(kind="matvec", wtype="q4_k", M=11008, K=4096, N=1, seed=1),
+    "decode_q6k_4096x11008": dict(kind="matvec", wtype="q6_k", M=4096, K=11008, N=1, seed=1),
+    "decode_q6k_11008x4096": dict(kind="matvec", wtype="q6_k", M=11008, K=4096, N=1, seed=1),
     "decode_tq4_1s_18944x3584": dict(kind="matvec", wtype="tq4_1s", M=18944, K=3584, N=1, seed=6),
     "decode_tq4_1s_3584x18944": dict(kind="matvec", wtype="tq4_1s", M=3584, K=18944, N=1, seed=6),
     "smalln_q4k_4096x11008_n4": dict(kind="gemm", wtype="q4_k", M=4096, K=11008, N=4, seed=5),

@@ -48,11 +48,24 @@ def test_quantize_argument_checks(L):
 
 
 def test_matvec_argument_checks(L):
-    assert L.kq_matvec(3, A, A, A, 16, 256, NUL) == nat.KQ_ERR_TYPE
+    assert L.kq_matvec(9, A, A, A, 16, 256, NUL) == nat.KQ_ERR_TYPE
     assert L.kq_matvec(nat.KQ_Q4_K, NUL, A, A, 16, 256, NUL) == nat.KQ_ERR_NULL
     assert L.kq_matvec(nat.KQ_Q4_K, A, A, A, 16, 300, NUL) == nat.KQ_ERR_SHAPE
     assert L.kq_matvec(nat.KQ_Q6_K, A, A, A, 0, 256, NUL) == nat.KQ_ERR_SHAPE
     assert L.kq_matvec(nat.KQ_Q4_K, A, U, A, 16, 256, NUL) == nat.KQ_ERR_ALIGN
+
+
+def test_tq4_1s_argument_checks(L):
+    # TQ4_1S: K a multiple of 32; the decode matvec is its only entry point.
+    assert L.kq_matvec(nat.KQ_TQ4_1S, NUL, A, A, 16, 256, NUL) == nat.KQ_ERR_NULL
+    assert L.kq_matvec(nat.KQ_TQ4_1S, A, A, A, 16, 48, NUL) == nat.KQ_ERR_SHAPE
+    assert L.kq_matvec(nat.KQ_TQ4_1S, A, A, A, 0, 64, NUL) == nat.KQ_ERR_SHAPE
+    assert L.kq_matvec(nat.KQ_TQ4_1S, U, A, A, 16, 64, NUL) == nat.KQ_ERR_ALIGN
+    assert L.kq_matvec_swiglu(nat.KQ_TQ4_1S, A, A, A, A, 16, 256, NUL) == nat.KQ_ERR_TYPE
+    assert L.kq_matvec_rmsnorm(nat.KQ_TQ4_1S, A, A, A, ctypes.c_float(1e-6), A, 16, 256, NUL) == nat.KQ_ERR_TYPE
+    assert L.kq_gemm(nat.KQ_TQ4_1S, A, A, A, 16, 256, 4, A, 1 << 30, NUL) == nat.KQ_ERR_TYPE
+    assert L.kq_gemm_noalloc(nat.KQ_TQ4_1S, A, A, A, 16, 256, 4, NUL) == nat.KQ_ERR_TYPE
+    assert L.kq_moe_grouped_gemm(nat.KQ_TQ4_1S, A, 8, A, 2, A, A, 16, 256, 4, A, 1 << 30, NUL) == nat.KQ_ERR_TYPE
 
 
 def test_fused_matvec_argument_checks(L):
