@@ -56,8 +56,14 @@ constexpr int TQ_CHUNK_TARGET = 24 * 1024;
 constexpr int TQD_WARPS = 8;           // rows per CTA of the fallback kernel
 constexpr int TQD_SEG = 512;           // blocks of x rotated per pass of the fallback kernel (64 KB)
 constexpr float TQ_INV_SQRT32 = 0.17677669529663688f;
+constexpr int TQ_CODE_BIAS = 4096;              // pair-table codes are 1000 * centroid + 4096 (13 bits)
+constexpr float TQ_MAGIC = 8388608.0f + 4096.0f;  // float bits 0x4B000000 | code equal 2^23 + code
+constexpr int TQ_PAIR_TABLE_BYTES = 256 * 32 * 4;  // a word per index byte, one copy per lane
 
-// Lloyd-Max centroids of N(0, 1), index order, as printed on the page.
+// Lloyd-Max centroids of N(0, 1), index order, as printed on the page, and
+// the same values times 1000 (integers, since the page prints three decimals).
+__constant__ int c_tq_centroids_milli[16] = {-2733, -2069, -1618, -1256, -942, -657, -388, -128,
+                                             128,   388,   657,   942,   1256, 1618, 2069, 2733};
 __constant__ float c_tq_centroids[16] = {-2.733f, -2.069f, -1.618f, -1.256f, -0.942f, -0.657f, -0.388f, -0.128f,
                                          0.128f,  0.388f,  0.657f,  0.942f,  1.256f,  1.618f,  2.069f,  2.733f};
 
@@ -89,6 +95,18 @@ __device__ __forceinline__ void load_rotate(const float* __restrict__ x, int b, 
   wht32(v);
 }
 
+__device__ __forceinline__ void load_block(const float* src, float (&v)[TQ_BLOCK]) {
+  const float4* s4 = reinterpret_cast<const float4*>(src);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const float4 t = s4[k];
+    v[4 * k] = t.x;
+    v[4 * k + 1] = t.y;
+    v[4 * k + 2] = t.z;
+    v[4 * k + 3] = t.w;
+  }
+}
+
 __device__ __forceinline__ void store_block(float* dst, const float (&v)[TQ_BLOCK]) {
   float4* d = reinterpret_cast<float4*>(dst);
 #pragma unroll
@@ -106,27 +124,62 @@ __device__ __forceinline__ float lut_at(const float* lut, uint32_t off) {
 // activations (16-byte aligned).
 __device__ __forceinline__ float block_dot(uint32_t dw, const uint32_t (&q)[4], const float* xr, const float* lut) {
   const float4* x4 = reinterpret_cast<const float4*>(xr);
-  float s[2] = {0.f, 0.f};
+  float2 s[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // per half block: even / odd elements
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const uint32_t w = q[k];
     const uint32_t e4 = (w << 2) & 0x3C3C3C3Cu;  // 4 * index of elements 8k, 8k+2, 8k+4, 8k+6 (one per byte)
     const uint32_t o4 = (w >> 2) & 0x3C3C3C3Cu;  // 4 * index of elements 8k+1, 8k+3, 8k+5, 8k+7
     const float4 xa = x4[2 * k], xb = x4[2 * k + 1];
-    float a = s[k >> 1];
-    a = fmaf(lut_at(lut, e4 & 0xFFu), xa.x, a);
-    a = fmaf(lut_at(lut, o4 & 0xFFu), xa.y, a);
-    a = fmaf(lut_at(lut, __byte_perm(e4, 0u, 0x4441u)), xa.z, a);
-    a = fmaf(lut_at(lut, __byte_perm(o4, 0u, 0x4441u)), xa.w, a);
-    a = fmaf(lut_at(lut, __byte_perm(e4, 0u, 0x4442u)), xb.x, a);
-    a = fmaf(lut_at(lut, __byte_perm(o4, 0u, 0x4442u)), xb.y, a);
-    a = fmaf(lut_at(lut, e4 >> 24), xb.z, a);
-    a = fmaf(lut_at(lut, o4 >> 24), xb.w, a);
+    float2 a = s[k >> 1];
+    a = __ffma2_rn(make_float2(lut_at(lut, e4 & 0xFFu), lut_at(lut, o4 & 0xFFu)), make_float2(xa.x, xa.y), a);
+    a = __ffma2_rn(make_float2(lut_at(lut, __byte_perm(e4, 0u, 0x4441u)), lut_at(lut, __byte_perm(o4, 0u, 0x4441u))),
+                   make_float2(xa.z, xa.w), a);
+    a = __ffma2_rn(make_float2(lut_at(lut, __byte_perm(e4, 0u, 0x4442u)), lut_at(lut, __byte_perm(o4, 0u, 0x4442u))),
+                   make_float2(xb.x, xb.y), a);
+    a = __ffma2_rn(make_float2(lut_at(lut, e4 >> 24), lut_at(lut, o4 >> 24)), make_float2(xb.z, xb.w), a);
     s[k >> 1] = a;
   }
   const float d0 = __half2float(__ushort_as_half(static_cast<unsigned short>(dw & 0xFFFFu)));
   const float d1 = __half2float(__ushort_as_half(static_cast<unsigned short>(dw >> 16)));
-  return fmaf(d1, s[1], d0 * s[0]);
+  return fmaf(d1, s[1].x + s[1].y, d0 * (s[0].x + s[0].y));
+}
+
+// The same dot product with the pair table: word (b, lane) of `tbl` holds the
+// codes of both centroids of index byte b, 1000 c[b & 15] + 4096 in its low half
+// and 1000 c[b >> 4] + 4096 in its high half. Each lane reads its own copy
+// (bank = lane), so the 32 lanes never conflict, and one 4-byte read serves two
+// elements. A code placed in the mantissa of 2^23 (one byte permute) minus
+// 2^23 + 4096 gives 1000 c exactly in fp32; the half-block scales carry the
+// 1/1000.
+__device__ __forceinline__ float block_dot_pairs(uint32_t dw, const uint32_t (&q)[4], const float* xr,
+                                                 const uint8_t* tbl, uint32_t laneoff) {
+  const float4* x4 = reinterpret_cast<const float4*>(xr);
+  const float2 neg_magic = make_float2(-TQ_MAGIC, -TQ_MAGIC);
+  float2 s[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // per half block: even / odd elements
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t w = q[k];
+    const float4 xa = x4[2 * k], xb = x4[2 * k + 1];
+    float2 a = s[k >> 1];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {  // byte m: elements 8k + 2m (low nibble) and 8k + 2m + 1
+      const uint32_t b = __byte_perm(w, 0u, 0x4440u + m);
+      const uint32_t t = *reinterpret_cast<const uint32_t*>(tbl + b * 128u + laneoff);
+      const float2 f = make_float2(__uint_as_float(__byte_perm(t, 0x4B000000u, 0x7610u)),
+                                   __uint_as_float(__byte_perm(t, 0x4B000000u, 0x7632u)));
+      const float2 c = __fadd2_rn(f, neg_magic);  // exact: 1000 * centroid
+      const float2 xv = m == 0 ? make_float2(xa.x, xa.y)
+                        : m == 1 ? make_float2(xa.z, xa.w)
+                        : m == 2 ? make_float2(xb.x, xb.y)
+                                 : make_float2(xb.z, xb.w);
+      a = __ffma2_rn(c, xv, a);
+    }
+    s[k >> 1] = a;
+  }
+  const float d0 = __half2float(__ushort_as_half(static_cast<unsigned short>(dw & 0xFFFFu))) * 0.001f;
+  const float d1 = __half2float(__ushort_as_half(static_cast<unsigned short>(dw >> 16))) * 0.001f;
+  return fmaf(d1, s[1].x + s[1].y, d0 * (s[0].x + s[0].y));
 }
 
 // i / d for d >= 1, with inv = ceil(2^32 / d) when d >= 2 (exact while i * d < 2^32).
@@ -151,7 +204,7 @@ struct TqLaneRowParams {
   int chunk_bytes;     // Qc * qpad
   int S;               // chunk slots
   uint32_t inv_per_chunk, inv_steps, inv_R;  // ceil(2^32 / d) for d = n_groups * steps, steps, R (d >= 2)
-  int xr_off, part_off, lut_off, bar_off;    // shared-memory layout (bytes)
+  int slot_off, xr_off, part_off, bar_off;   // shared-memory layout (bytes); the pair table sits at 0
   int* err;
 };
 
@@ -160,7 +213,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
     tq4_lanerow_kernel(const __grid_constant__ CUtensorMap tmW, const TqLaneRowParams p) {
   constexpr int CT = NW * 32;
   extern __shared__ __align__(1024) uint8_t smem[];
-  float* lut = reinterpret_cast<float*>(smem + p.lut_off);      // 16 centroids, 128-byte aligned
+  const uint8_t* tbl = smem;                                     // pair table at offset 0 (a constant address)
   float* xr = reinterpret_cast<float*>(smem + p.xr_off);        // [quad][132]
   float* part = reinterpret_cast<float*>(smem + p.part_off);    // [warp][group][lane]
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);  // one per slot
@@ -182,7 +235,6 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
     *chunks_issued = 0;
     fence_mbar_init();
   }
-  if (threadIdx.x < 16) lut[threadIdx.x] = c_tq_centroids[threadIdx.x];
   __syncthreads();
 
   if (warp == NW) {
@@ -196,7 +248,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
         const int q0 = c * p.Qc;
         const int nqc = min(p.Qc, p.nq - q0);  // quads past the row end are not copied (never used)
         mbar_expect_tx(&full[sl], static_cast<uint32_t>(nqc) * qbytes);
-        uint8_t* dst = smem + static_cast<size_t>(sl) * p.chunk_bytes;
+        uint8_t* dst = smem + p.slot_off + static_cast<size_t>(sl) * p.chunk_bytes;
         for (int k = 0; k < nqc; ++k)
           tma_load_2d(dst + static_cast<size_t>(k) * p.qpad, &tmW, &full[sl], (q0 + k) * (TQ_QUAD_BYTES / 4), r0);
         issued = c + 1;
@@ -211,14 +263,39 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
     return;
   }
 
+  // Pair table: word (b, l) at byte (32 b + l) * 4 holds the codes of index byte b.
+  for (int e = threadIdx.x; e < 256 * 32; e += CT) {
+    const int b = e >> 5;
+    const uint32_t lo = static_cast<uint32_t>(c_tq_centroids_milli[b & 15] + TQ_CODE_BIAS);
+    const uint32_t hi = static_cast<uint32_t>(c_tq_centroids_milli[b >> 4] + TQ_CODE_BIAS);
+    reinterpret_cast<uint32_t*>(smem)[e] = lo | (hi << 16);
+  }
+
   asm volatile("griddepcontrol.wait;" ::: "memory");  // x may come from the previous kernel
 
-  // Rotated activations: block b -> xr[(b / 4) * 132 + (b % 4) * 32 ...].
+  // x -> xr, a warp per 512-byte quad (coalesced), then each 32-block rotated
+  // in place: block b sits at xr[(b / 4) * 132 + (b % 4) * 32 ...].
+  for (int q0 = warp; q0 < p.nq; q0 += 8 * NW) {  // up to eight loads in flight per lane
+    float4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int q = q0 + i * NW;
+      if (q < p.nq) v[i] = __ldg(reinterpret_cast<const float4*>(p.x) + static_cast<size_t>(q) * 32 + lane);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int q = q0 + i * NW;
+      if (q < p.nq) *reinterpret_cast<float4*>(xr + q * TQ_XR_QUAD + 4 * lane) = v[i];
+    }
+  }
+  asm volatile("bar.sync 1, %0;" ::"r"(CT) : "memory");
   const int nbt = p.nq * TQ_QUAD;
   for (int b = threadIdx.x; b < nbt; b += CT) {
+    float* blk = xr + (b >> 2) * TQ_XR_QUAD + (b & 3) * TQ_BLOCK;
     float v[TQ_BLOCK];
-    load_rotate(p.x, b, v);
-    store_block(xr + (b >> 2) * TQ_XR_QUAD + (b & 3) * TQ_BLOCK, v);
+    load_block(blk, v);
+    wht32(v);
+    store_block(blk, v);
   }
   asm volatile("bar.sync 1, %0;" ::"r"(CT) : "memory");
 
@@ -245,7 +322,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
     const int q = c * p.Qc + ql;  // quad within the row
     const bool valid = q < p.nq;
     const int qx = valid ? q : p.nq - 1;  // past the row end: read a valid quad, drop the result
-    const uint4* wq = reinterpret_cast<const uint4*>(smem + static_cast<size_t>(sl) * p.chunk_bytes +
+    const uint4* wq = reinterpret_cast<const uint4*>(smem + p.slot_off + static_cast<size_t>(sl) * p.chunk_bytes +
                                                      static_cast<size_t>(ql) * p.qpad + row * TQ_QUAD_BYTES);
     const uint4 u0 = wq[0], u1 = wq[1], u2 = wq[2], u3 = wq[3], u4 = wq[4];
     // block 0: words 0..4, block 1: 5..9, block 2: 10..14, block 3: 15..19
@@ -254,10 +331,11 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
     const uint32_t qc[4] = {u2.w, u3.x, u3.y, u3.z};
     const uint32_t qd[4] = {u4.x, u4.y, u4.z, u4.w};
     const float* xq = xr + qx * TQ_XR_QUAD;
-    float v = block_dot(u0.x, qa, xq, lut);
-    v += block_dot(u1.y, qb, xq + TQ_BLOCK, lut);
-    v += block_dot(u2.z, qc, xq + 2 * TQ_BLOCK, lut);
-    v += block_dot(u3.w, qd, xq + 3 * TQ_BLOCK, lut);
+    const uint32_t laneoff = static_cast<uint32_t>(lane) * 4u;
+    float v = block_dot_pairs(u0.x, qa, xq, tbl, laneoff);
+    v += block_dot_pairs(u1.y, qb, xq + TQ_BLOCK, tbl, laneoff);
+    v += block_dot_pairs(u2.z, qc, xq + 2 * TQ_BLOCK, tbl, laneoff);
+    v += block_dot_pairs(u3.w, qd, xq + 3 * TQ_BLOCK, tbl, laneoff);
     v = valid ? v : 0.f;
 #pragma unroll
     for (int k = 0; k < 4; ++k) acc[k] += (g == k) ? v : 0.f;
@@ -284,8 +362,9 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
 __global__ void __launch_bounds__(TQD_WARPS * 32) tq4_direct_kernel(const uint8_t* __restrict__ W,
                                                                     const float* __restrict__ x, float* __restrict__ y,
                                                                     int M, int nbt) {
-  extern __shared__ __align__(128) float xs[];  // [seg][32] rotated activations of the segment, then the table
-  float* lut = xs + min(nbt, TQD_SEG) * TQ_BLOCK;  // 128-byte aligned
+  extern __shared__ __align__(128) float tq_direct_smem[];  // the table (32 floats reserved), then the segment
+  float* lut = tq_direct_smem;
+  float* xs = tq_direct_smem + 32;  // [seg][32] rotated activations of the segment
   pdl_enter();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * TQD_WARPS + warp;
@@ -352,7 +431,7 @@ bool plan_tq_lanerow(int64_t M, int64_t K, int num_sms, TqLaneRowParams* p, int*
   p->n_chunks = (nq + p->Qc - 1) / p->Qc;
   const int xr_bytes = round_up_i(nq * TQ_XR_QUAD * 4, 128);
   const int part_bytes = TQ_NW * p->n_groups * 32 * 4;
-  const size_t fixed = static_cast<size_t>(xr_bytes) + part_bytes + 128 + 16;
+  const size_t fixed = static_cast<size_t>(xr_bytes) + part_bytes + TQ_PAIR_TABLE_BYTES + 16;
   if (fixed + p->chunk_bytes + 16 > static_cast<size_t>(TQ_SMEM_LIMIT)) return false;
   const int S = static_cast<int>((TQ_SMEM_LIMIT - fixed) / (p->chunk_bytes + 16));
   p->S = std::min(S, p->n_chunks);
@@ -362,13 +441,13 @@ bool plan_tq_lanerow(int64_t M, int64_t K, int num_sms, TqLaneRowParams* p, int*
   p->inv_per_chunk = per_chunk >= 2 ? recip32(per_chunk) : 0u;
   p->inv_steps = p->steps >= 2 ? recip32(p->steps) : 0u;
   p->inv_R = p->R >= 2 ? recip32(p->R) : 0u;
-  size_t off = static_cast<size_t>(p->S) * p->chunk_bytes;
+  size_t off = TQ_PAIR_TABLE_BYTES;  // the pair table
+  p->slot_off = static_cast<int>(off);
+  off += static_cast<size_t>(p->S) * p->chunk_bytes;
   p->xr_off = static_cast<int>(off);
   off += xr_bytes;
   p->part_off = static_cast<int>(off);
   off += part_bytes;
-  p->lut_off = static_cast<int>(off);  // part_bytes is a multiple of 128
-  off += 128;
   p->bar_off = static_cast<int>(off);
   off += static_cast<size_t>(2 * p->S) * sizeof(uint64_t) + 16;  // + abort, chunks issued
   *smem = off;
@@ -400,7 +479,7 @@ cudaError_t launch_tq4_matvec(const void* W, const float* x, float* y, int64_t M
     return launch_pdl(tq4_lanerow_kernel<TQ_NW>, dim3(grid), dim3((TQ_NW + 1) * 32), smem, s, tmW, lp);
   }
   const int nbt = static_cast<int>(K / TQ_BLOCK);
-  const size_t dsmem = static_cast<size_t>(std::min(nbt, TQD_SEG)) * TQ_BLOCK * sizeof(float) + 16 * sizeof(float);
+  const size_t dsmem = static_cast<size_t>(std::min(nbt, TQD_SEG) + 1) * TQ_BLOCK * sizeof(float);
   const int64_t blocks = (M + TQD_WARPS - 1) / TQD_WARPS;
   cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(tq4_direct_kernel), 25);
   if (e != cudaSuccess) return e;
