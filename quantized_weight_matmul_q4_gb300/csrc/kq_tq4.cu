@@ -58,7 +58,7 @@ constexpr int TQD_SEG = 512;           // blocks of x rotated per pass of the fa
 constexpr float TQ_INV_SQRT32 = 0.17677669529663688f;
 constexpr int TQ_CODE_BIAS = 4096;              // pair-table codes are 1000 * centroid + 4096 (13 bits)
 constexpr float TQ_MAGIC = 8388608.0f + 4096.0f;  // float bits 0x4B000000 | code equal 2^23 + code
-constexpr int TQ_PAIR_TABLE_BYTES = 256 * 32 * 4;  // a word per index byte, one copy per lane
+constexpr int TQ_PAIR_TABLE_BYTES = 256 * 64 * 4;  // a word per index byte and lane, rows of 256 bytes
 
 // Lloyd-Max centroids of N(0, 1), index order, as printed on the page, and
 // the same values times 1000 (integers, since the page prints three decimals).
@@ -145,15 +145,17 @@ __device__ __forceinline__ float block_dot(uint32_t dw, const uint32_t (&q)[4], 
   return fmaf(d1, s[1].x + s[1].y, d0 * (s[0].x + s[0].y));
 }
 
-// The same dot product with the pair table: word (b, lane) of `tbl` holds the
-// codes of both centroids of index byte b, 1000 c[b & 15] + 4096 in its low half
-// and 1000 c[b >> 4] + 4096 in its high half. Each lane reads its own copy
-// (bank = lane), so the 32 lanes never conflict, and one 4-byte read serves two
-// elements. A code placed in the mantissa of 2^23 (one byte permute) minus
-// 2^23 + 4096 gives 1000 c exactly in fp32; the half-block scales carry the
-// 1/1000.
-__device__ __forceinline__ float block_dot_pairs(uint32_t dw, const uint32_t (&q)[4], const float* xr,
-                                                 const uint8_t* tbl, uint32_t laneoff) {
+// The same dot product with the pair table, added into acc: word (b, lane) of
+// `tbl`, at byte 256 b + 4 lane, holds the codes of both centroids of index
+// byte b, 1000 c[b & 15] + 4096 in its low half and 1000 c[b >> 4] + 4096 in its
+// high half. Each lane reads its own copy (bank = lane), so the 32 lanes never
+// conflict, one 4-byte read serves two elements, and one byte permute of the
+// index word and the lane's offset forms the address. A code placed in the
+// mantissa of 2^23 minus 2^23 + 4096 gives 1000 c exactly in fp32. acc gets
+// d0 * (r . x) over elements 0..15 plus d1 * (r . x) over 16..31 (as an even /
+// odd pair), with the table's factor 1000 left in.
+__device__ __forceinline__ void block_dot_pairs(uint32_t dw, const uint32_t (&q)[4], const float* xr,
+                                                const uint8_t* tbl, uint32_t laneoff, float2& acc) {
   const float4* x4 = reinterpret_cast<const float4*>(xr);
   const float2 neg_magic = make_float2(-TQ_MAGIC, -TQ_MAGIC);
   float2 s[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // per half block: even / odd elements
@@ -164,8 +166,7 @@ __device__ __forceinline__ float block_dot_pairs(uint32_t dw, const uint32_t (&q
     float2 a = s[k >> 1];
 #pragma unroll
     for (int m = 0; m < 4; ++m) {  // byte m: elements 8k + 2m (low nibble) and 8k + 2m + 1
-      const uint32_t b = __byte_perm(w, 0u, 0x4440u + m);
-      const uint32_t t = *reinterpret_cast<const uint32_t*>(tbl + b * 128u + laneoff);
+      const uint32_t t = *reinterpret_cast<const uint32_t*>(tbl + __byte_perm(w, laneoff, 0x5504u + 16u * m));
       const float2 f = make_float2(__uint_as_float(__byte_perm(t, 0x4B000000u, 0x7610u)),
                                    __uint_as_float(__byte_perm(t, 0x4B000000u, 0x7632u)));
       const float2 c = __fadd2_rn(f, neg_magic);  // exact: 1000 * centroid
@@ -177,9 +178,9 @@ __device__ __forceinline__ float block_dot_pairs(uint32_t dw, const uint32_t (&q
     }
     s[k >> 1] = a;
   }
-  const float d0 = __half2float(__ushort_as_half(static_cast<unsigned short>(dw & 0xFFFFu))) * 0.001f;
-  const float d1 = __half2float(__ushort_as_half(static_cast<unsigned short>(dw >> 16))) * 0.001f;
-  return fmaf(d1, s[1].x + s[1].y, d0 * (s[0].x + s[0].y));
+  const float2 d = __half22float2(*reinterpret_cast<const __half2*>(&dw));
+  acc = __ffma2_rn(s[0], make_float2(d.x, d.x), acc);
+  acc = __ffma2_rn(s[1], make_float2(d.y, d.y), acc);
 }
 
 // i / d for d >= 1, with inv = ceil(2^32 / d) when d >= 2 (exact while i * d < 2^32).
@@ -263,12 +264,13 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
     return;
   }
 
-  // Pair table: word (b, l) at byte (32 b + l) * 4 holds the codes of index byte b.
+  // Pair table: word (b, l) at byte 256 b + 4 l holds the codes of index byte b
+  // (the other half of each 256-byte row is unused).
   for (int e = threadIdx.x; e < 256 * 32; e += CT) {
     const int b = e >> 5;
     const uint32_t lo = static_cast<uint32_t>(c_tq_centroids_milli[b & 15] + TQ_CODE_BIAS);
     const uint32_t hi = static_cast<uint32_t>(c_tq_centroids_milli[b >> 4] + TQ_CODE_BIAS);
-    reinterpret_cast<uint32_t*>(smem)[e] = lo | (hi << 16);
+    reinterpret_cast<uint32_t*>(smem)[(b << 6) | (e & 31)] = lo | (hi << 16);
   }
 
   asm volatile("griddepcontrol.wait;" ::: "memory");  // x may come from the previous kernel
@@ -300,7 +302,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
   asm volatile("bar.sync 1, %0;" ::"r"(CT) : "memory");
 
   const int items = p.n_chunks * per_chunk;
-  int ready = -1, sl = 0;
+  int ready = -1, sl = -1, phase = 0;  // last chunk seen, its slot and the slot's fill parity
   float acc[4] = {0.f, 0.f, 0.f, 0.f};  // this warp's sums for lane groups 0..3
   for (int i = warp; i < items; i += NW) {
     // i = (c * n_groups + g) * steps + t
@@ -309,11 +311,15 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
     const int g = fdiv(rem, p.steps, p.inv_steps);
     const int t = rem - g * p.steps;
     if (c != ready) {
-      sl = c % p.S;
+      while (ready < c) {  // chunks only move forward: slot c % S, parity (c / S) & 1
+        ++ready;
+        if (++sl == p.S) {
+          sl = 0;
+          phase ^= 1;
+        }
+      }
       // chunk c issued first: the parity wait cannot take an older fill of the slot
-      if (!wait_counter_above(chunks_issued, c, abort, p.err) || !mbar_wait(&full[sl], (c / p.S) & 1, abort, p.err))
-        break;
-      ready = c;
+      if (!wait_counter_above(chunks_issued, c, abort, p.err) || !mbar_wait(&full[sl], phase, abort, p.err)) break;
     }
     const int pr = min(32 * g + lane, p.RF - 1);  // lanes past the last pair repeat it; their result is dropped
     const int s = fdiv(pr, p.R, p.inv_R);
@@ -332,10 +338,12 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
     const uint32_t qd[4] = {u4.x, u4.y, u4.z, u4.w};
     const float* xq = xr + qx * TQ_XR_QUAD;
     const uint32_t laneoff = static_cast<uint32_t>(lane) * 4u;
-    float v = block_dot_pairs(u0.x, qa, xq, tbl, laneoff);
-    v += block_dot_pairs(u1.y, qb, xq + TQ_BLOCK, tbl, laneoff);
-    v += block_dot_pairs(u2.z, qc, xq + 2 * TQ_BLOCK, tbl, laneoff);
-    v += block_dot_pairs(u3.w, qd, xq + 3 * TQ_BLOCK, tbl, laneoff);
+    float2 a2 = make_float2(0.f, 0.f);
+    block_dot_pairs(u0.x, qa, xq, tbl, laneoff, a2);
+    block_dot_pairs(u1.y, qb, xq + TQ_BLOCK, tbl, laneoff, a2);
+    block_dot_pairs(u2.z, qc, xq + 2 * TQ_BLOCK, tbl, laneoff, a2);
+    block_dot_pairs(u3.w, qd, xq + 3 * TQ_BLOCK, tbl, laneoff, a2);
+    float v = a2.x + a2.y;
     v = valid ? v : 0.f;
 #pragma unroll
     for (int k = 0; k < 4; ++k) acc[k] += (g == k) ? v : 0.f;
@@ -354,7 +362,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
         const int pidx = s * p.R + r;
         a += part[(w * p.n_groups + (pidx >> 5)) * 32 + (pidx & 31)];
       }
-    p.y[r0 + r] = a * TQ_INV_SQRT32;
+    p.y[r0 + r] = a * (0.001f * TQ_INV_SQRT32);  // the pair table's codes are 1000 c
   }
 }
 
