@@ -32,10 +32,11 @@ Sources (page title, section):
         back" to the tokens).
 
 Where the pages leave a step open, the reading taken is stated at the function.
-The two bit layouts the pages elide (the Q4_K 6-bit scale/min packing and the
-Q6_K ql/qh bit arrangement) follow the GGUF k-quant layout; their agreement
-with GGUF files is "parity unpinned" (no GGUF file is available to check
-against); every other function here is pinned by ``tests/test_oracle_pins.py``.
+The bit layouts the pages elide (the Q4_K 6-bit scale/min packing, the Q6_K
+ql/qh bit arrangement and the whole Q5_K block) follow the GGUF k-quant
+layout; their agreement with GGUF files is "parity unpinned" (no GGUF file is
+available to check against); every other function here is pinned by
+``tests/test_oracle_pins.py``.
 """
 from __future__ import annotations
 
@@ -44,6 +45,7 @@ import numpy as np
 QK_K = 256
 Q4_K_BYTES = 144
 Q6_K_BYTES = 210
+Q5_K_BYTES = 176
 QK8_1 = 32
 Q8_1_BYTES = 36
 
@@ -173,7 +175,52 @@ def q6_k_dequant(W: np.ndarray, K: int) -> np.ndarray:
     return w.reshape(M, K)
 
 
+# ----------------------------------------------------------------------------
+# Q5_K
+# ----------------------------------------------------------------------------
+def q5_k_fields(blocks: np.ndarray):
+    """Decode Q5_K super-blocks.
+
+    The pages name Q5_K only as a sibling of the Q4_K and Q6_K decode kernels,
+    with its own unpacking and no layout ([MMVQ] §3.2 "one kernel per type";
+    the Q4_K value d·s·nib − dm·m of §2 with a fifth bit). The reading taken is
+    the GGUF Q5_K block, 176 bytes: fp16 d at byte 0, fp16 dmin at byte 2, the
+    Q4_K 6-bit scale/min packing at bytes 4..15, ``qh[32]`` at byte 16,
+    ``qs[128]`` at byte 48. Sub-block j (32 weights) takes its low four bits
+    like Q4_K (low nibbles of ``qs[32*(j>>1) : +32]`` for even j, high nibbles
+    for odd j) and weight r of the sub-block its fifth bit from bit j of
+    ``qh[r]``. Agreement with GGUF files is parity unpinned (no file here).
+
+    Returns (d [...], dmin [...], sc [..., 8], m [..., 8], q [..., 8, 32]), q in [0, 31].
+    """
+    blocks = np.asarray(blocks, dtype=np.uint8)
+    d = fp16_to_f64(blocks[..., 0:2].copy().view(np.uint16)[..., 0])
+    dmin = fp16_to_f64(blocks[..., 2:4].copy().view(np.uint16)[..., 0])
+    sc, m = q4_k_scale_min(blocks[..., 4:16])
+    qh = blocks[..., 16:48].astype(np.int64)
+    qs = blocks[..., 48:176].astype(np.int64)
+    q = np.empty(blocks.shape[:-1] + (8, 32), dtype=np.int64)
+    for j in range(8):
+        chunk = qs[..., 32 * (j >> 1): 32 * (j >> 1) + 32]
+        low = (chunk & 15) if j % 2 == 0 else (chunk >> 4)
+        q[..., j, :] = low | (((qh >> j) & 1) << 4)
+    return d, dmin, sc, m, q
+
+
+def q5_k_dequant(W: np.ndarray, K: int) -> np.ndarray:
+    """Dequantise a row-major Q5_K matrix to fp64 [M, K]: d*sc*q - dmin*m."""
+    W = np.asarray(W, dtype=np.uint8)
+    M = W.shape[0]
+    nb = K // QK_K
+    d, dmin, sc, m, q = q5_k_fields(W.reshape(M, nb, Q5_K_BYTES))
+    w = (d[..., None, None] * sc[..., None] * q
+         - (dmin[..., None] * m)[..., None])
+    return w.reshape(M, K)
+
+
 def dequant(wtype: str, W: np.ndarray, K: int) -> np.ndarray:
+    if wtype == "q5_k":
+        return q5_k_dequant(W, K)
     if wtype == "q4_k":
         return q4_k_dequant(W, K)
     if wtype == "q6_k":

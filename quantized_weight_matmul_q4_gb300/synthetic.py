@@ -20,6 +20,11 @@ Distributions follow the workloads of the k-quant matmul pages:
   ``scales[16]`` uniform on [-64, 63] at byte 192 and fp16 ``d`` at byte 208
   (the generator bug described in "06 · 8e/8e②", §3.3 Pitfalls, put d at byte
   0; it sits at 208). ``d`` is drawn like the Q4_K ``d``.
+* Q5_K super-block (256 weights, 176 bytes; the GGUF layout, which the pages
+  do not give): fp16 ``d`` at byte 0 and ``dmin`` at byte 2 drawn like the Q4_K
+  ones, then 12 bytes of packed 6-bit scales/mins, ``qh[32]`` and ``qs[128]``;
+  every one of those fields is uniform over all its bits, so bytes 4..175 are
+  uniform random bytes.
 * TQ4_1S block (32 weights, 20 bytes; "TQ4_1S Weight Kernel Optimization",
   Block Layout): fp16 ``d0`` at byte 0 and ``d1`` at byte 2, each drawn as
   0.02 * exp(0.25 * N(0, 1)) (positive half-block scales of the size of a
@@ -38,6 +43,7 @@ import numpy as np
 QK_K = 256            # weights per k-quant super-block
 Q4_K_BYTES = 144      # bytes per Q4_K super-block
 Q6_K_BYTES = 210      # bytes per Q6_K super-block
+Q5_K_BYTES = 176      # bytes per Q5_K super-block
 Q8_1_BYTES = 36       # bytes per 32-element Q8_1 activation block
 QK_TQ = 32            # weights per TQ4_1S block
 TQ4_1S_BYTES = 20     # bytes per TQ4_1S block
@@ -96,7 +102,22 @@ def tq4_1s_weights(rng: np.random.Generator, M: int, K: int) -> np.ndarray:
     return w.reshape(M, nb * TQ4_1S_BYTES)
 
 
+def q5_k_weights(rng: np.random.Generator, M: int, K: int) -> np.ndarray:
+    """Random Q5_K matrix: uint8 array of shape [M, (K/256)*176], row-major."""
+    if K % QK_K:
+        raise ValueError("K must be a multiple of 256")
+    nb = K // QK_K
+    w = rng.integers(0, 256, size=(M, nb, Q5_K_BYTES), dtype=np.uint8)
+    d = _fp16_abs_normal(rng, (M, nb))
+    dmin = _fp16_abs_normal(rng, (M, nb))
+    w[:, :, 0:2] = d[..., None].view(np.uint8).reshape(M, nb, 2)
+    w[:, :, 2:4] = dmin[..., None].view(np.uint8).reshape(M, nb, 2)
+    return w.reshape(M, nb * Q5_K_BYTES)
+
+
 def weights(wtype: str, rng: np.random.Generator, M: int, K: int) -> np.ndarray:
+    if wtype == "q5_k":
+        return q5_k_weights(rng, M, K)
     if wtype == "tq4_1s":
         return tq4_1s_weights(rng, M, K)
     if wtype == "q4_k":
@@ -130,6 +151,8 @@ WORKLOADS = {
     "matvec_q4k_512x2048": dict(kind="matvec", wtype="q4_k", M=512, K=2048, N=1, seed=0),
     "decode_q4k_4096x11008": dict(kind="matvec", wtype="q4_k", M=4096, K=11008, N=1, seed=1),
     "decode_q4k_11008x4096": dict(kind="matvec", wtype="q4_k", M=11008, K=4096, N=1, seed=1),
+    "decode_q5k_4096x11008": dict(kind="matvec", wtype="q5_k", M=4096, K=11008, N=1, seed=1),
+    "decode_q5k_11008x4096": dict(kind="matvec", wtype="q5_k", M=11008, K=4096, N=1, seed=1),
     "decode_q6k_4096x11008": dict(kind="matvec", wtype="q6_k", M=4096, K=11008, N=1, seed=1),
     "decode_q6k_11008x4096": dict(kind="matvec", wtype="q6_k", M=11008, K=4096, N=1, seed=1),
     "decode_tq4_1s_18944x3584": dict(kind="matvec", wtype="tq4_1s", M=18944, K=3584, N=1, seed=6),

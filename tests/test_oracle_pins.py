@@ -14,6 +14,7 @@ import numpy as np
 import pytest
 
 from oracle import kq_oracle as ora
+from quantized_weight_matmul_q4_gb300 import synthetic as syn
 
 
 # ----------------------------------------------------------------------------
@@ -285,10 +286,10 @@ def test_matmul_q6k_one_hot():
         assert Y[0, 0] == -127 * 2.0 * (k // 16 - 8) * (_q6k_code(k) - 32)
 
 
-@pytest.mark.parametrize("wtype", ["q4_k", "q6_k"])
+@pytest.mark.parametrize("wtype", ["q4_k", "q6_k", "q5_k"])
 def test_matmul_brute_force_tiny(wtype):
     M, N, K = 3, 4, 512
-    W = _q4k_random(11, M, K) if wtype == "q4_k" else _q6k_random(11, M, K)
+    W = syn.weights(wtype, np.random.default_rng(11), M, K)
     X = _rand_x(12, N, K)
     Y, B = ora.matmul(wtype, W, X, M, K)
     w = ora.dequant(wtype, W, K)
@@ -425,3 +426,59 @@ def test_moe_combine_equals_matmul_with_the_weighted_weights():
     for t in range(T):
         weff = sum(probs[t, j] * w[ids[t, j]] for j in range(top_k))
         assert np.allclose(out[t], weff @ xh[t], rtol=1e-12, atol=1e-12)
+
+
+# ----------------------------------------------------------------------------
+# Q5_K (GGUF layout, a reading: the pages give none): the Q4_K value with a
+# fifth bit, so it reduces to Q4_K exactly when every high bit is zero
+# ----------------------------------------------------------------------------
+def _q5k_from_q4k(q4: np.ndarray, qh: np.ndarray) -> np.ndarray:
+    """Q5_K blocks holding the fields of Q4_K blocks q4 [..., 144] and the high-bit bytes qh [..., 32]."""
+    out = np.zeros(q4.shape[:-1] + (176,), np.uint8)
+    out[..., 0:16] = q4[..., 0:16]
+    out[..., 16:48] = qh
+    out[..., 48:176] = q4[..., 16:144]
+    return out
+
+
+def test_q5k_with_zero_high_bits_is_q4k():
+    M, K = 5, 768
+    q4 = syn.q4_k_weights(np.random.default_rng(31), M, K).reshape(M, K // 256, 144)
+    q5 = _q5k_from_q4k(q4, np.zeros(q4.shape[:-1] + (32,), np.uint8)).reshape(M, -1)
+    assert np.array_equal(ora.q5_k_dequant(q5, K), ora.q4_k_dequant(q4.reshape(M, -1), K))
+
+
+def test_q5k_all_high_bits_add_16_d_sc():
+    M, K = 4, 512
+    q4 = syn.q4_k_weights(np.random.default_rng(32), M, K).reshape(M, K // 256, 144)
+    q5 = _q5k_from_q4k(q4, np.full(q4.shape[:-1] + (32,), 0xFF, np.uint8)).reshape(M, -1)
+    d, _, sc, _, _ = ora.q4_k_fields(q4)
+    extra = (16 * d[..., None, None] * sc[..., None] * np.ones(32)).reshape(M, K)
+    assert np.allclose(ora.q5_k_dequant(q5, K), ora.q4_k_dequant(q4.reshape(M, -1), K) + extra, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("j,r", [(0, 0), (1, 5), (4, 31), (7, 17)])
+def test_q5k_one_high_bit_moves_one_weight(j, r):
+    # bit j of qh[r] is the fifth bit of weight r of sub-block j, i.e. element 32 j + r
+    q4 = _q4k_block()
+    qh = np.zeros(32, np.uint8)
+    base = ora.q5_k_dequant(_q5k_from_q4k(q4, qh).reshape(1, 176), 256)[0]
+    qh[r] = 1 << j
+    moved = ora.q5_k_dequant(_q5k_from_q4k(q4, qh).reshape(1, 176), 256)[0]
+    diff = moved - base
+    want = np.zeros(256)
+    want[32 * j + r] = 16 * 1.0 * Q4K_SC[j]          # d = 1.0 in the hand block
+    assert np.array_equal(diff, want)
+
+
+def test_q5k_hand_block_closed_form():
+    # the Q4_K hand block with fifth bits (i + j) % 3 == 0
+    qh = np.zeros(32, np.uint8)
+    for i in range(32):
+        for j in range(8):
+            if (i + j) % 3 == 0:
+                qh[i] |= 1 << j
+    w = ora.q5_k_dequant(_q5k_from_q4k(_q4k_block(), qh).reshape(1, 176), 256)[0]
+    want = [1.0 * Q4K_SC[j] * (_q4k_nib(j, i) + (16 if (i + j) % 3 == 0 else 0)) - 0.5 * Q4K_M[j]
+            for j in range(8) for i in range(32)]
+    assert w.tolist() == want

@@ -35,6 +35,17 @@ def test_q6k_generator_fields_and_d_offset():
     assert not (0.005 < np.abs(lead[np.isfinite(lead)]).mean() < 0.011)
 
 
+def test_q5k_generator_fields():
+    W = syn.q5_k_weights(np.random.default_rng(4), 64, 512)
+    assert W.shape == (64, 2 * 176) and W.dtype == np.uint8
+    blk = W.reshape(64, 2, 176)
+    d = _f16(blk[..., 0:2]).ravel()
+    dmin = _f16(blk[..., 2:4]).ravel()
+    assert np.all(d >= 0) and np.all(dmin >= 0)
+    assert 0.005 < d.mean() < 0.011 and 0.005 < dmin.mean() < 0.011
+    assert len(np.unique(blk[..., 4:176])) == 256   # scales, qh, qs: uniform bytes
+
+
 def test_tq4_1s_generator_fields():
     W = syn.tq4_1s_weights(np.random.default_rng(3), 32, 4096)
     assert W.shape == (32, 128 * 20) and W.dtype == np.uint8
