@@ -417,6 +417,7 @@ def _timed_calls(fn, iters, warm, flush, torch, stream):
 DECODE_SECTIONS = {
     "decode_tq4_1s_18944x3584_3584x18944": (("decode_tq4_1s_18944x3584", "decode_tq4_1s_3584x18944"), 4),
     "decode_q6k_4096x11008_11008x4096": (("decode_q6k_4096x11008", "decode_q6k_11008x4096"), 4),
+    "decode_q5k_4096x11008_11008x4096": (("decode_q5k_4096x11008", "decode_q5k_11008x4096"), 4),
 }
 
 

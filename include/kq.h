@@ -3,7 +3,8 @@
  *
  *   Y[M, N] = dequant(W)[M, K] . X[K, N]
  *
- * W holds 4-bit Q4_K or 6-bit Q6_K super-blocks; X is fp32 and is quantised to
+ * W holds 4-bit Q4_K or 6-bit Q6_K super-blocks (5-bit Q5_K for the decode
+ * matvec); X is fp32 and is quantised to
  * Q8_1 (int8 codes with an fp16 scale per 32 values) inside every call. The
  * decode matvec also takes TQ4_1S weights (WHT-rotated 4-bit Lloyd-Max codes),
  * which it multiplies with the fp32 activations directly.
@@ -32,6 +33,9 @@
  *      W : M rows x (K/256) super-blocks; a Q4_K block is 144 bytes
  *          [fp16 d][fp16 dmin][12 B packed 6-bit scales/mins][128 B nibbles],
  *          a Q6_K block is 210 bytes [ql 128][qh 64][int8 scales 16][fp16 d].
+ *          Q5_K (the GGUF layout; the pages give none): 176 bytes [fp16 d][fp16 dmin]
+ *          [12 B scales/mins packed as Q4_K][qh 32][128 B nibbles], weight r of
+ *          sub-block j taking its fifth bit from bit j of qh[r].
  *          TQ4_1S: M rows x (K/32) blocks of 20 bytes [fp16 d0][fp16 d1][qs 16],
  *          element j's centroid index in qs[j/2], low nibble for even j.
  *          For MoE the experts' matrices are concatenated, expert-major.
@@ -81,9 +85,10 @@ typedef enum kq_status {
   KQ_ERR_DEVICE = 7     /* a kernel recorded an error; see kq_get_device_error */
 } kq_status;
 
-/* KQ_TQ4_1S is taken by kq_matvec only; the other entry points return
- * KQ_ERR_TYPE for it. */
-typedef enum kq_wtype { KQ_Q4_K = 1, KQ_Q6_K = 2, KQ_TQ4_1S = 3 } kq_wtype;
+/* KQ_Q5_K is taken by the decode matvecs (kq_matvec, kq_matvec_swiglu,
+ * kq_matvec_rmsnorm) and KQ_TQ4_1S by kq_matvec only; the other entry points
+ * return KQ_ERR_TYPE for them. */
+typedef enum kq_wtype { KQ_Q4_K = 1, KQ_Q6_K = 2, KQ_TQ4_1S = 3, KQ_Q5_K = 4 } kq_wtype;
 
 typedef enum kq_op { KQ_OP_MATVEC = 1, KQ_OP_GEMM = 2, KQ_OP_MOE = 3 } kq_op;
 
@@ -108,7 +113,9 @@ KQ_API kq_status kq_quantize_q8_1(const float* X, void* Xq, int64_t K, int64_t N
  * integer dot products of the 4/6-bit codes with the Q8_1 codes of x, the
  * min term from the Q8_1 block sum, warp-shuffle row reductions). x is
  * quantised to Q8_1 inside the call. Needs no workspace.
- * wtype: KQ_Q4_K or KQ_Q6_K. W: M rows of K/256 blocks; x: fp32 [K];
+ * wtype: KQ_Q4_K, KQ_Q6_K or KQ_Q5_K (the Q4_K value d*sc*q - dmin*m with a
+ * 5-bit q; the pages ship it as a sibling decode kernel). W: M rows of K/256
+ * blocks; x: fp32 [K];
  * y: fp32 [M], written.
  * Weight streaming starts before the kernel waits for the previous kernel on
  * the stream: W must not be written by a kernel that is still running when this

@@ -1,4 +1,4 @@
-"""kq — k-quant (Q4_K / Q6_K) and TQ4_1S weight matmul for NVIDIA GB300.
+"""kq — k-quant (Q4_K / Q5_K / Q6_K) and TQ4_1S weight matmul for NVIDIA GB300.
 
 Thin Python binding over the C ABI of libkq (include/kq.h): every function
 here only checks and marshals its arguments (device pointers, sizes, the
@@ -11,23 +11,23 @@ from __future__ import annotations
 import ctypes
 
 from ._native import (KQ_DEVERR_EXPERT_ID, KQ_DEVERR_NONE, KQ_DEVERR_WAIT_TIMEOUT, KQ_GEMM_STATIC_WS_BYTES,
-                      KQ_OP_GEMM, KQ_OP_MATVEC, KQ_OP_MOE, KQ_Q4_K, KQ_Q6_K, KQ_TQ4_1S, KQError, check, lib)
+                      KQ_OP_GEMM, KQ_OP_MATVEC, KQ_OP_MOE, KQ_Q4_K, KQ_Q5_K, KQ_Q6_K, KQ_TQ4_1S, KQError, check, lib)
 
 __all__ = [
-    "KQ_Q4_K", "KQ_Q6_K", "KQ_TQ4_1S", "KQ_OP_MATVEC", "KQ_OP_GEMM", "KQ_OP_MOE", "KQError",
+    "KQ_Q4_K", "KQ_Q5_K", "KQ_Q6_K", "KQ_TQ4_1S", "KQ_OP_MATVEC", "KQ_OP_GEMM", "KQ_OP_MOE", "KQError",
     "KQ_DEVERR_NONE", "KQ_DEVERR_WAIT_TIMEOUT", "KQ_DEVERR_EXPERT_ID",
     "KQ_GEMM_STATIC_WS_BYTES", "kq_quantize_q8_1", "kq_matvec", "kq_matvec_swiglu", "kq_matvec_rmsnorm",
     "kq_gemm", "kq_gemm_noalloc", "kq_moe_grouped_gemm", "kq_moe_combine", "kq_workspace_bytes",
     "kq_get_device_error", "block_bytes", "row_bytes",
 ]
 
-_BLOCK_BYTES = {KQ_Q4_K: 144, KQ_Q6_K: 210, KQ_TQ4_1S: 20}
-_BLOCK_WEIGHTS = {KQ_Q4_K: 256, KQ_Q6_K: 256, KQ_TQ4_1S: 32}
+_BLOCK_BYTES = {KQ_Q4_K: 144, KQ_Q5_K: 176, KQ_Q6_K: 210, KQ_TQ4_1S: 20}
+_BLOCK_WEIGHTS = {KQ_Q4_K: 256, KQ_Q5_K: 256, KQ_Q6_K: 256, KQ_TQ4_1S: 32}
 
 
 def _wt(wtype) -> int:
     if isinstance(wtype, str):
-        return {"q4_k": KQ_Q4_K, "q6_k": KQ_Q6_K, "tq4_1s": KQ_TQ4_1S}[wtype.lower()]
+        return {"q4_k": KQ_Q4_K, "q5_k": KQ_Q5_K, "q6_k": KQ_Q6_K, "tq4_1s": KQ_TQ4_1S}[wtype.lower()]
     return int(wtype)
 
 
@@ -74,7 +74,7 @@ def kq_quantize_q8_1(X, Xq=None, stream=None):
 
 
 def kq_matvec(wtype, W, x, M: int, K: int, y=None, stream=None):
-    """y[M] = dequant(W) . x; W uint8 [M, row_bytes], x fp32 [K] (wtype q4_k, q6_k or tq4_1s)."""
+    """y[M] = dequant(W) . x; W uint8 [M, row_bytes], x fp32 [K] (wtype q4_k, q5_k, q6_k or tq4_1s)."""
     torch = _torch()
     if y is None:
         y = torch.empty(M, dtype=torch.float32, device=x.device)

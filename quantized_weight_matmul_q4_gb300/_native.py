@@ -23,6 +23,7 @@ KQ_ERR_DEVICE = 7
 KQ_Q4_K = 1
 KQ_Q6_K = 2
 KQ_TQ4_1S = 3
+KQ_Q5_K = 4
 KQ_OP_MATVEC = 1
 KQ_OP_GEMM = 2
 KQ_OP_MOE = 3

@@ -52,7 +52,8 @@ int sm_count_or_default() {
 std::atomic<uint8_t> g_smem_set[kSmemSlots][kMaxDevices];
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-inline bool valid_wtype(int t) { return t == KQ_Q4_K || t == KQ_Q6_K; }
+inline bool valid_wtype(int t) { return t == KQ_Q4_K || t == KQ_Q6_K; }  // every entry point
+inline bool valid_matvec_wtype(int t) { return valid_wtype(t) || t == KQ_Q5_K; }  // the decode matvecs
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
 
 kq_status finish(cudaError_t e, int status) {
@@ -121,7 +122,7 @@ static kq_status matvec_entry(int wtype, const void* W, const float* x, const fl
     e = launch_tq4_matvec(W, x, y, M, K, err, sms, reinterpret_cast<cudaStream_t>(stream), &status);
     return finish(e, status);
   }
-  if (!valid_wtype(wtype)) return KQ_ERR_TYPE;
+  if (!valid_matvec_wtype(wtype)) return KQ_ERR_TYPE;
   if (!W || !x || !y || (prod != PROD_X && !aux)) return KQ_ERR_NULL;
   if (M <= 0 || K <= 0 || K % QK_K != 0 || M > kMaxDim || K > kMaxDim) return KQ_ERR_SHAPE;
   if (prod == PROD_RMSNORM && !(eps >= 0.f && eps < 1e30f)) return KQ_ERR_SHAPE;  // also rejects NaN

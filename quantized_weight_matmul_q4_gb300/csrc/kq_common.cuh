@@ -21,6 +21,7 @@ namespace kq {
 constexpr int QK_K = 256;          // weights per super-block
 constexpr int Q4K_BYTES = 144;     // fp16 d, fp16 dmin, 12 B scales, 128 B nibbles
 constexpr int Q6K_BYTES = 210;     // ql[128], qh[64], int8 scales[16], fp16 d @208
+constexpr int Q5K_BYTES = 176;     // fp16 d, fp16 dmin, 12 B scales, qh[32] @16, 128 B nibbles @48
 constexpr int QK8_1 = 32;          // activations per Q8_1 block
 constexpr int Q8_1_BYTES = 36;     // fp16 d, fp16 s, int8 q[32]
 

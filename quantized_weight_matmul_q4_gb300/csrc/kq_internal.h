@@ -75,7 +75,7 @@ cudaError_t device_context(int* dev, int* num_sms, int** err);
 // Raises a kernel's dynamic shared-memory limit to the 227 KB maximum, once per
 // device (later calls only read a flag, so launches stay cheap and capturable).
 cudaError_t allow_max_smem(const void* kernel, int slot);
-constexpr int kSmemSlots = 26;
+constexpr int kSmemSlots = 35;
 
 // Launches `kernel` on `s` with programmatic stream serialization allowed (the
 // kernel calls pdl_enter() before its first global memory access).

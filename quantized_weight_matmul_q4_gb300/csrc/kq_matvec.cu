@@ -31,6 +31,7 @@ constexpr int MV_SMEM_LIMIT = 227 * 1024;
 constexpr int MV_PART_MAX = 4096;                   // block partials per row group
 constexpr int MV_CHUNK_BLOCKS_Q4K = 112;            // 16128 B per chunk
 constexpr int MV_CHUNK_BLOCKS_Q6K = 80;             // 16800 B per chunk
+constexpr int MV_CHUNK_BLOCKS_Q5K = 92;             // 16192 B per chunk
 constexpr int MV_MAX_RING = 14;
 
 struct MatvecParams {
@@ -162,6 +163,84 @@ __device__ __forceinline__ float block_dot_q4k(const uint8_t* __restrict__ blk, 
   return d * fmaf(acc_hi, 0.0625f, acc_lo) - dmin * acc_m;
 }
 
+// Q5_K codes of four weights: the low (LO) or high nibbles of the four qs
+// bytes in w, with the fifth bit, bit `BIT` of the matching qh bytes in h,
+// moved to bit 4 of each byte (the Q5_K block: the Q4_K fields with qh[32] at
+// byte 16 and the nibbles at byte 48; weight r of sub-block j has its fifth
+// bit in bit j of qh[r]).
+template <bool LO, int BIT>
+__device__ __forceinline__ int q5_codes(uint32_t w, uint32_t h) {
+  const uint32_t hb = (BIT <= 4 ? (h << (4 - BIT)) : (h >> (BIT - 4))) & 0x10101010u;
+  return static_cast<int>(((LO ? w : (w >> 4)) & 0x0F0F0F0Fu) | hb);
+}
+
+// Integer dots of one 64-weight chunk of a Q5_K block: sub-block J (low
+// nibbles, against x0 | x1) into dA and sub-block J + 1 (high nibbles, against
+// x2 | x3) into dB. qa, qb: the chunk's 32 nibble bytes; ha, hb: qh[0..15] and
+// qh[16..31].
+template <int J>
+__device__ __forceinline__ void q5_chunk_dots(const uint4& qa, const uint4& qb, const uint4& ha, const uint4& hb,
+                                              const int4& x0, const int4& x1, const int4& x2, const int4& x3, int& dA,
+                                              int& dB) {
+  dA = __dp4a(q5_codes<true, J>(qa.x, ha.x), x0.x, 0);
+  dA = __dp4a(q5_codes<true, J>(qa.y, ha.y), x0.y, dA);
+  dA = __dp4a(q5_codes<true, J>(qa.z, ha.z), x0.z, dA);
+  dA = __dp4a(q5_codes<true, J>(qa.w, ha.w), x0.w, dA);
+  dA = __dp4a(q5_codes<true, J>(qb.x, hb.x), x1.x, dA);
+  dA = __dp4a(q5_codes<true, J>(qb.y, hb.y), x1.y, dA);
+  dA = __dp4a(q5_codes<true, J>(qb.z, hb.z), x1.z, dA);
+  dA = __dp4a(q5_codes<true, J>(qb.w, hb.w), x1.w, dA);
+  dB = __dp4a(q5_codes<false, J + 1>(qa.x, ha.x), x2.x, 0);
+  dB = __dp4a(q5_codes<false, J + 1>(qa.y, ha.y), x2.y, dB);
+  dB = __dp4a(q5_codes<false, J + 1>(qa.z, ha.z), x2.z, dB);
+  dB = __dp4a(q5_codes<false, J + 1>(qa.w, ha.w), x2.w, dB);
+  dB = __dp4a(q5_codes<false, J + 1>(qb.x, hb.x), x3.x, dB);
+  dB = __dp4a(q5_codes<false, J + 1>(qb.y, hb.y), x3.y, dB);
+  dB = __dp4a(q5_codes<false, J + 1>(qb.z, hb.z), x3.z, dB);
+  dB = __dp4a(q5_codes<false, J + 1>(qb.w, hb.w), x3.w, dB);
+}
+
+// Sum over one Q5_K super-block of w * x_hat, w = d * sc * q - dmin * m with q
+// the 5-bit code: the Q4_K form with the codes built by q5_codes.
+__device__ __forceinline__ float block_dot_q5k(const uint8_t* __restrict__ blk, int b, const uint8_t* __restrict__ xq,
+                                               const int4* __restrict__ xds) {
+  const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
+  const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x & 0xFFFFu)));
+  const float dmin = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x >> 16)));
+  const uint32_t sc_lo = hdr.y & 0x3F3F3F3Fu, m_lo = hdr.z & 0x3F3F3F3Fu;
+  const uint32_t sc_hi = (hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u);
+  const uint32_t m_hi = ((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u);
+  const uint4 ha = *reinterpret_cast<const uint4*>(blk + 16);  // qh[0..15]
+  const uint4 hb = *reinterpret_cast<const uint4*>(blk + 32);  // qh[16..31]
+  float acc = 0.f, acc_m = 0.f;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint4 qa = *reinterpret_cast<const uint4*>(blk + 48 + 32 * c);
+    const uint4 qb = *reinterpret_cast<const uint4*>(blk + 64 + 32 * c);
+    const int4 x0 = *reinterpret_cast<const int4*>(xq + xq_piece(b, 4 * c + 0));
+    const int4 x1 = *reinterpret_cast<const int4*>(xq + xq_piece(b, 4 * c + 1));
+    const int4 x2 = *reinterpret_cast<const int4*>(xq + xq_piece(b, 4 * c + 2));
+    const int4 x3 = *reinterpret_cast<const int4*>(xq + xq_piece(b, 4 * c + 3));
+    const int4 ds = xds[xds_q4k(b, c)];
+    int dA, dB;
+    if (c == 0) q5_chunk_dots<0>(qa, qb, ha, hb, x0, x1, x2, x3, dA, dB);
+    else if (c == 1) q5_chunk_dots<2>(qa, qb, ha, hb, x0, x1, x2, x3, dA, dB);
+    else if (c == 2) q5_chunk_dots<4>(qa, qb, ha, hb, x0, x1, x2, x3, dA, dB);
+    else q5_chunk_dots<6>(qa, qb, ha, hb, x0, x1, x2, x3, dA, dB);
+    const uint32_t scw = (c < 2) ? sc_lo : sc_hi;
+    const uint32_t mw = (c < 2) ? m_lo : m_hi;
+    const int sh = (c & 1) * 16;
+    const int scA = (scw >> sh) & 0xFF, scB = (scw >> (sh + 8)) & 0xFF;
+    const int mA = (mw >> sh) & 0xFF, mB = (mw >> (sh + 8)) & 0xFF;
+    const float d8A = __int_as_float(ds.x), d8B = __int_as_float(ds.y);
+    acc = fmaf(d8A, i2f(scA * dA), acc);
+    acc = fmaf(d8B, i2f(scB * dB), acc);
+    acc_m = fmaf(d8A, i2f(mA * ds.z), acc_m);
+    acc_m = fmaf(d8B, i2f(mB * ds.w), acc_m);
+  }
+  return d * acc - dmin * acc_m;
+}
+
 // Four bytes from a 2-byte aligned shared address, as one 32-bit word.
 __device__ __forceinline__ uint32_t ld_u32_a2(const uint8_t* p) {
   const uint16_t* q = reinterpret_cast<const uint16_t*>(p);
@@ -290,7 +369,7 @@ __global__ void __launch_bounds__(MV_THREADS, 1) matvec_kernel(const MatvecParam
         *reinterpret_cast<uint32_t*>(xq + xq_piece(b, j) + (k & 15)) = pack_q4(r.q);
         if ((qd & 7) == 0) {
           const int g8 = (k >> 5) & 7;
-          if (WT == KQ_Q4_K) {
+          if (WT != KQ_Q6_K) {  // Q4_K and Q5_K share the sub-block layout
             int* e = reinterpret_cast<int*>(&xds[xds_q4k(b, g8 >> 1)]);
             e[g8 & 1] = __float_as_int(r.dh);
             e[2 + (g8 & 1)] = r.sumq;
@@ -320,7 +399,9 @@ __global__ void __launch_bounds__(MV_THREADS, 1) matvec_kernel(const MatvecParam
       const uint8_t* blk = ring + static_cast<size_t>(slot) * p.slot_bytes +
                            static_cast<size_t>(it - c * p.chunk_blocks) * p.bb;
       const int b = it % p.nb;
-      part[it - g0] = (WT == KQ_Q4_K) ? block_dot_q4k(blk, b, xq, xds) : block_dot_q6k(blk, b, xq, xds);
+      part[it - g0] = (WT == KQ_Q4_K)   ? block_dot_q4k(blk, b, xq, xds)
+                      : (WT == KQ_Q5_K) ? block_dot_q5k(blk, b, xq, xds)
+                                        : block_dot_q6k(blk, b, xq, xds);
       mbar_arrive(&empty[slot]);
     }
     (void)ok;
@@ -396,9 +477,11 @@ struct MatvecLaneRowParams {
   int* err;
 };
 
-template <int NW, bool RING, int PROD>
+template <int NW, bool RING, int PROD, int WT = KQ_Q4_K>
 __global__ void __launch_bounds__((NW + 1) * 32, RING ? 2 : 1)
     matvec_q4k_lanerow_kernel(const __grid_constant__ CUtensorMap tmW, const MatvecLaneRowParams p) {
+  static_assert(WT == KQ_Q4_K || WT == KQ_Q5_K, "Q4_K or Q5_K super-blocks");
+  constexpr int BB = (WT == KQ_Q5_K) ? Q5K_BYTES : Q4K_BYTES;  // bytes per super-block
   constexpr int LR_CT = NW * 32;
   extern __shared__ __align__(1024) uint8_t smem[];
   int8_t* xq = reinterpret_cast<int8_t*>(smem + p.xq_off);
@@ -429,11 +512,11 @@ __global__ void __launch_bounds__((NW + 1) * 32, RING ? 2 : 1)
   if (warp == NW) {
     if (lane == 0) {
       tma_prefetch_desc(&tmW);
-      const uint32_t box = static_cast<uint32_t>(p.R * p.cb * Q4K_BYTES);
+      const uint32_t box = static_cast<uint32_t>(p.R * p.cb * BB);
       if (!RING) {
         for (int c = 0; c < p.n_chunks; ++c) {
           mbar_expect_tx(&full[c], box);
-          tma_load_2d(smem + static_cast<size_t>(c) * p.chunk_bytes, &tmW, &full[c], c * p.cb * (Q4K_BYTES / 4), r0);
+          tma_load_2d(smem + static_cast<size_t>(c) * p.chunk_bytes, &tmW, &full[c], c * p.cb * (BB / 4), r0);
         }
         // Every copy lands before the CTA may exit (also when the consumers gave up).
         for (int c = 0; c < p.n_chunks; ++c)
@@ -444,8 +527,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, RING ? 2 : 1)
           const int sl = c % p.S;
           if (c >= p.S && !mbar_wait(&empty[sl], ((c / p.S) - 1) & 1, abort, p.err)) break;
           mbar_expect_tx(&full[sl], box);
-          tma_load_2d(smem + static_cast<size_t>(sl) * p.chunk_bytes, &tmW, &full[sl], c * p.cb * (Q4K_BYTES / 4),
-                      r0);
+          tma_load_2d(smem + static_cast<size_t>(sl) * p.chunk_bytes, &tmW, &full[sl], c * p.cb * (BB / 4), r0);
           issued = c + 1;
           *chunks_issued = issued;
         }
@@ -491,7 +573,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, RING ? 2 : 1)
   asm volatile("bar.sync 1, %0;" ::"r"(LR_CT) : "memory");
 
   const float4* xs4 = reinterpret_cast<const float4*>(xs);
-  const int pitch = p.cb * Q4K_BYTES;
+  const int pitch = p.cb * BB;
   const int items = p.n_chunks * per_chunk;
   int ready = -1, sl = 0;  // last chunk this warp has seen land, and its slot
   float acc[4] = {0.f, 0.f, 0.f, 0.f};  // this warp's sums for row groups 0..3
@@ -525,7 +607,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, RING ? 2 : 1)
     }
     const int row = 32 * g + lane;
     const int srow = min(row, p.R - 1);  // lanes past the last row repeat it; their result is dropped
-    const uint8_t* blk = smem + static_cast<size_t>(sl) * p.chunk_bytes + srow * pitch + j * Q4K_BYTES;
+    const uint8_t* blk = smem + static_cast<size_t>(sl) * p.chunk_bytes + srow * pitch + j * BB;
     const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
     const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x & 0xFFFFu)));
     const float dmin = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x >> 16)));
@@ -535,16 +617,39 @@ __global__ void __launch_bounds__((NW + 1) * 32, RING ? 2 : 1)
     const uint32_t m_hi = ((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u);
     const int8_t* xb = xq + (b << 8);
     float lo = 0.f, mn = 0.f;
+    uint4 ha, hb;  // Q5_K: qh[0..15], qh[16..31]
+    if (WT == KQ_Q5_K) {
+      ha = *reinterpret_cast<const uint4*>(blk + 16);
+      hb = *reinterpret_cast<const uint4*>(blk + 32);
+    }
+    constexpr int QS = (WT == KQ_Q5_K) ? 48 : 16;  // byte offset of the nibbles
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       // bytes 32q .. 32q+31 of the nibbles: low nibbles are sub-block 2q, high nibbles 2q+1
-      const uint4 qa = *reinterpret_cast<const uint4*>(blk + 16 + 32 * q);
-      const uint4 qb = *reinterpret_cast<const uint4*>(blk + 32 + 32 * q);
+      const uint4 qa = *reinterpret_cast<const uint4*>(blk + QS + 32 * q);
+      const uint4 qb = *reinterpret_cast<const uint4*>(blk + QS + 16 + 32 * q);
       const int4 x0 = *reinterpret_cast<const int4*>(xb + 64 * q);
       const int4 x1 = *reinterpret_cast<const int4*>(xb + 64 * q + 16);
       const int4 x2 = *reinterpret_cast<const int4*>(xb + 64 * q + 32);
       const int4 x3 = *reinterpret_cast<const int4*>(xb + 64 * q + 48);
       const float4 ds = xs4[(b << 2) + q];  // {d8, s} of sub-blocks 2q and 2q+1
+      const uint32_t scw = (q < 2) ? sc_lo : sc_hi;
+      const uint32_t mw = (q < 2) ? m_lo : m_hi;
+      const int sh = (q & 1) * 16;
+      const int scA = (scw >> sh) & 0xFF, scB = (scw >> (sh + 8)) & 0xFF;
+      const int mA = (mw >> sh) & 0xFF, mB = (mw >> (sh + 8)) & 0xFF;
+      if (WT == KQ_Q5_K) {
+        int dA, dB;
+        if (q == 0) q5_chunk_dots<0>(qa, qb, ha, hb, x0, x1, x2, x3, dA, dB);
+        else if (q == 1) q5_chunk_dots<2>(qa, qb, ha, hb, x0, x1, x2, x3, dA, dB);
+        else if (q == 2) q5_chunk_dots<4>(qa, qb, ha, hb, x0, x1, x2, x3, dA, dB);
+        else q5_chunk_dots<6>(qa, qb, ha, hb, x0, x1, x2, x3, dA, dB);
+        lo = fmaf(ds.x, i2f(scA * dA), lo);
+        lo = fmaf(ds.z, i2f(scB * dB), lo);
+        mn = fmaf(ds.y, i2f(mA), mn);
+        mn = fmaf(ds.w, i2f(mB), mn);
+        continue;
+      }
       // high nibbles are taken in place (w & 0xF0F0F0F0 = 16 * nibble): the sums
       // h0, h1 are exact multiples of 16
       int a0 = __dp4a(static_cast<int>(qa.x & 0x0F0F0F0Fu), x0.x, 0);
@@ -563,11 +668,6 @@ __global__ void __launch_bounds__((NW + 1) * 32, RING ? 2 : 1)
       a1 = __dp4a(static_cast<int>(qb.w & 0x0F0F0F0Fu), x1.w, a1);
       h0 = dp4a_us(qa.w & 0xF0F0F0F0u, x2.w, h0);
       h1 = dp4a_us(qb.w & 0xF0F0F0F0u, x3.w, h1);
-      const uint32_t scw = (q < 2) ? sc_lo : sc_hi;
-      const uint32_t mw = (q < 2) ? m_lo : m_hi;
-      const int sh = (q & 1) * 16;
-      const int scA = (scw >> sh) & 0xFF, scB = (scw >> (sh + 8)) & 0xFF;
-      const int mA = (mw >> sh) & 0xFF, mB = (mw >> (sh + 8)) & 0xFF;
       lo = fmaf(ds.x, i2f(scA * (a0 + a1)), lo);
       lo = fmaf(ds.z, i2f(scB * ((h0 + h1) >> 4)), lo);
       mn = fmaf(ds.y, i2f(mA), mn);
@@ -752,7 +852,7 @@ static inline int round_up(int v, int a) { return (v + a - 1) / a * a; }
 // allows fewer chunk slots than chunks (at least two). False when the rows do
 // not fit (then the item kernel above runs).
 static bool plan_lanerow(int64_t M, int64_t K, int num_sms, int nw, int nt, int budget, bool ring,
-                         MatvecLaneRowParams* p, int* grid, size_t* smem) {
+                         MatvecLaneRowParams* p, int* grid, size_t* smem, int bb = Q4K_BYTES) {
   if (K > (int64_t(1) << 20)) return false;
   p->M = static_cast<int>(M);
   p->K = static_cast<int>(K);
@@ -767,11 +867,12 @@ static bool plan_lanerow(int64_t M, int64_t K, int num_sms, int nw, int nt, int 
   p->xq_tok = round_up(p->K, 128);                      // activation codes of a token
   p->xs_tok = round_up((p->K / 32) * 8, 128);           // {d8, d8 * Sum q} per 32-block
   const int fixed = nt * (p->xq_tok + p->xs_tok) + part_bytes;  // + per-warp partials
-  // Widest odd chunk that fits. cb >= 3 keeps both divisors of the item index
-  // (cb and n_groups * cb) at least 3, so their reciprocals fit in 32 bits.
-  for (int cb = 7; cb >= 3; cb -= 2) {
+  // Widest odd chunk that fits (the TMA box row, cb * bb bytes, is at most 256
+  // words: cb <= 7 for Q4_K, 5 for Q5_K). cb >= 3 keeps both divisors of the item
+  // index (cb and n_groups * cb) at least 3, so their reciprocals fit in 32 bits.
+  for (int cb = (bb == Q5K_BYTES ? 5 : 7); cb >= 3; cb -= 2) {
     const int n_chunks = (p->nb + cb - 1) / cb;
-    const int chunk_bytes = round_up(p->R * cb * Q4K_BYTES, 128);
+    const int chunk_bytes = round_up(p->R * cb * bb, 128);
     int S = n_chunks;
     auto total = [&](int slots) { return static_cast<size_t>(slots) * chunk_bytes + fixed + slots * 16 + 16; };
     while (ring && S > 2 && total(S) > static_cast<size_t>(budget)) --S;
@@ -801,24 +902,47 @@ static bool plan_lanerow(int64_t M, int64_t K, int num_sms, int nw, int nt, int 
 // Shared-memory attribute slot of a kernel instantiation (allow_max_smem).
 constexpr int smem_slot(int base_x, int base_prod, int prod) { return prod == PROD_X ? base_x : base_prod + prod - 1; }
 
+// Shared-memory attribute slots of the lane-row instantiations: full, ring.
+constexpr int lanerow_slot(int wt, bool ring, int prod) {
+  return wt == KQ_Q5_K ? smem_slot(ring ? 29 : 26, ring ? 30 : 27, prod) : smem_slot(ring ? 10 : 9, ring ? 18 : 16, prod);
+}
+
+template <int WT, int PROD>
+static cudaError_t launch_lanerow(bool ring, const CUtensorMap& tmW, const MatvecLaneRowParams& lp, int grid,
+                                  size_t smem, cudaStream_t s) {
+  if (ring) {
+    cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(matvec_q4k_lanerow_kernel<LR_NW_RING, true, PROD, WT>),
+                                   lanerow_slot(WT, true, PROD));
+    if (e != cudaSuccess) return e;
+    return launch_pdl(matvec_q4k_lanerow_kernel<LR_NW_RING, true, PROD, WT>, dim3(grid), dim3((LR_NW_RING + 1) * 32),
+                      smem, s, tmW, lp);
+  }
+  cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(matvec_q4k_lanerow_kernel<LR_NW_FULL, false, PROD, WT>),
+                                 lanerow_slot(WT, false, PROD));
+  if (e != cudaSuccess) return e;
+  return launch_pdl(matvec_q4k_lanerow_kernel<LR_NW_FULL, false, PROD, WT>, dim3(grid), dim3((LR_NW_FULL + 1) * 32),
+                    smem, s, tmW, lp);
+}
+
 template <int PROD>
 static cudaError_t launch_matvec_p(int wtype, const void* W, const float* x, const float* aux, float eps, float* y,
                                    int64_t M, int64_t K, int* err, int num_sms, cudaStream_t s, int* status) {
   *status = KQ_OK;
-  // Q4_K: the lane-row kernel with all rows staged at once when they fit
-  // (measured faster at the decode sizes: the ring's refills wait for the
+  // Q4_K and Q5_K: the lane-row kernel with all rows staged at once when they
+  // fit (measured faster at the decode sizes: the ring's refills wait for the
   // activations and then for HBM), else its ring form.
-  if (wtype == KQ_Q4_K) {
+  if (wtype == KQ_Q4_K || wtype == KQ_Q5_K) {
+    const int bb = wtype == KQ_Q5_K ? Q5K_BYTES : Q4K_BYTES;
     MatvecLaneRowParams lp{};
     size_t smem = 0;
     int grid = 0;
-    const bool full = plan_lanerow(M, K, num_sms, LR_NW_FULL, 1, MV_SMEM_LIMIT, false, &lp, &grid, &smem);
-    const bool ring = !full && plan_lanerow(M, K, num_sms, LR_NW_RING, 1, LR_RING_SMEM, true, &lp, &grid, &smem);
+    const bool full = plan_lanerow(M, K, num_sms, LR_NW_FULL, 1, MV_SMEM_LIMIT, false, &lp, &grid, &smem, bb);
+    const bool ring = !full && plan_lanerow(M, K, num_sms, LR_NW_RING, 1, LR_RING_SMEM, true, &lp, &grid, &smem, bb);
     if (full || ring) {
       CUtensorMap tmW;
-      const uint64_t rs = static_cast<uint64_t>(lp.nb) * Q4K_BYTES;
+      const uint64_t rs = static_cast<uint64_t>(lp.nb) * bb;
       if (!encode_tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT32, W, rs / 4, static_cast<uint64_t>(M), rs,
-                          static_cast<uint32_t>(lp.cb * Q4K_BYTES / 4), static_cast<uint32_t>(lp.R),
+                          static_cast<uint32_t>(lp.cb * bb / 4), static_cast<uint32_t>(lp.R),
                           CU_TENSOR_MAP_SWIZZLE_NONE)) {
         *status = KQ_ERR_CUDA;
         return cudaSuccess;
@@ -829,18 +953,8 @@ static cudaError_t launch_matvec_p(int wtype, const void* W, const float* x, con
       lp.y = y;
       lp.n_tok = 1;
       lp.err = err;
-      if (ring) {
-        cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(matvec_q4k_lanerow_kernel<LR_NW_RING, true, PROD>),
-                                       smem_slot(10, 18, PROD));
-        if (e != cudaSuccess) return e;
-        return launch_pdl(matvec_q4k_lanerow_kernel<LR_NW_RING, true, PROD>, dim3(grid), dim3((LR_NW_RING + 1) * 32), smem,
-                          s, tmW, lp);
-      }
-      cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(matvec_q4k_lanerow_kernel<LR_NW_FULL, false, PROD>),
-                                     smem_slot(9, 16, PROD));
-      if (e != cudaSuccess) return e;
-      return launch_pdl(matvec_q4k_lanerow_kernel<LR_NW_FULL, false, PROD>, dim3(grid), dim3((LR_NW_FULL + 1) * 32), smem,
-                        s, tmW, lp);
+      if (wtype == KQ_Q5_K) return launch_lanerow<KQ_Q5_K, PROD>(ring, tmW, lp, grid, smem, s);
+      return launch_lanerow<KQ_Q4_K, PROD>(ring, tmW, lp, grid, smem, s);
     }
   }
   MatvecParams p{};
@@ -852,10 +966,10 @@ static cudaError_t launch_matvec_p(int wtype, const void* W, const float* x, con
   p.M = static_cast<int>(M);
   p.K = static_cast<int>(K);
   p.nb = static_cast<int>(K / QK_K);
-  p.bb = wtype == KQ_Q4_K ? Q4K_BYTES : Q6K_BYTES;
+  p.bb = wtype == KQ_Q4_K ? Q4K_BYTES : wtype == KQ_Q5_K ? Q5K_BYTES : Q6K_BYTES;
   p.rs = p.nb * p.bb;
   p.unit_rows = (p.rs % 16 == 0) ? 1 : 8;  // 8 rows of 210-byte blocks span a multiple of 16 bytes
-  p.chunk_blocks = wtype == KQ_Q4_K ? MV_CHUNK_BLOCKS_Q4K : MV_CHUNK_BLOCKS_Q6K;
+  p.chunk_blocks = wtype == KQ_Q4_K ? MV_CHUNK_BLOCKS_Q4K : wtype == KQ_Q5_K ? MV_CHUNK_BLOCKS_Q5K : MV_CHUNK_BLOCKS_Q6K;
   p.chunk_bytes = p.chunk_blocks * p.bb;
   p.slot_bytes = round_up(p.chunk_bytes, 128);
   p.rows_per_group = MV_PART_MAX / p.nb;
@@ -887,6 +1001,10 @@ static cudaError_t launch_matvec_p(int wtype, const void* W, const float* x, con
     e = allow_max_smem(reinterpret_cast<const void*>(matvec_kernel<KQ_Q4_K, PROD>), smem_slot(0, 20, PROD));
     if (e != cudaSuccess) return e;
     e = launch_pdl(matvec_kernel<KQ_Q4_K, PROD>, dim3(G), dim3(MV_THREADS), smem, s, p);
+  } else if (wtype == KQ_Q5_K) {
+    e = allow_max_smem(reinterpret_cast<const void*>(matvec_kernel<KQ_Q5_K, PROD>), smem_slot(32, 33, PROD));
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(matvec_kernel<KQ_Q5_K, PROD>, dim3(G), dim3(MV_THREADS), smem, s, p);
   } else {
     e = allow_max_smem(reinterpret_cast<const void*>(matvec_kernel<KQ_Q6_K, PROD>), smem_slot(1, 22, PROD));
     if (e != cudaSuccess) return e;
