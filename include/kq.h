@@ -138,6 +138,21 @@ KQ_API kq_status kq_matvec(int wtype, const void* W, const float* x, float* y, i
                            kq_stream_t stream);
 
 /*
+ * kq_matvec_prefetch — kq_matvec, and while it runs each CTA also asks L2 to
+ * fetch its share of W_next[0, W_next_bytes) (rounded down to a multiple of 16):
+ * the weights of the call that follows on the stream, e.g. the next layer's
+ * matrix in a decode step. That call's weight stream then starts from L2 while
+ * this one waits for its activations and computes. y is bit-identical to
+ * kq_matvec's; the prefetch is a hint (nothing waits for it). An addition of
+ * this library (the pages launch one matrix per call without it). Taken by the
+ * Q4_K and Q5_K staged kernels; the other kernel forms ignore it.
+ * W_next: NULL (no prefetch) or 16-byte aligned device memory readable for
+ * W_next_bytes bytes (KQ_ERR_ALIGN otherwise). Other arguments as kq_matvec.
+ */
+KQ_API kq_status kq_matvec_prefetch(int wtype, const void* W, const float* x, float* y, int64_t M, int64_t K,
+                                    const void* W_next, size_t W_next_bytes, kq_stream_t stream);
+
+/*
  * kq_matvec_swiglu, kq_matvec_rmsnorm — kq_matvec with the producer of its
  * activations fused into the Q8_1 quantiser ([MMVQ] §3.2 Key code: the
  * quantisation body moved into the RMSNorm and SwiGLU producers), so the

@@ -16,7 +16,7 @@ from ._native import (KQ_DEVERR_EXPERT_ID, KQ_DEVERR_NONE, KQ_DEVERR_WAIT_TIMEOU
 __all__ = [
     "KQ_Q4_K", "KQ_Q5_K", "KQ_Q6_K", "KQ_TQ4_1S", "KQ_OP_MATVEC", "KQ_OP_GEMM", "KQ_OP_MOE", "KQError",
     "KQ_DEVERR_NONE", "KQ_DEVERR_WAIT_TIMEOUT", "KQ_DEVERR_EXPERT_ID",
-    "KQ_GEMM_STATIC_WS_BYTES", "kq_quantize_q8_1", "kq_matvec", "kq_matvec_swiglu", "kq_matvec_rmsnorm",
+    "KQ_GEMM_STATIC_WS_BYTES", "kq_quantize_q8_1", "kq_matvec", "kq_matvec_prefetch", "kq_matvec_swiglu", "kq_matvec_rmsnorm",
     "kq_gemm", "kq_gemm_noalloc", "kq_moe_grouped_gemm", "kq_moe_combine", "kq_workspace_bytes",
     "kq_get_device_error", "block_bytes", "row_bytes",
 ]
@@ -80,6 +80,20 @@ def kq_matvec(wtype, W, x, M: int, K: int, y=None, stream=None):
         y = torch.empty(M, dtype=torch.float32, device=x.device)
     check(lib().kq_matvec(_wt(wtype), _dev(W, "W", torch.uint8), _dev(x, "x", torch.float32),
                           _dev(y, "y", torch.float32), M, K, _stream(stream)), "kq_matvec")
+    return y
+
+
+def kq_matvec_prefetch(wtype, W, x, M: int, K: int, W_next=None, y=None, stream=None):
+    """kq_matvec, and L2 is asked to prefetch W_next (the next call's weights,
+    a uint8 CUDA tensor) while it runs; y is identical to kq_matvec's."""
+    torch = _torch()
+    if y is None:
+        y = torch.empty(M, dtype=torch.float32, device=x.device)
+    nxt = _dev(W_next, "W_next", torch.uint8) if W_next is not None else ctypes.c_void_p(0)
+    nbytes = W_next.numel() if W_next is not None else 0
+    check(lib().kq_matvec_prefetch(_wt(wtype), _dev(W, "W", torch.uint8), _dev(x, "x", torch.float32),
+                                   _dev(y, "y", torch.float32), M, K, nxt, nbytes, _stream(stream)),
+          "kq_matvec_prefetch")
     return y
 
 

@@ -42,6 +42,7 @@ _sz = ctypes.c_size_t
 SIGNATURES = {
     "kq_quantize_q8_1": (ctypes.c_int, [_vp, _vp, _i64, _i64, _vp]),
     "kq_matvec": (ctypes.c_int, [ctypes.c_int, _vp, _vp, _vp, _i64, _i64, _vp]),
+    "kq_matvec_prefetch": (ctypes.c_int, [ctypes.c_int, _vp, _vp, _vp, _i64, _i64, _vp, ctypes.c_size_t, _vp]),
     "kq_matvec_swiglu": (ctypes.c_int, [ctypes.c_int, _vp, _vp, _vp, _vp, _i64, _i64, _vp]),
     "kq_matvec_rmsnorm": (ctypes.c_int, [ctypes.c_int, _vp, _vp, _vp, ctypes.c_float, _vp, _i64, _i64, _vp]),
     "kq_moe_combine": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, _i32, _vp]),

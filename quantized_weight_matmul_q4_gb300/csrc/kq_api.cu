@@ -109,7 +109,9 @@ kq_status kq_quantize_q8_1(const float* X, void* Xq, int64_t K, int64_t N, kq_st
 }
 
 static kq_status matvec_entry(int wtype, const void* W, const float* x, const float* aux, float eps, int prod,
-                              float* y, int64_t M, int64_t K, kq_stream_t stream) {
+                              float* y, int64_t M, int64_t K, kq_stream_t stream, const void* W_next = nullptr,
+                              size_t W_next_bytes = 0) {
+  if (W_next && !aligned16(W_next)) return KQ_ERR_ALIGN;
   if (wtype == KQ_TQ4_1S && prod == PROD_X) {
     if (!W || !x || !y) return KQ_ERR_NULL;
     if (M <= 0 || K <= 0 || K % 32 != 0 || M > kMaxDim || K > kMaxDim) return KQ_ERR_SHAPE;
@@ -132,12 +134,19 @@ static kq_status matvec_entry(int wtype, const void* W, const float* x, const fl
   cudaError_t e = device_state(&dev, &sms, &err);
   if (e != cudaSuccess) return KQ_ERR_CUDA;
   int status = KQ_OK;
-  e = launch_matvec(wtype, W, x, aux, eps, prod, y, M, K, err, sms, reinterpret_cast<cudaStream_t>(stream), &status);
+  const uint64_t pf_bytes = W_next ? (static_cast<uint64_t>(W_next_bytes) & ~uint64_t(15)) : 0;
+  e = launch_matvec(wtype, W, x, aux, eps, prod, y, M, K, W_next, pf_bytes, err, sms,
+                    reinterpret_cast<cudaStream_t>(stream), &status);
   return finish(e, status);
 }
 
 kq_status kq_matvec(int wtype, const void* W, const float* x, float* y, int64_t M, int64_t K, kq_stream_t stream) {
   return matvec_entry(wtype, W, x, nullptr, 0.f, PROD_X, y, M, K, stream);
+}
+
+kq_status kq_matvec_prefetch(int wtype, const void* W, const float* x, float* y, int64_t M, int64_t K,
+                             const void* W_next, size_t W_next_bytes, kq_stream_t stream) {
+  return matvec_entry(wtype, W, x, nullptr, 0.f, PROD_X, y, M, K, stream, W_next, W_next_bytes);
 }
 
 kq_status kq_matvec_swiglu(int wtype, const void* W, const float* gate, const float* up, float* y, int64_t M,

@@ -23,8 +23,12 @@ cudaError_t launch_gather_rows(const __half* Xtok, __half* Xh, int64_t K, int64_
 constexpr int PROD_X = 0;
 constexpr int PROD_SWIGLU = 1;
 constexpr int PROD_RMSNORM = 2;
+// pf: the next call's weights, of which each CTA asks L2 to prefetch its share
+// of pf_bytes (a multiple of 16) while it runs (the Q4_K / Q5_K lane-row
+// kernels; the other kernels ignore it); null for none.
 cudaError_t launch_matvec(int wtype, const void* W, const float* x, const float* aux, float eps, int prod, float* y,
-                          int64_t M, int64_t K, int* err, int num_sms, cudaStream_t s, int* status);
+                          int64_t M, int64_t K, const void* pf, uint64_t pf_bytes, int* err, int num_sms, cudaStream_t s,
+                          int* status);
 
 // TQ4_1S decode matvec y = W . x (K a multiple of 32; W 16-byte aligned).
 cudaError_t launch_tq4_matvec(const void* W, const float* x, float* y, int64_t M, int64_t K, int* err, int num_sms,

@@ -474,8 +474,21 @@ struct MatvecLaneRowParams {
   int xq_tok, xs_tok;                     // bytes of one token's codes and of its {d8, s} pairs
   const uint8_t* xq_g;                    // several tokens: codes [n_tok][xq_tok], quantised beforehand
   const uint8_t* xs_g;                    // several tokens: {d8, s} pairs [n_tok][xs_tok]
+  const uint8_t* pf;                      // the next call's weights, prefetched into L2 (or null)
+  uint64_t pf_bytes;                      // a multiple of 16
   int* err;
 };
+
+// This CTA's share of an L2 prefetch of pf[0, bytes): one slice per CTA, in
+// pieces of at most 64 KB (issued by one thread; nothing waits for them).
+__device__ __forceinline__ void prefetch_share_l2(const uint8_t* pf, uint64_t bytes) {
+  if (!pf || bytes == 0) return;
+  const uint64_t share = (bytes / gridDim.x + 15) & ~uint64_t(15);
+  const uint64_t begin = static_cast<uint64_t>(blockIdx.x) * share;
+  const uint64_t end = min(begin + share, bytes);
+  for (uint64_t off = begin; off < end; off += 65536)
+    bulk_prefetch_l2(pf + off, static_cast<uint32_t>(min(static_cast<uint64_t>(65536), end - off)));
+}
 
 template <int NW, bool RING, int PROD, int WT = KQ_Q4_K>
 __global__ void __launch_bounds__((NW + 1) * 32, RING ? 2 : 1)
@@ -518,6 +531,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, RING ? 2 : 1)
           mbar_expect_tx(&full[c], box);
           tma_load_2d(smem + static_cast<size_t>(c) * p.chunk_bytes, &tmW, &full[c], c * p.cb * (BB / 4), r0);
         }
+        prefetch_share_l2(p.pf, p.pf_bytes);  // behind this call's own copies
         // Every copy lands before the CTA may exit (also when the consumers gave up).
         for (int c = 0; c < p.n_chunks; ++c)
           if (!mbar_wait_bounded(&full[c], 0)) report_error(p.err, ERR_WAIT_TIMEOUT);
@@ -525,12 +539,14 @@ __global__ void __launch_bounds__((NW + 1) * 32, RING ? 2 : 1)
         int issued = 0;
         for (int c = 0; c < p.n_chunks; ++c) {
           const int sl = c % p.S;
+          if (c == p.S) prefetch_share_l2(p.pf, p.pf_bytes);  // once the ring is primed
           if (c >= p.S && !mbar_wait(&empty[sl], ((c / p.S) - 1) & 1, abort, p.err)) break;
           mbar_expect_tx(&full[sl], box);
           tma_load_2d(smem + static_cast<size_t>(sl) * p.chunk_bytes, &tmW, &full[sl], c * p.cb * (BB / 4), r0);
           issued = c + 1;
           *chunks_issued = issued;
         }
+        if (p.n_chunks <= p.S) prefetch_share_l2(p.pf, p.pf_bytes);
         // Every copy lands before the CTA may exit (also when the consumers gave up).
         for (int sl = 0; sl < min(issued, p.S); ++sl) {
           const int fills = (issued - sl + p.S - 1) / p.S;
@@ -926,7 +942,8 @@ static cudaError_t launch_lanerow(bool ring, const CUtensorMap& tmW, const Matve
 
 template <int PROD>
 static cudaError_t launch_matvec_p(int wtype, const void* W, const float* x, const float* aux, float eps, float* y,
-                                   int64_t M, int64_t K, int* err, int num_sms, cudaStream_t s, int* status) {
+                                   int64_t M, int64_t K, const void* pf, uint64_t pf_bytes, int* err, int num_sms,
+                                   cudaStream_t s, int* status) {
   *status = KQ_OK;
   // Q4_K and Q5_K: the lane-row kernel with all rows staged at once when they
   // fit (measured faster at the decode sizes: the ring's refills wait for the
@@ -952,6 +969,8 @@ static cudaError_t launch_matvec_p(int wtype, const void* W, const float* x, con
       lp.eps = eps;
       lp.y = y;
       lp.n_tok = 1;
+      lp.pf = static_cast<const uint8_t*>(pf);
+      lp.pf_bytes = pf_bytes;
       lp.err = err;
       if (wtype == KQ_Q5_K) return launch_lanerow<KQ_Q5_K, PROD>(ring, tmW, lp, grid, smem, s);
       return launch_lanerow<KQ_Q4_K, PROD>(ring, tmW, lp, grid, smem, s);
@@ -1014,14 +1033,15 @@ static cudaError_t launch_matvec_p(int wtype, const void* W, const float* x, con
 }
 
 cudaError_t launch_matvec(int wtype, const void* W, const float* x, const float* aux, float eps, int prod, float* y,
-                          int64_t M, int64_t K, int* err, int num_sms, cudaStream_t s, int* status) {
+                          int64_t M, int64_t K, const void* pf, uint64_t pf_bytes, int* err, int num_sms, cudaStream_t s,
+                          int* status) {
   switch (prod) {
     case PROD_SWIGLU:
-      return launch_matvec_p<PROD_SWIGLU>(wtype, W, x, aux, eps, y, M, K, err, num_sms, s, status);
+      return launch_matvec_p<PROD_SWIGLU>(wtype, W, x, aux, eps, y, M, K, pf, pf_bytes, err, num_sms, s, status);
     case PROD_RMSNORM:
-      return launch_matvec_p<PROD_RMSNORM>(wtype, W, x, aux, eps, y, M, K, err, num_sms, s, status);
+      return launch_matvec_p<PROD_RMSNORM>(wtype, W, x, aux, eps, y, M, K, pf, pf_bytes, err, num_sms, s, status);
     default:
-      return launch_matvec_p<PROD_X>(wtype, W, x, aux, eps, y, M, K, err, num_sms, s, status);
+      return launch_matvec_p<PROD_X>(wtype, W, x, aux, eps, y, M, K, pf, pf_bytes, err, num_sms, s, status);
   }
 }
 

@@ -68,6 +68,14 @@ def test_tq4_1s_argument_checks(L):
     assert L.kq_moe_grouped_gemm(nat.KQ_TQ4_1S, A, 8, A, 2, A, A, 16, 256, 4, A, 1 << 30, NUL) == nat.KQ_ERR_TYPE
 
 
+def test_prefetch_argument_checks(L):
+    f = L.kq_matvec_prefetch
+    assert f(nat.KQ_Q4_K, A, A, A, 16, 256, U, 1024, NUL) == nat.KQ_ERR_ALIGN    # misaligned W_next
+    assert f(nat.KQ_Q4_K, NUL, A, A, 16, 256, A, 1024, NUL) == nat.KQ_ERR_NULL
+    assert f(nat.KQ_Q4_K, A, A, A, 16, 300, A, 1024, NUL) == nat.KQ_ERR_SHAPE
+    assert f(9, A, A, A, 16, 256, NUL, 0, NUL) == nat.KQ_ERR_TYPE
+
+
 def test_q5k_argument_checks(L):
     # Q5_K: the decode matvecs take it (K a multiple of 256); the GEMM and MoE calls do not.
     assert L.kq_matvec(nat.KQ_Q5_K, NUL, A, A, 16, 256, NUL) == nat.KQ_ERR_NULL

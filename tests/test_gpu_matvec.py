@@ -109,3 +109,21 @@ def test_shallow_rings_sampled_rows(wtype, M, K):
     Yr, B = ora.matmul_rows(wtype, W, x, K, rows)
     assert_within_bound(y[rows], Yr[0], B[0], f"shallow ring {wtype} {M}x{K}")
     assert np.all(np.isfinite(y))
+
+
+def test_prefetch_call_is_bit_identical():
+    # kq_matvec_prefetch only adds an L2 prefetch of the next call's weights.
+    import torch
+    from quantized_weight_matmul_q4_gb300 import kq_matvec_prefetch
+    for wtype, name in [("q4_k", "decode_q4k_4096x11008"), ("q5_k", "decode_q5k_11008x4096"),
+                        ("q6_k", "decode_q6k_4096x11008")]:
+        wl = syn.make_workload(name, copies=2)
+        M, K = wl["M"], wl["K"]
+        W = to_dev(wl["W"][0], torch)
+        W_next = to_dev(wl["W"][1], torch)
+        x = to_dev(wl["X"].reshape(-1), torch)
+        a = kq_matvec(wtype, W, x, M, K)
+        b = kq_matvec_prefetch(wtype, W, x, M, K, W_next=W_next)
+        c = kq_matvec_prefetch(wtype, W, x, M, K, W_next=None)
+        torch.cuda.synchronize()
+        assert torch.equal(a, b) and torch.equal(a, c), wtype
