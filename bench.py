@@ -495,7 +495,8 @@ def run_sections(args, kq, syn, torch, dev, stream, pk, only=None):
         return res
     iters = max(3, args.section_iters)
     gemm_names = ["smalln_q4k_4096x11008_n4", "prefill_q4k_4096x4096_n64", "prefill_q4k_4096x4096_n512",
-                  "prefill_q4k_14336x4096_n2048", "prefill_q6k_4096x14336_n2048"]
+                  "prefill_q4k_14336x4096_n2048", "prefill_q6k_4096x14336_n2048",
+                  "prefill_q5k_14336x4096_n2048"]
     moe_name = "moe_q4k_128x768x2048_t1024_top8"
     if only is not None:
         if only not in gemm_names + [moe_name] + list(DECODE_SECTIONS):

@@ -3,8 +3,8 @@
  *
  *   Y[M, N] = dequant(W)[M, K] . X[K, N]
  *
- * W holds 4-bit Q4_K or 6-bit Q6_K super-blocks (5-bit Q5_K for the decode
- * matvec); X is fp32 and is quantised to
+ * W holds 4-bit Q4_K, 5-bit Q5_K or 6-bit Q6_K super-blocks; X is fp32 and is
+ * quantised to
  * Q8_1 (int8 codes with an fp16 scale per 32 values) inside every call. The
  * decode matvec also takes TQ4_1S weights (WHT-rotated 4-bit Lloyd-Max codes),
  * which it multiplies with the fp32 activations directly.
@@ -85,9 +85,8 @@ typedef enum kq_status {
   KQ_ERR_DEVICE = 7     /* a kernel recorded an error; see kq_get_device_error */
 } kq_status;
 
-/* KQ_Q5_K is taken by the decode matvecs (kq_matvec, kq_matvec_swiglu,
- * kq_matvec_rmsnorm) and KQ_TQ4_1S by kq_matvec only; the other entry points
- * return KQ_ERR_TYPE for them. */
+/* KQ_Q5_K is taken wherever Q4_K is; KQ_TQ4_1S by kq_matvec only (the other
+ * entry points return KQ_ERR_TYPE for it). */
 typedef enum kq_wtype { KQ_Q4_K = 1, KQ_Q6_K = 2, KQ_TQ4_1S = 3, KQ_Q5_K = 4 } kq_wtype;
 
 typedef enum kq_op { KQ_OP_MATVEC = 1, KQ_OP_GEMM = 2, KQ_OP_MOE = 3 } kq_op;

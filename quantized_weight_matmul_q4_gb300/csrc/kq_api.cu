@@ -52,8 +52,8 @@ int sm_count_or_default() {
 std::atomic<uint8_t> g_smem_set[kSmemSlots][kMaxDevices];
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-inline bool valid_wtype(int t) { return t == KQ_Q4_K || t == KQ_Q6_K; }  // every entry point
-inline bool valid_matvec_wtype(int t) { return valid_wtype(t) || t == KQ_Q5_K; }  // the decode matvecs
+inline bool valid_wtype(int t) { return t == KQ_Q4_K || t == KQ_Q6_K || t == KQ_Q5_K; }  // the k-quants
+inline bool valid_matvec_wtype(int t) { return valid_wtype(t); }
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
 
 kq_status finish(cudaError_t e, int status) {

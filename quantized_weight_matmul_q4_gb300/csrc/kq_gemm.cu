@@ -71,6 +71,10 @@ struct RawBox<KQ_Q4_K> {
   static constexpr int BYTES = 144;  // one Q4_K super-block per row, 16-byte aligned in a row
 };
 template <>
+struct RawBox<KQ_Q5_K> {
+  static constexpr int BYTES = 176;  // one Q5_K super-block per row, 16-byte aligned in a row
+};
+template <>
 struct RawBox<KQ_Q6_K> {
   // A 16-byte aligned window covering one 210-byte Q6_K block (which starts up
   // to 14 bytes in). 240 bytes = 60 words: the unpackers' 32-bit loads of 32
@@ -214,6 +218,48 @@ __device__ __forceinline__ void dequant_q4k(const uint4& hdr, const uint8_t* __r
     const uint32_t l1 = __byte_perm(w[i], 0x64646464u, 0x7362) & 0xFF0FFF0Fu;
     const uint32_t h0 = __byte_perm(w[i] >> 4, 0x64646464u, 0x5140) & 0xFF0FFF0Fu;
     const uint32_t h1 = __byte_perm(w[i] >> 4, 0x64646464u, 0x7362) & 0xFF0FFF0Fu;
+    lo[2 * i] = half2_bits(__hfma2(__hsub2(bits_half2(l0), k1024), sc_lo, mn_lo));
+    lo[2 * i + 1] = half2_bits(__hfma2(__hsub2(bits_half2(l1), k1024), sc_lo, mn_lo));
+    hi[2 * i] = half2_bits(__hfma2(__hsub2(bits_half2(h0), k1024), sc_hi, mn_hi));
+    hi[2 * i + 1] = half2_bits(__hfma2(__hsub2(bits_half2(h1), k1024), sc_hi, mn_hi));
+  }
+}
+
+// Q5_K K step s, the Q4_K unpack with 5-bit codes: the 16 nibble bytes of half
+// hf of sub-blocks 2s (low nibbles) and 2s+1 (high nibbles) take their fifth
+// bits from bits 2s and 2s+1 of the matching qh bytes (qh[16 hf ..]); a code q
+// (0..31) becomes fp16 1024 + q in one byte permute, as in dequant_q4k.
+__device__ __forceinline__ void dequant_q5k(const uint4& hdr, const uint8_t* __restrict__ raw, int s, int r, int hf,
+                                            uint32_t (&lo)[8], uint32_t (&hi)[8]) {
+  const uint8_t* row = raw + r * Q5K_BYTES;
+  const uint4 q = *reinterpret_cast<const uint4*>(row + 48 + 32 * s + 16 * hf);
+  const uint4 qh = *reinterpret_cast<const uint4*>(row + 16 + 16 * hf);
+  uint32_t scw, mw;
+  if (s < 2) {
+    scw = hdr.y & 0x3F3F3F3Fu;
+    mw = hdr.z & 0x3F3F3F3Fu;
+  } else {
+    scw = (hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u);
+    mw = ((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u);
+  }
+  const int b0 = (s & 1) * 16;
+  const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x & 0xFFFFu)));
+  const float dmin = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x >> 16)));
+  const __half2 sc_lo = __float2half2_rn(d * static_cast<float>((scw >> b0) & 0xFFu));
+  const __half2 mn_lo = __float2half2_rn(-(dmin * static_cast<float>((mw >> b0) & 0xFFu)));
+  const __half2 sc_hi = __float2half2_rn(d * static_cast<float>((scw >> (b0 + 8)) & 0xFFu));
+  const __half2 mn_hi = __float2half2_rn(-(dmin * static_cast<float>((mw >> (b0 + 8)) & 0xFFu)));
+  const __half2 k1024 = __float2half2_rn(1024.f);
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  const uint32_t h[4] = {qh.x, qh.y, qh.z, qh.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t cl = (w[i] & 0x0F0F0F0Fu) | (((h[i] >> (2 * s)) & 0x01010101u) << 4);
+    const uint32_t ch = ((w[i] >> 4) & 0x0F0F0F0Fu) | (((h[i] >> (2 * s + 1)) & 0x01010101u) << 4);
+    const uint32_t l0 = __byte_perm(cl, 0x64646464u, 0x5140);
+    const uint32_t l1 = __byte_perm(cl, 0x64646464u, 0x7362);
+    const uint32_t h0 = __byte_perm(ch, 0x64646464u, 0x5140);
+    const uint32_t h1 = __byte_perm(ch, 0x64646464u, 0x7362);
     lo[2 * i] = half2_bits(__hfma2(__hsub2(bits_half2(l0), k1024), sc_lo, mn_lo));
     lo[2 * i + 1] = half2_bits(__hfma2(__hsub2(bits_half2(l1), k1024), sc_lo, mn_lo));
     hi[2 * i] = half2_bits(__hfma2(__hsub2(bits_half2(h0), k1024), sc_hi, mn_hi));
@@ -411,7 +457,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
         for (int kb = T.kb0; kb < T.kb1; ++kb) {
           if (!mbar_wait(&raw_empty[st], ph ^ 1, abort, a.err)) break;
           mbar_expect_tx(&raw_full[st], RAW_BYTES);
-          const int x = (WT == KQ_Q4_K) ? kb * Q4K_BYTES : ((kb * Q6K_BYTES) & ~15);
+          const int x = (WT == KQ_Q4_K) ? kb * Q4K_BYTES : (WT == KQ_Q5_K) ? kb * Q5K_BYTES : ((kb * Q6K_BYTES) & ~15);
           tma_load_2d(sRaw + st * RAW_BYTES, &tmW, &raw_full[st], x, T.wrow0);
           if (++st == a.raw_stages) {
             st = 0;
@@ -580,7 +626,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
         uint4 hdr = make_uint4(0u, 0u, 0u, 0u);
         Q6Half q6;
         for (int s = 0; s < 4; ++s) {
-          const bool mine = (WT == KQ_Q4_K) ? ((s & 1) == grp) : ((s >> 1) == grp);
+          const bool mine = (WT != KQ_Q6_K) ? ((s & 1) == grp) : ((s >> 1) == grp);
           if (mine) {
             if (!mbar_wait(&k_empty[ast], aph ^ 1, abort, a.err)) break;
             tc_fence_after();
@@ -588,6 +634,9 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
             if (WT == KQ_Q4_K) {
               if (s < 2) hdr = *reinterpret_cast<const uint4*>(raw + r * Q4K_BYTES);
               dequant_q4k(hdr, raw, s, r, hf, lo, hi);
+            } else if (WT == KQ_Q5_K) {
+              if (s < 2) hdr = *reinterpret_cast<const uint4*>(raw + r * Q5K_BYTES);
+              dequant_q5k(hdr, raw, s, r, hf, lo, hi);
             } else {
               if ((s & 1) == 0) load_q6k_half(raw, rem, s >> 1, r, hf, q6);
               dequant_q6k(raw, rem, q6, s, r, hf, lo, hi);
@@ -836,7 +885,13 @@ bool encode_tmap_2d(CUtensorMap* tm, CUtensorMapDataType dtype, const void* base
   return r == CUDA_SUCCESS;
 }
 
-static int raw_box_bytes(int wtype) { return wtype == KQ_Q4_K ? RawBox<KQ_Q4_K>::BYTES : RawBox<KQ_Q6_K>::BYTES; }
+static int raw_box_bytes(int wtype) {
+  return wtype == KQ_Q4_K ? RawBox<KQ_Q4_K>::BYTES : wtype == KQ_Q5_K ? RawBox<KQ_Q5_K>::BYTES : RawBox<KQ_Q6_K>::BYTES;
+}
+
+// Shared-memory attribute slots of the GEMM instantiations.
+constexpr int gemm_slot(int wt, bool moe) { return wt == KQ_Q5_K ? (moe ? 3 : 2) : 2 + 2 * wt + (moe ? 1 : 0); }
+constexpr int pair_slot(int wt) { return wt == KQ_Q5_K ? 15 : 11 + wt; }
 
 // Tensor memory: the accumulators (two when that leaves room for four A stages,
 // so the epilogue of one tile overlaps the next tile's MMAs), then up to eight
@@ -903,7 +958,7 @@ template <int WT, bool MOE>
 static cudaError_t launch_kernel(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmArgs& a, int grid,
                                  size_t smem, cudaStream_t s) {
   cudaError_t e =
-      allow_max_smem(reinterpret_cast<const void*>(kq_gemm_kernel<WT, MOE, false>), 2 + 2 * WT + (MOE ? 1 : 0));
+      allow_max_smem(reinterpret_cast<const void*>(kq_gemm_kernel<WT, MOE, false>), gemm_slot(WT, MOE));
   if (e != cudaSuccess) return e;
   return launch_pdl(kq_gemm_kernel<WT, MOE, false>, dim3(grid), dim3(GM_THREADS), smem, s, tmW, tmX, a);
 }
@@ -914,12 +969,12 @@ static cudaError_t launch_kernel(const CUtensorMap& tmW, const CUtensorMap& tmX,
 template <int WT>
 static int pair_clusters(cudaLaunchConfig_t cfg) {
   static std::mutex mu;
-  static int cached[2][64];
-  static bool known[2][64];
+  static int cached[3][64];
+  static bool known[3][64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   std::lock_guard<std::mutex> lock(mu);
-  const int w = WT == KQ_Q4_K ? 0 : 1;
+  const int w = WT == KQ_Q4_K ? 0 : WT == KQ_Q5_K ? 1 : 2;
   if (!known[w][dev]) {
     int n = 0;
     cfg.gridDim = dim3(2);
@@ -939,7 +994,7 @@ template <int WT>
 static cudaError_t launch_pair(const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmArgs& a, int units,
                                size_t smem, cudaStream_t s, bool* launched) {
   *launched = false;
-  cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(kq_gemm_kernel<WT, false, true>), 11 + WT);
+  cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(kq_gemm_kernel<WT, false, true>), pair_slot(WT));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(GM_THREADS);
@@ -966,12 +1021,15 @@ static cudaError_t dispatch(int wtype, bool moe, const CUtensorMap& tmW, const C
   if (wtype == KQ_Q4_K)
     return moe ? launch_kernel<KQ_Q4_K, true>(tmW, tmX, a, grid, smem, s)
                : launch_kernel<KQ_Q4_K, false>(tmW, tmX, a, grid, smem, s);
+  if (wtype == KQ_Q5_K)
+    return moe ? launch_kernel<KQ_Q5_K, true>(tmW, tmX, a, grid, smem, s)
+               : launch_kernel<KQ_Q5_K, false>(tmW, tmX, a, grid, smem, s);
   return moe ? launch_kernel<KQ_Q6_K, true>(tmW, tmX, a, grid, smem, s)
              : launch_kernel<KQ_Q6_K, false>(tmW, tmX, a, grid, smem, s);
 }
 
 static bool weight_tmap(CUtensorMap* tm, int wtype, const void* W, int64_t rows, int64_t K) {
-  const int64_t rs = (K / QK_K) * (wtype == KQ_Q4_K ? Q4K_BYTES : Q6K_BYTES);
+  const int64_t rs = (K / QK_K) * (wtype == KQ_Q4_K ? Q4K_BYTES : wtype == KQ_Q5_K ? Q5K_BYTES : Q6K_BYTES);
   return encode_tmap_2d(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, static_cast<uint64_t>(rs), static_cast<uint64_t>(rows),
                         static_cast<uint64_t>(rs), static_cast<uint32_t>(raw_box_bytes(wtype)), GM_BM,
                         CU_TENSOR_MAP_SWIZZLE_NONE);
@@ -1022,8 +1080,9 @@ cudaError_t launch_gemm(int wtype, const void* W, const float* X, float* Y, int6
     size_t smem = 0;
     if (choose_stages(wtype, plan.bn, 0, true, &ap, &smem)) {
       const int units = ap.m_tiles * plan.n_tiles * plan.splits;
-      e = wtype == KQ_Q4_K ? launch_pair<KQ_Q4_K>(tmW, tmX, ap, units, smem, s, &launched)
-                           : launch_pair<KQ_Q6_K>(tmW, tmX, ap, units, smem, s, &launched);
+      e = wtype == KQ_Q4_K   ? launch_pair<KQ_Q4_K>(tmW, tmX, ap, units, smem, s, &launched)
+          : wtype == KQ_Q5_K ? launch_pair<KQ_Q5_K>(tmW, tmX, ap, units, smem, s, &launched)
+                             : launch_pair<KQ_Q6_K>(tmW, tmX, ap, units, smem, s, &launched);
       if (e != cudaSuccess) return e;
     }
   }

@@ -49,7 +49,7 @@ using namespace kq;
 
 extern "C" kq_status kq_gemm_noalloc(int wtype, const void* W, const float* X, float* Y, int64_t M, int64_t K,
                                      int64_t N, kq_stream_t stream) {
-  if (wtype != KQ_Q4_K && wtype != KQ_Q6_K) return KQ_ERR_TYPE;
+  if (wtype != KQ_Q4_K && wtype != KQ_Q6_K && wtype != KQ_Q5_K) return KQ_ERR_TYPE;
   if (!W || !X || !Y) return KQ_ERR_NULL;
   if (M <= 0 || K <= 0 || N <= 0 || K % QK_K != 0 || M > kMaxDim || K > kMaxDim || N > kMaxDim ||
       M * N > (int64_t(1) << 40) || N * K > (int64_t(1) << 40))

@@ -161,6 +161,7 @@ WORKLOADS = {
     "prefill_q4k_4096x4096_n64": dict(kind="gemm", wtype="q4_k", M=4096, K=4096, N=64, seed=2),
     "prefill_q4k_4096x4096_n512": dict(kind="gemm", wtype="q4_k", M=4096, K=4096, N=512, seed=2),
     "prefill_q4k_14336x4096_n2048": dict(kind="gemm", wtype="q4_k", M=14336, K=4096, N=2048, seed=3),
+    "prefill_q5k_14336x4096_n2048": dict(kind="gemm", wtype="q5_k", M=14336, K=4096, N=2048, seed=3),
     "prefill_q6k_4096x14336_n2048": dict(kind="gemm", wtype="q6_k", M=4096, K=14336, N=2048, seed=3),
     "moe_q4k_128x768x2048_t1024_top8": dict(kind="moe", wtype="q4_k", M=768, K=2048, T=1024,
                                            n_experts=128, top_k=8, seed=4),

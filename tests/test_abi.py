@@ -77,14 +77,15 @@ def test_prefetch_argument_checks(L):
 
 
 def test_q5k_argument_checks(L):
-    # Q5_K: the decode matvecs take it (K a multiple of 256); the GEMM and MoE calls do not.
+    # Q5_K is taken wherever Q4_K is (K a multiple of 256).
     assert L.kq_matvec(nat.KQ_Q5_K, NUL, A, A, 16, 256, NUL) == nat.KQ_ERR_NULL
     assert L.kq_matvec(nat.KQ_Q5_K, A, A, A, 16, 288, NUL) == nat.KQ_ERR_SHAPE
     assert L.kq_matvec(nat.KQ_Q5_K, A, U, A, 16, 256, NUL) == nat.KQ_ERR_ALIGN
     assert L.kq_matvec_swiglu(nat.KQ_Q5_K, A, A, NUL, A, 16, 256, NUL) == nat.KQ_ERR_NULL
-    assert L.kq_gemm(nat.KQ_Q5_K, A, A, A, 16, 256, 4, A, 1 << 30, NUL) == nat.KQ_ERR_TYPE
-    assert L.kq_gemm_noalloc(nat.KQ_Q5_K, A, A, A, 16, 256, 4, NUL) == nat.KQ_ERR_TYPE
-    assert L.kq_moe_grouped_gemm(nat.KQ_Q5_K, A, 8, A, 2, A, A, 16, 256, 4, A, 1 << 30, NUL) == nat.KQ_ERR_TYPE
+    assert L.kq_gemm(nat.KQ_Q5_K, A, A, A, 16, 256, 4, NUL, 1 << 30, NUL) == nat.KQ_ERR_NULL
+    assert L.kq_gemm(nat.KQ_Q5_K, A, A, A, 16, 128, 4, A, 1 << 30, NUL) == nat.KQ_ERR_SHAPE
+    assert L.kq_gemm_noalloc(nat.KQ_Q5_K, A, A, A, 16, 128, 4, NUL) == nat.KQ_ERR_SHAPE
+    assert L.kq_moe_grouped_gemm(nat.KQ_Q5_K, A, 0, A, 1, A, A, 16, 256, 4, A, 1 << 30, NUL) == nat.KQ_ERR_SHAPE
 
 
 def test_fused_matvec_argument_checks(L):
