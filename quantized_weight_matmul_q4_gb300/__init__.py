@@ -39,27 +39,39 @@ def row_bytes(wtype, K: int) -> int:
     return (K // _BLOCK_WEIGHTS[_wt(wtype)]) * block_bytes(wtype)
 
 
+_TORCH = None
+
+
 def _torch():
-    import torch
-    return torch
+    global _TORCH
+    if _TORCH is None:
+        import torch
+        _TORCH = torch
+    return _TORCH
 
 
 def _dev(t, name: str, dtype=None):
+    """Device pointer (an int) of a contiguous CUDA tensor of the given dtype."""
     torch = _torch()
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor (libkq has no CPU path)")
+    if dtype is not None and t.dtype is not dtype:
+        raise TypeError(f"{name} must have dtype {dtype}, got {t.dtype}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
-    if dtype is not None and t.dtype != dtype:
-        raise TypeError(f"{name} must have dtype {dtype}, got {t.dtype}")
-    return ctypes.c_void_p(t.data_ptr())
+    return t.data_ptr()
 
 
 def _stream(stream):
+    """The cudaStream_t to queue on: `stream` (a torch stream or a raw handle),
+    else the current stream of the current device."""
     torch = _torch()
     if stream is None:
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)  # the handle, without a Stream object
+        if raw is not None:
+            return raw(torch.cuda.current_device())
         stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
 def kq_quantize_q8_1(X, Xq=None, stream=None):
@@ -89,7 +101,7 @@ def kq_matvec_prefetch(wtype, W, x, M: int, K: int, W_next=None, y=None, stream=
     torch = _torch()
     if y is None:
         y = torch.empty(M, dtype=torch.float32, device=x.device)
-    nxt = _dev(W_next, "W_next", torch.uint8) if W_next is not None else ctypes.c_void_p(0)
+    nxt = _dev(W_next, "W_next", torch.uint8) if W_next is not None else None
     nbytes = W_next.numel() if W_next is not None else 0
     check(lib().kq_matvec_prefetch(_wt(wtype), _dev(W, "W", torch.uint8), _dev(x, "x", torch.float32),
                                    _dev(y, "y", torch.float32), M, K, nxt, nbytes, _stream(stream)),
