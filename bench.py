@@ -439,7 +439,7 @@ def _decode_sweep(kq, syn, torch, dev, stream, names, copies, reps, pk):
         y = torch.empty(wl["M"], dtype=torch.float32, device=dev)
         sets.append((wl["wtype"], wl["M"], wl["K"], Ws, x, y))
 
-    def step():
+    def step():  # plain calls: the next-weights prefetch measured no gain for these kernels (TQ4_1S: slower)
         for c in range(copies):
             for (wt, M, K, Ws, x, y) in sets:
                 kq.kq_matvec(wt, Ws[c], x, M, K, y=y)

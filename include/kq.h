@@ -143,8 +143,8 @@ KQ_API kq_status kq_matvec(int wtype, const void* W, const float* x, float* y, i
  * matrix in a decode step. That call's weight stream then starts from L2 while
  * this one waits for its activations and computes. y is bit-identical to
  * kq_matvec's; the prefetch is a hint (nothing waits for it). An addition of
- * this library (the pages launch one matrix per call without it). Taken by the
- * Q4_K and Q5_K staged kernels; the other kernel forms ignore it.
+ * this library (the pages launch one matrix per call without it). Every decode
+ * kernel form takes it except the TQ4_1S fallback for K % 128 != 0.
  * W_next: NULL (no prefetch) or 16-byte aligned device memory readable for
  * W_next_bytes bytes (KQ_ERR_ALIGN otherwise). Other arguments as kq_matvec.
  */

@@ -121,7 +121,8 @@ static kq_status matvec_entry(int wtype, const void* W, const float* x, const fl
     cudaError_t e = device_state(&dev, &sms, &err);
     if (e != cudaSuccess) return KQ_ERR_CUDA;
     int status = KQ_OK;
-    e = launch_tq4_matvec(W, x, y, M, K, err, sms, reinterpret_cast<cudaStream_t>(stream), &status);
+    const uint64_t pf_bytes = W_next ? (static_cast<uint64_t>(W_next_bytes) & ~uint64_t(15)) : 0;
+    e = launch_tq4_matvec(W, x, y, M, K, W_next, pf_bytes, err, sms, reinterpret_cast<cudaStream_t>(stream), &status);
     return finish(e, status);
   }
   if (!valid_matvec_wtype(wtype)) return KQ_ERR_TYPE;

@@ -200,6 +200,17 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// This CTA's share of an L2 prefetch of pf[0, bytes): one slice per CTA, in
+// pieces of at most 64 KB (issued by one thread; nothing waits for them).
+__device__ __forceinline__ void prefetch_share_l2(const uint8_t* pf, uint64_t bytes) {
+  if (!pf || bytes == 0) return;
+  const uint64_t share = (bytes / gridDim.x + 15) & ~uint64_t(15);
+  const uint64_t begin = static_cast<uint64_t>(blockIdx.x) * share;
+  const uint64_t end = min(begin + share, bytes);
+  for (uint64_t off = begin; off < end; off += 65536)
+    bulk_prefetch_l2(pf + off, static_cast<uint32_t>(min(static_cast<uint64_t>(65536), end - off)));
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* tm) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
 }

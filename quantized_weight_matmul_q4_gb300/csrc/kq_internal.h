@@ -24,15 +24,15 @@ constexpr int PROD_X = 0;
 constexpr int PROD_SWIGLU = 1;
 constexpr int PROD_RMSNORM = 2;
 // pf: the next call's weights, of which each CTA asks L2 to prefetch its share
-// of pf_bytes (a multiple of 16) while it runs (the Q4_K / Q5_K lane-row
-// kernels; the other kernels ignore it); null for none.
+// of pf_bytes (a multiple of 16) while it runs; null for none.
 cudaError_t launch_matvec(int wtype, const void* W, const float* x, const float* aux, float eps, int prod, float* y,
                           int64_t M, int64_t K, const void* pf, uint64_t pf_bytes, int* err, int num_sms, cudaStream_t s,
                           int* status);
 
-// TQ4_1S decode matvec y = W . x (K a multiple of 32; W 16-byte aligned).
-cudaError_t launch_tq4_matvec(const void* W, const float* x, float* y, int64_t M, int64_t K, int* err, int num_sms,
-                              cudaStream_t s, int* status);
+// TQ4_1S decode matvec y = W . x (K a multiple of 32; W 16-byte aligned); pf
+// as for launch_matvec (the fallback for K % 128 != 0 ignores it).
+cudaError_t launch_tq4_matvec(const void* W, const float* x, float* y, int64_t M, int64_t K, const void* pf,
+                              uint64_t pf_bytes, int* err, int num_sms, cudaStream_t s, int* status);
 
 // Several tokens (Q4_K, 2 <= N <= LR_TOKENS_MAX) on the decode matvec path:
 // Y[N][M] = dequant(W) . X[N][K], the tokens' Q8_1 codes made once into

@@ -52,6 +52,8 @@ struct MatvecParams {
   int rows_per_group;   // rows whose block partials are reduced together
   int xq_bytes;         // int8 activation codes (block-swizzled 16-byte pieces)
   int xds_bytes;        // per-32 activation scales and sums
+  const uint8_t* pf;    // the next call's weights, prefetched into L2 (or null)
+  uint64_t pf_bytes;    // a multiple of 16
   int* err;
 };
 
@@ -324,6 +326,7 @@ __global__ void __launch_bounds__(MV_THREADS, 1) matvec_kernel(const MatvecParam
       const int64_t total = static_cast<int64_t>(n_items) * p.bb;
       for (int c = 0; c < n_chunks; ++c) {
         const int slot = c % p.n_ring;
+        if (c == p.n_ring) prefetch_share_l2(p.pf, p.pf_bytes);  // once the ring is primed
         if (c >= p.n_ring && !mbar_wait(&empty[slot], ((c / p.n_ring) & 1) ^ 1, abort, p.err)) break;
         const int64_t off = static_cast<int64_t>(c) * p.chunk_bytes;
         const uint32_t bytes = static_cast<uint32_t>(min(static_cast<int64_t>(p.chunk_bytes), total - off));
@@ -334,6 +337,7 @@ __global__ void __launch_bounds__(MV_THREADS, 1) matvec_kernel(const MatvecParam
         if (main_bytes) bulk_g2s(dst, base + off, main_bytes, &full[slot]);
         *issued = c + 1;
       }
+      if (n_chunks <= p.n_ring) prefetch_share_l2(p.pf, p.pf_bytes);
       // Every copy lands before the CTA may exit (also when the consumers gave up).
       const int done = *issued;
       for (int sl = 0; sl < min(done, p.n_ring); ++sl) {
@@ -479,16 +483,6 @@ struct MatvecLaneRowParams {
   int* err;
 };
 
-// This CTA's share of an L2 prefetch of pf[0, bytes): one slice per CTA, in
-// pieces of at most 64 KB (issued by one thread; nothing waits for them).
-__device__ __forceinline__ void prefetch_share_l2(const uint8_t* pf, uint64_t bytes) {
-  if (!pf || bytes == 0) return;
-  const uint64_t share = (bytes / gridDim.x + 15) & ~uint64_t(15);
-  const uint64_t begin = static_cast<uint64_t>(blockIdx.x) * share;
-  const uint64_t end = min(begin + share, bytes);
-  for (uint64_t off = begin; off < end; off += 65536)
-    bulk_prefetch_l2(pf + off, static_cast<uint32_t>(min(static_cast<uint64_t>(65536), end - off)));
-}
 
 template <int NW, bool RING, int PROD, int WT = KQ_Q4_K>
 __global__ void __launch_bounds__((NW + 1) * 32, RING ? 2 : 1)
@@ -994,6 +988,8 @@ static cudaError_t launch_matvec_p(int wtype, const void* W, const float* x, con
   p.rows_per_group = MV_PART_MAX / p.nb;
   p.xq_bytes = round_up(p.K, 128);
   p.xds_bytes = round_up((p.K / QK_K) * 8 * 16, 128);
+  p.pf = static_cast<const uint8_t*>(pf);
+  p.pf_bytes = pf_bytes;
   p.err = err;
   if (p.rows_per_group < 1) {
     *status = KQ_ERR_SHAPE;

@@ -206,6 +206,8 @@ struct TqLaneRowParams {
   int S;               // chunk slots
   uint32_t inv_per_chunk, inv_steps, inv_R;  // ceil(2^32 / d) for d = n_groups * steps, steps, R (d >= 2)
   int slot_off, xr_off, part_off, bar_off;   // shared-memory layout (bytes); the pair table sits at 0
+  const uint8_t* pf;                         // the next call's weights, prefetched into L2 (or null)
+  uint64_t pf_bytes;                         // a multiple of 16
   int* err;
 };
 
@@ -245,6 +247,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
       int issued = 0;
       for (int c = 0; c < p.n_chunks; ++c) {
         const int sl = c % p.S;
+        if (c == p.S) prefetch_share_l2(p.pf, p.pf_bytes);  // once the ring is primed
         if (c >= p.S && !mbar_wait(&empty[sl], ((c / p.S) - 1) & 1, abort, p.err)) break;
         const int q0 = c * p.Qc;
         const int nqc = min(p.Qc, p.nq - q0);  // quads past the row end are not copied (never used)
@@ -255,6 +258,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
         issued = c + 1;
         *chunks_issued = issued;
       }
+      if (p.n_chunks <= p.S) prefetch_share_l2(p.pf, p.pf_bytes);
       // Every copy lands before the CTA may exit (also when the consumers gave up).
       for (int sl = 0; sl < min(issued, p.S); ++sl) {
         const int fills = (issued - sl + p.S - 1) / p.S;
@@ -464,8 +468,8 @@ bool plan_tq_lanerow(int64_t M, int64_t K, int num_sms, TqLaneRowParams* p, int*
 
 }  // namespace
 
-cudaError_t launch_tq4_matvec(const void* W, const float* x, float* y, int64_t M, int64_t K, int* err, int num_sms,
-                              cudaStream_t s, int* status) {
+cudaError_t launch_tq4_matvec(const void* W, const float* x, float* y, int64_t M, int64_t K, const void* pf,
+                              uint64_t pf_bytes, int* err, int num_sms, cudaStream_t s, int* status) {
   *status = KQ_OK;
   TqLaneRowParams lp{};
   int grid = 0;
@@ -481,6 +485,8 @@ cudaError_t launch_tq4_matvec(const void* W, const float* x, float* y, int64_t M
     }
     lp.x = x;
     lp.y = y;
+    lp.pf = static_cast<const uint8_t*>(pf);
+    lp.pf_bytes = pf_bytes;
     lp.err = err;
     cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(tq4_lanerow_kernel<TQ_NW>), 24);
     if (e != cudaSuccess) return e;

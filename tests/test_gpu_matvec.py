@@ -116,7 +116,7 @@ def test_prefetch_call_is_bit_identical():
     import torch
     from quantized_weight_matmul_q4_gb300 import kq_matvec_prefetch
     for wtype, name in [("q4_k", "decode_q4k_4096x11008"), ("q5_k", "decode_q5k_11008x4096"),
-                        ("q6_k", "decode_q6k_4096x11008")]:
+                        ("q6_k", "decode_q6k_4096x11008"), ("tq4_1s", "decode_tq4_1s_3584x18944")]:
         wl = syn.make_workload(name, copies=2)
         M, K = wl["M"], wl["K"]
         W = to_dev(wl["W"][0], torch)
