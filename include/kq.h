@@ -121,6 +121,10 @@ KQ_API kq_status kq_quantize_q8_1(const float* X, void* Xq, int64_t K, int64_t N
  * call starts, i.e. by a preceding kernel that allows programmatic dependent
  * launch. (A preceding ordinary kernel, copy or event is always complete.)
  * A Q6_K row whose byte length is not a multiple of 16 must have K <= 15360.
+ * The k-quant decode kernels hold the whole Q8_1 activation in shared memory:
+ * K <= 121600 is always taken; a larger K only when a CTA's rows fit the staged
+ * kernel (few rows), else KQ_ERR_SHAPE with nothing queued. TQ4_1S has no such
+ * limit (its fallback rotates x in segments).
  *
  * wtype KQ_TQ4_1S ([TQ]): W holds rotated weights r_b[j] = c[idx_j] * d_h(j)
  * per 32-block b (c the page's 16-entry centroid table, d0 for j < 16, d1

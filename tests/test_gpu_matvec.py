@@ -127,3 +127,24 @@ def test_prefetch_call_is_bit_identical():
         c = kq_matvec_prefetch(wtype, W, x, M, K, W_next=None)
         torch.cuda.synchronize()
         assert torch.equal(a, b) and torch.equal(a, c), wtype
+
+
+def test_largest_k_for_many_rows():
+    # Many rows (more than a CTA of the staged kernel takes) put the activations
+    # and two ring slots in one CTA's shared memory: K = 121600 is the largest K
+    # that fits; the next multiple of 256 is refused before any launch.
+    import torch
+    import quantized_weight_matmul_q4_gb300 as kq
+    M, K = 20000, 121600
+    rng = np.random.default_rng(9)
+    W = syn.q4_k_weights(rng, M, K)
+    x = syn.activations(rng, K, 1)
+    Wd = to_dev(W, torch)
+    y = kq_matvec("q4_k", Wd, to_dev(x.reshape(-1), torch), M, K).cpu().numpy()
+    rows = np.unique(np.concatenate([rng.choice(M, 48, replace=False), [0, M - 1]]))
+    Yr, B = ora.matmul_rows("q4_k", W, x, K, rows)
+    assert_within_bound(y[rows], Yr[0], B[0], "q4_k 20000x121600")
+    K2 = K + 256
+    W2 = torch.zeros((M, (K2 // 256) * 144), dtype=torch.uint8, device="cuda")
+    with pytest.raises(kq.KQError):
+        kq_matvec("q4_k", W2, torch.zeros(K2, device="cuda"), M, K2)
