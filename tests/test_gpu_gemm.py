@@ -52,7 +52,8 @@ def test_prefill_workloads_full_parity(name):
     assert_within_bound(Y, Yr, B, name)
 
 
-@pytest.mark.parametrize("name", ["prefill_q4k_14336x4096_n2048", "prefill_q6k_4096x14336_n2048"])
+@pytest.mark.parametrize("name", ["prefill_q4k_14336x4096_n2048", "prefill_q6k_4096x14336_n2048",
+                                  "prefill_q5k_14336x4096_n2048"])
 def test_large_workloads_sampled_rows(name):
     wl = syn.make_workload(name)
     M, K = wl["M"], wl["K"]

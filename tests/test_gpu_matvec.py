@@ -18,12 +18,13 @@ def _run(wtype, W, x, M, K):
     return y.cpu().numpy()
 
 
-@pytest.mark.parametrize("name", ["matvec_q4k_512x2048", "decode_q4k_4096x11008", "decode_q4k_11008x4096"])
+@pytest.mark.parametrize("name", ["matvec_q4k_512x2048", "decode_q4k_4096x11008", "decode_q4k_11008x4096",
+                                  "decode_q6k_4096x11008", "decode_q6k_11008x4096"])
 def test_workload_full_parity(name):
     wl = syn.make_workload(name)
     M, K = wl["M"], wl["K"]
-    y = _run("q4_k", wl["W"][0], wl["X"], M, K)
-    Y, B = ora.matmul("q4_k", wl["W"][0], wl["X"], M, K)
+    y = _run(wl["wtype"], wl["W"][0], wl["X"], M, K)
+    Y, B = ora.matmul(wl["wtype"], wl["W"][0], wl["X"], M, K)
     assert_within_bound(y, Y[0], B[0], name)
 
 
