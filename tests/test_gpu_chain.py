@@ -101,3 +101,53 @@ def test_chained_decode_calls(graph):
     for o in outs:
         assert np.all(np.isfinite(o))
     _check_stages(Ws, x0, outs, gamma)
+
+
+GEMM_D, GEMM_N = 2048, 96  # Q6_K on the tensor-core path needs K % 2048 == 0
+GEMM_STAGES = ["q4_k", "q5_k", "q6_k"]
+
+
+@pytest.mark.parametrize("graph", [False, True])
+def test_chained_prefill_calls(graph):
+    # Y_i = W_i . Y_{i-1} for 96 tokens: each call's activation quantiser and
+    # epilogue wait for the previous kernel (programmatic dependent launch).
+    import torch
+    rng = np.random.default_rng(79)
+    Ws = [_scaled(syn.weights(wt, rng, GEMM_D, GEMM_D), wt) for wt in GEMM_STAGES]
+    Wd = [to_dev(W, torch) for W in Ws]
+    X0 = syn.activations(rng, GEMM_D, GEMM_N)
+    X0d = to_dev(X0, torch)
+    ws = [torch.empty(kq.kq_workspace_bytes(kq.KQ_OP_GEMM, wt, GEMM_D, GEMM_D, GEMM_N), dtype=torch.uint8,
+                      device="cuda") for wt in GEMM_STAGES]
+    Ys = [torch.empty((GEMM_N, GEMM_D), dtype=torch.float32, device="cuda") for _ in GEMM_STAGES]
+
+    def chain():
+        x = X0d
+        for i, wt in enumerate(GEMM_STAGES):
+            kq.kq_gemm(wt, Wd[i], x, GEMM_D, GEMM_D, Y=Ys[i], ws=ws[i])
+            x = Ys[i]
+
+    if graph:
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            chain()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        for y in Ys:
+            y.fill_(float("nan"))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            chain()
+        g.replay()
+    else:
+        chain()
+    torch.cuda.synchronize()
+    assert kq.kq_get_device_error() == 0
+    x = X0
+    for i, wt in enumerate(GEMM_STAGES):
+        out = Ys[i].cpu().numpy()
+        assert np.all(np.isfinite(out)), wt
+        Yr, B = ora.matmul(wt, Ws[i], x, GEMM_D, GEMM_D)
+        assert_within_bound(out, Yr, B, f"prefill stage {i} ({wt})")
+        x = out
