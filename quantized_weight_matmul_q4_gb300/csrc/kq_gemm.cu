@@ -15,7 +15,7 @@
 //    stage) with 2-D TMA, warp 22 streams x_hat tiles (128-byte swizzle) with
 //    2-D TMA, each into its own mbarrier ring;
 //  * warps 0-15 (two groups of 8 taking alternate K steps, so two steps are
-//    unpacked at once) unpack Q4_K / Q6_K to fp16 and store the A operand straight
+//    unpacked at once) unpack Q4_K / Q5_K / Q6_K to fp16 and store the A operand straight
 //    into tensor memory (tcgen05.st; the page unpacks into shared memory), four
 //    64-wide K steps per super-block: the weights never pass through shared
 //    memory as fp16, which leaves its bandwidth to the x_hat tiles the MMA

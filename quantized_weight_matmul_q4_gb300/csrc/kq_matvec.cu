@@ -1,5 +1,7 @@
-// Decode matvec y[M] = dequant(W)[M,K] . x[K] for Q4_K and Q6_K weights, with
-// the fp32 -> Q8_1 quantisation of x fused in.
+// Decode matvec y[M] = dequant(W)[M,K] . x[K] for Q4_K, Q5_K and Q6_K weights,
+// with the fp32 -> Q8_1 quantisation of x (and optionally its RMSNorm or
+// SwiGLU producer) fused in. Q5_K is the Q4_K value with a fifth bit per code
+// (the page's "one kernel per type" sibling), read with the GGUF block layout.
 //
 // Method: "06 · 8e/8e② — decode MMVQ: dp4a integer dot products + the
 // llama.cpp launch table", §2 Principle and §3.2 Key code: per 32-weight
@@ -16,7 +18,9 @@
 // shared memory while the first chunks land; then each thread takes whole
 // super-blocks (row, block) in arrival order, so a block's header is decoded
 // once for its 256 weights, and writes one partial sum per block; each row's
-// partials are added in a fixed order at the end (deterministic).
+// partials are added in a fixed order at the end (deterministic). That is the
+// item kernel (matvec_kernel); the lane-row kernel further down stages whole row
+// ranges by TMA and is the one the decode shapes take for Q4_K and Q5_K.
 #include <algorithm>
 
 #include "kq_internal.h"
