@@ -36,6 +36,9 @@ def test_workload_full_parity():
     ("q6_k", 4, 136, 2048, 50, 2),
     ("q4_k", 6, 256, 512, 300, 2),     # buckets of more than one 128-token tile
     ("q6_k", 3, 512, 2048, 70, 3),
+    ("q4_k", 1, 128, 256, 1, 1),       # one expert, one token
+    ("q4_k", 1, 256, 512, 300, 1),     # every token to the only expert: a bucket of several tiles
+    ("q4_k", 512, 128, 256, 20, 4),    # the most experts the call takes; nearly all get no token
 ])
 def test_small_shapes_full_parity(wtype, E, M, K, T, top_k):
     rng = np.random.default_rng(E * 100 + T)
