@@ -1045,11 +1045,11 @@ cudaError_t launch_gemm(int wtype, const void* W, const float* X, float* Y, int6
                         void* ws, const GemmPlan& plan, int* err, cudaStream_t s, int* status) {
   *status = KQ_OK;
   // A few tokens are a decode, not a GEMM: the tensor-core tiles would be
-  // nearly empty, so Q4_K runs on the matvec path, which streams the weights
-  // once and multiplies each staged block with every token.
-  if (wtype == KQ_Q4_K && N <= LR_TOKENS_MAX) {
+  // nearly empty, so Q4_K and Q5_K run on the matvec path, which streams the
+  // weights once and multiplies each staged block with every token.
+  if ((wtype == KQ_Q4_K || wtype == KQ_Q5_K) && N <= LR_TOKENS_MAX) {
     bool handled = false;
-    cudaError_t e = launch_matvec_tokens(W, X, Y, M, K, N, ws, plan.xhat_bytes, err, plan.num_sms, s, &handled);
+    cudaError_t e = launch_matvec_tokens(wtype, W, X, Y, M, K, N, ws, plan.xhat_bytes, err, plan.num_sms, s, &handled);
     if (e != cudaSuccess || handled) return e;
   }
   uint8_t* wsb = static_cast<uint8_t*>(ws);

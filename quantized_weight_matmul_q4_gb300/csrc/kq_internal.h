@@ -34,13 +34,13 @@ cudaError_t launch_matvec(int wtype, const void* W, const float* x, const float*
 cudaError_t launch_tq4_matvec(const void* W, const float* x, float* y, int64_t M, int64_t K, const void* pf,
                               uint64_t pf_bytes, int* err, int num_sms, cudaStream_t s, int* status);
 
-// Several tokens (Q4_K, 2 <= N <= LR_TOKENS_MAX) on the decode matvec path:
+// Several tokens (Q4_K or Q5_K, 2 <= N <= LR_TOKENS_MAX) on the decode matvec path:
 // Y[N][M] = dequant(W) . X[N][K], the tokens' Q8_1 codes made once into
 // `scratch` (device memory; at most ~1.25 N K + 256 N bytes are used);
 // *handled = false when the shape or the scratch does not suit it (nothing
 // queued).
 constexpr int LR_TOKENS_MAX = 5;  // measured crossover with the tensor-core GEMM at the decode shapes
-cudaError_t launch_matvec_tokens(const void* W, const float* X, float* Y, int64_t M, int64_t K, int64_t N,
+cudaError_t launch_matvec_tokens(int wtype, const void* W, const float* X, float* Y, int64_t M, int64_t K, int64_t N,
                                  void* scratch, size_t scratch_bytes, int* err, int num_sms, cudaStream_t s,
                                  bool* handled);
 
@@ -79,7 +79,7 @@ cudaError_t device_context(int* dev, int* num_sms, int** err);
 // Raises a kernel's dynamic shared-memory limit to the 227 KB maximum, once per
 // device (later calls only read a flag, so launches stay cheap and capturable).
 cudaError_t allow_max_smem(const void* kernel, int slot);
-constexpr int kSmemSlots = 35;
+constexpr int kSmemSlots = 37;
 
 // Launches `kernel` on `s` with programmatic stream serialization allowed (the
 // kernel calls pdl_enter() before its first global memory access).

@@ -721,9 +721,12 @@ __global__ void __launch_bounds__((NW + 1) * 32, RING ? 2 : 1)
 // row-group sums, as in the one-token kernel. The weights are read from HBM once
 // whatever the number of tokens; later passes reuse them.
 // ---------------------------------------------------------------------------
-template <int NT>
+template <int NT, int WT = KQ_Q4_K>
 __global__ void __launch_bounds__((LR_NW_FULL + 1) * 32, 1)
     matvec_q4k_lanerow_tokens_kernel(const __grid_constant__ CUtensorMap tmW, const MatvecLaneRowParams p) {
+  static_assert(WT == KQ_Q4_K || WT == KQ_Q5_K, "Q4_K or Q5_K super-blocks");
+  constexpr int BB = (WT == KQ_Q5_K) ? Q5K_BYTES : Q4K_BYTES;  // bytes per super-block
+  constexpr int QS = (WT == KQ_Q5_K) ? 48 : 16;                // byte offset of the nibbles
   constexpr int NW = LR_NW_FULL;  // divisible by 1, 2, 3 and 4
   static_assert(NT >= 1 && NT <= 4 && NW % 12 == 0, "token split of the warps");
   constexpr int LR_CT = NW * 32;
@@ -751,10 +754,10 @@ __global__ void __launch_bounds__((LR_NW_FULL + 1) * 32, 1)
   if (warp == NW) {
     if (lane == 0) {
       tma_prefetch_desc(&tmW);
-      const uint32_t box = static_cast<uint32_t>(p.R * p.cb * Q4K_BYTES);
+      const uint32_t box = static_cast<uint32_t>(p.R * p.cb * BB);
       for (int c = 0; c < p.n_chunks; ++c) {
         mbar_expect_tx(&full[c], box);
-        tma_load_2d(smem + static_cast<size_t>(c) * p.chunk_bytes, &tmW, &full[c], c * p.cb * (Q4K_BYTES / 4), r0);
+        tma_load_2d(smem + static_cast<size_t>(c) * p.chunk_bytes, &tmW, &full[c], c * p.cb * (BB / 4), r0);
       }
       // Every copy lands before the CTA may exit (also when the consumers gave up).
       for (int c = 0; c < p.n_chunks; ++c)
@@ -765,7 +768,7 @@ __global__ void __launch_bounds__((LR_NW_FULL + 1) * 32, 1)
 
   asm volatile("griddepcontrol.wait;" ::: "memory");  // x may come from the previous kernel
 
-  const int pitch = p.cb * Q4K_BYTES;
+  const int pitch = p.cb * BB;
   const int items = p.n_chunks * per_chunk;
   for (int t0 = 0, pass = 0; t0 < p.n_tok; t0 += NT, ++pass) {
     const int tn = min(NT, p.n_tok - t0);  // tokens of this pass
@@ -796,7 +799,7 @@ __global__ void __launch_bounds__((LR_NW_FULL + 1) * 32, 1)
         ready = c;
       }
       const int srow = min(32 * g + lane, p.R - 1);  // lanes past the last row repeat it; dropped
-      const uint8_t* blk = smem + static_cast<size_t>(c) * p.chunk_bytes + srow * pitch + j * Q4K_BYTES;
+      const uint8_t* blk = smem + static_cast<size_t>(c) * p.chunk_bytes + srow * pitch + j * BB;
       const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
       const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x & 0xFFFFu)));
       const float dmin = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x >> 16)));
@@ -805,15 +808,37 @@ __global__ void __launch_bounds__((LR_NW_FULL + 1) * 32, 1)
       const uint32_t m_hi = ((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u);
       const int8_t* xb = xqt + (b << 8);
       float lo = 0.f, mn = 0.f;
+      uint4 ha, hb;  // Q5_K: qh[0..15], qh[16..31]
+      if (WT == KQ_Q5_K) {
+        ha = *reinterpret_cast<const uint4*>(blk + 16);
+        hb = *reinterpret_cast<const uint4*>(blk + 32);
+      }
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const uint4 qa = *reinterpret_cast<const uint4*>(blk + 16 + 32 * q);
-        const uint4 qb = *reinterpret_cast<const uint4*>(blk + 32 + 32 * q);
+        const uint4 qa = *reinterpret_cast<const uint4*>(blk + QS + 32 * q);
+        const uint4 qb = *reinterpret_cast<const uint4*>(blk + QS + 16 + 32 * q);
         const int4 x0 = *reinterpret_cast<const int4*>(xb + 64 * q);
         const int4 x1 = *reinterpret_cast<const int4*>(xb + 64 * q + 16);
         const int4 x2 = *reinterpret_cast<const int4*>(xb + 64 * q + 32);
         const int4 x3 = *reinterpret_cast<const int4*>(xb + 64 * q + 48);
         const float4 ds = xs4[(b << 2) + q];  // {d8, s} of sub-blocks 2q and 2q+1
+        const uint32_t scw = (q < 2) ? sc_lo : sc_hi;
+        const uint32_t mw = (q < 2) ? m_lo : m_hi;
+        const int sh = (q & 1) * 16;
+        const int scA = (scw >> sh) & 0xFF, scB = (scw >> (sh + 8)) & 0xFF;
+        const int mA = (mw >> sh) & 0xFF, mB = (mw >> (sh + 8)) & 0xFF;
+        if (WT == KQ_Q5_K) {
+          int dA, dB;
+          if (q == 0) q5_chunk_dots<0>(qa, qb, ha, hb, x0, x1, x2, x3, dA, dB);
+          else if (q == 1) q5_chunk_dots<2>(qa, qb, ha, hb, x0, x1, x2, x3, dA, dB);
+          else if (q == 2) q5_chunk_dots<4>(qa, qb, ha, hb, x0, x1, x2, x3, dA, dB);
+          else q5_chunk_dots<6>(qa, qb, ha, hb, x0, x1, x2, x3, dA, dB);
+          lo = fmaf(ds.x, i2f(scA * dA), lo);
+          lo = fmaf(ds.z, i2f(scB * dB), lo);
+          mn = fmaf(ds.y, i2f(mA), mn);
+          mn = fmaf(ds.w, i2f(mB), mn);
+          continue;
+        }
         int a0 = __dp4a(static_cast<int>(qa.x & 0x0F0F0F0Fu), x0.x, 0);
         int a1 = __dp4a(static_cast<int>(qb.x & 0x0F0F0F0Fu), x1.x, 0);
         int h0 = dp4a_us(qa.x & 0xF0F0F0F0u, x2.x, 0);
@@ -830,11 +855,6 @@ __global__ void __launch_bounds__((LR_NW_FULL + 1) * 32, 1)
         a1 = __dp4a(static_cast<int>(qb.w & 0x0F0F0F0Fu), x1.w, a1);
         h0 = dp4a_us(qa.w & 0xF0F0F0F0u, x2.w, h0);
         h1 = dp4a_us(qb.w & 0xF0F0F0F0u, x3.w, h1);
-        const uint32_t scw = (q < 2) ? sc_lo : sc_hi;
-        const uint32_t mw = (q < 2) ? m_lo : m_hi;
-        const int sh = (q & 1) * 16;
-        const int scA = (scw >> sh) & 0xFF, scB = (scw >> (sh + 8)) & 0xFF;
-        const int mA = (mw >> sh) & 0xFF, mB = (mw >> (sh + 8)) & 0xFF;
         lo = fmaf(ds.x, i2f(scA * (a0 + a1)), lo);
         lo = fmaf(ds.z, i2f(scB * ((h0 + h1) >> 4)), lo);
         mn = fmaf(ds.y, i2f(mA), mn);
@@ -1070,27 +1090,37 @@ __global__ void __launch_bounds__(256) quantize_split_kernel(const float* __rest
   }
 }
 
-// Q4_K for N = 2 .. LR_TOKENS_MAX tokens: the staged lane-row kernel with
-// LR_NT (else two) tokens per pass. *handled = false (nothing queued) when the
-// rows do not fit staged next to the activations of two tokens.
-cudaError_t launch_matvec_tokens(const void* W, const float* X, float* Y, int64_t M, int64_t K, int64_t N,
+// Q4_K and Q5_K for N = 2 .. LR_TOKENS_MAX tokens: the staged lane-row kernel
+// with LR_NT (else two) tokens per pass. *handled = false (nothing queued) when
+// the rows do not fit staged next to the activations of two tokens.
+template <int NT, int WT>
+static cudaError_t launch_tokens_kernel(const CUtensorMap& tmW, const MatvecLaneRowParams& lp, int grid, size_t smem,
+                                        cudaStream_t s) {
+  const int slot = WT == KQ_Q5_K ? (NT == LR_NT ? 35 : 36) : (NT == LR_NT ? 11 : 14);
+  cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(matvec_q4k_lanerow_tokens_kernel<NT, WT>), slot);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(matvec_q4k_lanerow_tokens_kernel<NT, WT>, dim3(grid), dim3((LR_NW_FULL + 1) * 32), smem, s, tmW,
+                    lp);
+}
+
+cudaError_t launch_matvec_tokens(int wtype, const void* W, const float* X, float* Y, int64_t M, int64_t K, int64_t N,
                                  void* scratch, size_t scratch_bytes, int* err, int num_sms, cudaStream_t s,
                                  bool* handled) {
   *handled = false;
-  if (N < 2 || N > LR_TOKENS_MAX) return cudaSuccess;
+  if (N < 2 || N > LR_TOKENS_MAX || (wtype != KQ_Q4_K && wtype != KQ_Q5_K)) return cudaSuccess;
+  const int bb = wtype == KQ_Q5_K ? Q5K_BYTES : Q4K_BYTES;
   MatvecLaneRowParams lp{};
   size_t smem = 0;
   int grid = 0;
   int nt = LR_NT;
-  if (!plan_lanerow(M, K, num_sms, LR_NW_FULL, nt, MV_SMEM_LIMIT, false, &lp, &grid, &smem)) {
+  if (!plan_lanerow(M, K, num_sms, LR_NW_FULL, nt, MV_SMEM_LIMIT, false, &lp, &grid, &smem, bb)) {
     nt = 2;
-    if (!plan_lanerow(M, K, num_sms, LR_NW_FULL, nt, MV_SMEM_LIMIT, false, &lp, &grid, &smem)) return cudaSuccess;
+    if (!plan_lanerow(M, K, num_sms, LR_NW_FULL, nt, MV_SMEM_LIMIT, false, &lp, &grid, &smem, bb)) return cudaSuccess;
   }
   CUtensorMap tmW;
-  const uint64_t rs = static_cast<uint64_t>(lp.nb) * Q4K_BYTES;
+  const uint64_t rs = static_cast<uint64_t>(lp.nb) * bb;
   if (!encode_tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT32, W, rs / 4, static_cast<uint64_t>(M), rs,
-                      static_cast<uint32_t>(lp.cb * Q4K_BYTES / 4), static_cast<uint32_t>(lp.R),
-                      CU_TENSOR_MAP_SWIZZLE_NONE))
+                      static_cast<uint32_t>(lp.cb * bb / 4), static_cast<uint32_t>(lp.R), CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaSuccess;
   const size_t xq_bytes = static_cast<size_t>(N) * lp.xq_tok, xs_bytes = static_cast<size_t>(N) * lp.xs_tok;
   if (xq_bytes + xs_bytes > scratch_bytes) return cudaSuccess;
@@ -1111,15 +1141,10 @@ cudaError_t launch_matvec_tokens(const void* W, const float* X, float* Y, int64_
                                static_cast<int>(N), static_cast<int>(K), lp.xq_tok, lp.xs_tok, xq_g, xs_g);
     if (e != cudaSuccess) return e;
   }
-  if (nt == LR_NT) {
-    cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(matvec_q4k_lanerow_tokens_kernel<LR_NT>), 11);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(matvec_q4k_lanerow_tokens_kernel<LR_NT>, dim3(grid), dim3((LR_NW_FULL + 1) * 32), smem, s,
-                      tmW, lp);
-  }
-  cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(matvec_q4k_lanerow_tokens_kernel<2>), 14);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(matvec_q4k_lanerow_tokens_kernel<2>, dim3(grid), dim3((LR_NW_FULL + 1) * 32), smem, s, tmW, lp);
+  if (wtype == KQ_Q5_K)
+    return nt == LR_NT ? launch_tokens_kernel<LR_NT, KQ_Q5_K>(tmW, lp, grid, smem, s)
+                       : launch_tokens_kernel<2, KQ_Q5_K>(tmW, lp, grid, smem, s);
+  return nt == LR_NT ? launch_tokens_kernel<LR_NT, KQ_Q4_K>(tmW, lp, grid, smem, s)
+                     : launch_tokens_kernel<2, KQ_Q4_K>(tmW, lp, grid, smem, s);
 }
-
 }  // namespace kq

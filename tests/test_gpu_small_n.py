@@ -1,6 +1,6 @@
 """Small-N decode (2 to 16 tokens at once) against the oracle, element by
 element, within |y - y_ref| <= 1e-3 * Sum_k |w_k x_k| + 1e-5. Through the
-public GEMM entry point: Q4_K with 2 <= N <= 5 runs on the decode matvec path
+public GEMM entry point: Q4_K and Q5_K with 2 <= N <= 5 run on the decode matvec path
 ("06 · 8e/8e② — decode MMVQ", §2 Principle: dp4a integer dots, the min term
 from the Q8_1 block sum), the staged weights multiplied with every token;
 larger N (the N = 8 and 16 cases) on the tensor-core GEMM."""
@@ -14,9 +14,9 @@ from _kqutil import assert_within_bound, to_dev
 pytestmark = pytest.mark.gpu
 
 
-def _run(W, X, M, K):
+def _run(W, X, M, K, wtype="q4_k"):
     import torch
-    Y = kq_gemm("q4_k", to_dev(W, torch), to_dev(X, torch), M, K)
+    Y = kq_gemm(wtype, to_dev(W, torch), to_dev(X, torch), M, K)
     torch.cuda.synchronize()
     return Y.cpu().numpy()
 
@@ -66,3 +66,15 @@ def test_small_n_deterministic_and_per_token():
     Yr, B = ora.matmul("q4_k", W, sub, M, K)
     assert_within_bound(c, Yr, B, "three tokens")
     assert_within_bound(a[[3, 0, 5]], Yr, B, "the same tokens among six")
+
+
+@pytest.mark.parametrize("M,K,N", [(512, 2048, 2), (300, 1024, 3), (777, 2816, 5), (4096, 11008, 4)])
+def test_small_n_q5k(M, K, N):
+    # Q5_K takes the same matvec path (its fifth bits merged into each dp4a word).
+    rng = np.random.default_rng(M + 11 * N)
+    W = syn.q5_k_weights(rng, M, K)
+    X = syn.activations(rng, K, N)
+    Y = _run(W, X, M, K, "q5_k")
+    rows = np.arange(M) if M <= 1000 else np.sort(np.concatenate([rng.choice(M, 160, replace=False), [0, M - 1]]))
+    Yr, B = ora.matmul_rows("q5_k", W, X, K, rows)
+    assert_within_bound(Y[:, rows], Yr, B, f"q5_k {M}x{K} N={N}")
