@@ -180,7 +180,7 @@ KQ_API kq_status kq_matvec_rmsnorm(int wtype, const void* W, const float* x, con
  * architecture; [GAP] T1). X is quantised to Q8_1 (as x_hat = fp16(d_h * q))
  * into the workspace once per call; weight super-blocks are staged by TMA and
  * unpacked to fp16 into tensor memory; tcgen05 MMAs accumulate in tensor memory.
- * A few tokens are a decode rather than a GEMM: Q4_K and Q5_K with 2 <= N <= 5 run on
+ * A few tokens are a decode rather than a GEMM: Q4_K and Q5_K with 2 <= N <= 7 run on
  * the decode matvec path instead ([MMVQ] §2: dp4a on the Q8_1 codes, the min
  * term from the block sums; the tokens' codes are made once into the
  * workspace, the weights are read once for all tokens). Both paths meet the

@@ -39,7 +39,7 @@ cudaError_t launch_tq4_matvec(const void* W, const float* x, float* y, int64_t M
 // `scratch` (device memory; at most ~1.25 N K + 256 N bytes are used);
 // *handled = false when the shape or the scratch does not suit it (nothing
 // queued).
-constexpr int LR_TOKENS_MAX = 5;  // measured crossover with the tensor-core GEMM at the decode shapes
+constexpr int LR_TOKENS_MAX = 7;  // measured crossover with the tensor-core GEMM at the decode shapes
 cudaError_t launch_matvec_tokens(int wtype, const void* W, const float* X, float* Y, int64_t M, int64_t K, int64_t N,
                                  void* scratch, size_t scratch_bytes, int* err, int num_sms, cudaStream_t s,
                                  bool* handled);

@@ -458,6 +458,7 @@ __global__ void __launch_bounds__(MV_THREADS, 1) matvec_kernel(const MatvecParam
 // whole.
 constexpr int LR_NW_FULL = 24;
 constexpr int LR_NW_RING = 14;
+constexpr int LR_NW_TOK = 16;               // consumer warps of the several-token kernel
 constexpr int LR_RING_SMEM = 113 * 1024;     // two CTAs per SM (228 KB, 1 KB reserved per CTA)
 constexpr int LR_MAX_ROWS = 128;             // rows per CTA: at most four row groups
 constexpr int LR_XT = 2;                     // 8-value activation tasks loaded per thread per round
@@ -474,6 +475,7 @@ struct MatvecLaneRowParams {
   int R;            // rows per CTA
   int n_groups;     // ceil(R / 32)
   int cb;           // super-blocks per chunk (odd)
+  int tail_cb;      // super-blocks in the last chunk's slot (cb, or only the rest when the plan trims it)
   int n_chunks;     // ceil(nb / cb)
   int chunk_bytes;  // shared-memory stride of a chunk (R * cb * 144 rounded up to 128)
   int S;            // chunk slots (== n_chunks: everything staged at once; fewer: a ring)
@@ -715,20 +717,21 @@ __global__ void __launch_bounds__((NW + 1) * 32, RING ? 2 : 1)
 // and arithmetic as the kernel above (staged form only); y is [n_tok][M]. The
 // tokens' Q8_1 codes and {d8, s} pairs are made once per call by
 // quantize_split_kernel (below) in exactly the shared-memory layout, and a pass
-// pulls up to NT tokens of them with two bulk copies. Warp w serves token
-// w % tn of the pass and takes every (24 / tn)-th work item of the CTA, so each
-// token's items are spread over several warps and a warp keeps one set of
-// row-group sums, as in the one-token kernel. The weights are read from HBM once
-// whatever the number of tokens; later passes reuse them.
+// pulls up to NT tokens of them with two bulk copies. Warp w takes every 16th
+// work item of the CTA, unpacks the item's codes
+// once and multiplies them with every token of the pass, keeping one set of
+// row-group sums per token. The weights are read from HBM once whatever the
+// number of tokens; later passes reuse them.
 // ---------------------------------------------------------------------------
 template <int NT, int WT = KQ_Q4_K>
-__global__ void __launch_bounds__((LR_NW_FULL + 1) * 32, 1)
-    matvec_q4k_lanerow_tokens_kernel(const __grid_constant__ CUtensorMap tmW, const MatvecLaneRowParams p) {
+__global__ void __launch_bounds__((LR_NW_TOK + 1) * 32, 1)
+    matvec_q4k_lanerow_tokens_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmT,
+                                     const MatvecLaneRowParams p) {
   static_assert(WT == KQ_Q4_K || WT == KQ_Q5_K, "Q4_K or Q5_K super-blocks");
   constexpr int BB = (WT == KQ_Q5_K) ? Q5K_BYTES : Q4K_BYTES;  // bytes per super-block
   constexpr int QS = (WT == KQ_Q5_K) ? 48 : 16;                // byte offset of the nibbles
-  constexpr int NW = LR_NW_FULL;  // divisible by 1, 2, 3 and 4
-  static_assert(NT >= 1 && NT <= 4 && NW % 12 == 0, "token split of the warps");
+  constexpr int NW = LR_NW_TOK;
+  static_assert(NT >= 1 && NT <= 4, "tokens per pass");
   constexpr int LR_CT = NW * 32;
   extern __shared__ __align__(1024) uint8_t smem[];
   int8_t* xq = reinterpret_cast<int8_t*>(smem + p.xq_off);           // [NT][xq_tok]
@@ -754,10 +757,14 @@ __global__ void __launch_bounds__((LR_NW_FULL + 1) * 32, 1)
   if (warp == NW) {
     if (lane == 0) {
       tma_prefetch_desc(&tmW);
-      const uint32_t box = static_cast<uint32_t>(p.R * p.cb * BB);
+      tma_prefetch_desc(&tmT);
+      // The last chunk comes through tmT, whose box holds only its tail_cb
+      // super-blocks (its slot is sized for them).
       for (int c = 0; c < p.n_chunks; ++c) {
-        mbar_expect_tx(&full[c], box);
-        tma_load_2d(smem + static_cast<size_t>(c) * p.chunk_bytes, &tmW, &full[c], c * p.cb * (BB / 4), r0);
+        const bool last = c == p.n_chunks - 1;
+        mbar_expect_tx(&full[c], static_cast<uint32_t>(p.R * (last ? p.tail_cb : p.cb) * BB));
+        tma_load_2d(smem + static_cast<size_t>(c) * p.chunk_bytes, last ? &tmT : &tmW, &full[c], c * p.cb * (BB / 4),
+                    r0);
       }
       // Every copy lands before the CTA may exit (also when the consumers gave up).
       for (int c = 0; c < p.n_chunks; ++c)
@@ -768,7 +775,7 @@ __global__ void __launch_bounds__((LR_NW_FULL + 1) * 32, 1)
 
   asm volatile("griddepcontrol.wait;" ::: "memory");  // x may come from the previous kernel
 
-  const int pitch = p.cb * BB;
+  const int pitch = p.cb * BB;  // row stride of a chunk; the last chunk's is tail_cb * BB
   const int items = p.n_chunks * per_chunk;
   for (int t0 = 0, pass = 0; t0 < p.n_tok; t0 += NT, ++pass) {
     const int tn = min(NT, p.n_tok - t0);  // tokens of this pass
@@ -781,13 +788,17 @@ __global__ void __launch_bounds__((LR_NW_FULL + 1) * 32, 1)
     }
     if (!mbar_wait(x_full, pass & 1, abort, p.err)) break;
 
-    const int wpt = NW / tn;          // warps per token
-    const int tt = warp % tn, wi = warp / tn;
-    const int8_t* xqt = xq + tt * p.xq_tok;
-    const float4* xs4 = reinterpret_cast<const float4*>(xsb + tt * p.xs_tok);
-    int ready = -1;                       // last chunk this warp has seen land (later passes: at once)
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};  // this warp's sums for row groups 0..3
-    for (int i = wi; i < items; i += wpt) {
+    // Warp w takes every NW-th work item and multiplies the item's codes with
+    // each token of the pass: a block's nibbles (and Q5_K high bits) are
+    // unpacked once per pass, then each token costs its activation loads, 16
+    // dp4a per 64 weights and the scale arithmetic.
+    int ready = -1;  // last chunk this warp has seen land (later passes: at once)
+    float acc[NT][4];
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc[t][k] = 0.f;
+    for (int i = warp; i < items; i += NW) {
       const int c = static_cast<int>(__umulhi(static_cast<uint32_t>(i), p.inv_per_chunk));
       const int rem = i - c * per_chunk;
       const int g = static_cast<int>(__umulhi(static_cast<uint32_t>(rem), p.inv_cb));
@@ -799,15 +810,17 @@ __global__ void __launch_bounds__((LR_NW_FULL + 1) * 32, 1)
         ready = c;
       }
       const int srow = min(32 * g + lane, p.R - 1);  // lanes past the last row repeat it; dropped
-      const uint8_t* blk = smem + static_cast<size_t>(c) * p.chunk_bytes + srow * pitch + j * BB;
+      const int rp = (c == p.n_chunks - 1) ? p.tail_cb * BB : pitch;
+      const uint8_t* blk = smem + static_cast<size_t>(c) * p.chunk_bytes + srow * rp + j * BB;
       const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
       const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x & 0xFFFFu)));
       const float dmin = __half2float(__ushort_as_half(static_cast<unsigned short>(hdr.x >> 16)));
       const uint32_t sc_lo = hdr.y & 0x3F3F3F3Fu, m_lo = hdr.z & 0x3F3F3F3Fu;
       const uint32_t sc_hi = (hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u);
       const uint32_t m_hi = ((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u);
-      const int8_t* xb = xqt + (b << 8);
-      float lo = 0.f, mn = 0.f;
+      float lo[NT], mn[NT];
+#pragma unroll
+      for (int t = 0; t < NT; ++t) lo[t] = mn[t] = 0.f;
       uint4 ha, hb;  // Q5_K: qh[0..15], qh[16..31]
       if (WT == KQ_Q5_K) {
         ha = *reinterpret_cast<const uint4*>(blk + 16);
@@ -817,63 +830,106 @@ __global__ void __launch_bounds__((LR_NW_FULL + 1) * 32, 1)
       for (int q = 0; q < 4; ++q) {
         const uint4 qa = *reinterpret_cast<const uint4*>(blk + QS + 32 * q);
         const uint4 qb = *reinterpret_cast<const uint4*>(blk + QS + 16 + 32 * q);
-        const int4 x0 = *reinterpret_cast<const int4*>(xb + 64 * q);
-        const int4 x1 = *reinterpret_cast<const int4*>(xb + 64 * q + 16);
-        const int4 x2 = *reinterpret_cast<const int4*>(xb + 64 * q + 32);
-        const int4 x3 = *reinterpret_cast<const int4*>(xb + 64 * q + 48);
-        const float4 ds = xs4[(b << 2) + q];  // {d8, s} of sub-blocks 2q and 2q+1
         const uint32_t scw = (q < 2) ? sc_lo : sc_hi;
         const uint32_t mw = (q < 2) ? m_lo : m_hi;
         const int sh = (q & 1) * 16;
         const int scA = (scw >> sh) & 0xFF, scB = (scw >> (sh + 8)) & 0xFF;
         const int mA = (mw >> sh) & 0xFF, mB = (mw >> (sh + 8)) & 0xFF;
+        // codes of sub-block 2q (cl, against x[64q .. 64q+31]) and 2q+1 (ch,
+        // against x[64q+32 .. 64q+63]); Q4_K keeps the high nibbles in place
+        // (their dots are 16x the code dots)
+        uint32_t cl[8], ch[8];
         if (WT == KQ_Q5_K) {
-          int dA, dB;
-          if (q == 0) q5_chunk_dots<0>(qa, qb, ha, hb, x0, x1, x2, x3, dA, dB);
-          else if (q == 1) q5_chunk_dots<2>(qa, qb, ha, hb, x0, x1, x2, x3, dA, dB);
-          else if (q == 2) q5_chunk_dots<4>(qa, qb, ha, hb, x0, x1, x2, x3, dA, dB);
-          else q5_chunk_dots<6>(qa, qb, ha, hb, x0, x1, x2, x3, dA, dB);
-          lo = fmaf(ds.x, i2f(scA * dA), lo);
-          lo = fmaf(ds.z, i2f(scB * dB), lo);
-          mn = fmaf(ds.y, i2f(mA), mn);
-          mn = fmaf(ds.w, i2f(mB), mn);
-          continue;
+          const uint32_t w[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+          const uint32_t h[8] = {ha.x, ha.y, ha.z, ha.w, hb.x, hb.y, hb.z, hb.w};
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            if (q == 0) { cl[e] = q5_codes<true, 0>(w[e], h[e]); ch[e] = q5_codes<false, 1>(w[e], h[e]); }
+            else if (q == 1) { cl[e] = q5_codes<true, 2>(w[e], h[e]); ch[e] = q5_codes<false, 3>(w[e], h[e]); }
+            else if (q == 2) { cl[e] = q5_codes<true, 4>(w[e], h[e]); ch[e] = q5_codes<false, 5>(w[e], h[e]); }
+            else { cl[e] = q5_codes<true, 6>(w[e], h[e]); ch[e] = q5_codes<false, 7>(w[e], h[e]); }
+          }
+        } else {
+          const uint32_t w[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            cl[e] = w[e] & 0x0F0F0F0Fu;
+            ch[e] = w[e] & 0xF0F0F0F0u;
+          }
         }
-        int a0 = __dp4a(static_cast<int>(qa.x & 0x0F0F0F0Fu), x0.x, 0);
-        int a1 = __dp4a(static_cast<int>(qb.x & 0x0F0F0F0Fu), x1.x, 0);
-        int h0 = dp4a_us(qa.x & 0xF0F0F0F0u, x2.x, 0);
-        int h1 = dp4a_us(qb.x & 0xF0F0F0F0u, x3.x, 0);
-        a0 = __dp4a(static_cast<int>(qa.y & 0x0F0F0F0Fu), x0.y, a0);
-        a1 = __dp4a(static_cast<int>(qb.y & 0x0F0F0F0Fu), x1.y, a1);
-        h0 = dp4a_us(qa.y & 0xF0F0F0F0u, x2.y, h0);
-        h1 = dp4a_us(qb.y & 0xF0F0F0F0u, x3.y, h1);
-        a0 = __dp4a(static_cast<int>(qa.z & 0x0F0F0F0Fu), x0.z, a0);
-        a1 = __dp4a(static_cast<int>(qb.z & 0x0F0F0F0Fu), x1.z, a1);
-        h0 = dp4a_us(qa.z & 0xF0F0F0F0u, x2.z, h0);
-        h1 = dp4a_us(qb.z & 0xF0F0F0F0u, x3.z, h1);
-        a0 = __dp4a(static_cast<int>(qa.w & 0x0F0F0F0Fu), x0.w, a0);
-        a1 = __dp4a(static_cast<int>(qb.w & 0x0F0F0F0Fu), x1.w, a1);
-        h0 = dp4a_us(qa.w & 0xF0F0F0F0u, x2.w, h0);
-        h1 = dp4a_us(qb.w & 0xF0F0F0F0u, x3.w, h1);
-        lo = fmaf(ds.x, i2f(scA * (a0 + a1)), lo);
-        lo = fmaf(ds.z, i2f(scB * ((h0 + h1) >> 4)), lo);
-        mn = fmaf(ds.y, i2f(mA), mn);
-        mn = fmaf(ds.w, i2f(mB), mn);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          if (t >= tn) break;
+          const int8_t* xb = xq + t * p.xq_tok + (b << 8) + 64 * q;
+          const int4 x0 = *reinterpret_cast<const int4*>(xb);
+          const int4 x1 = *reinterpret_cast<const int4*>(xb + 16);
+          const int4 x2 = *reinterpret_cast<const int4*>(xb + 32);
+          const int4 x3 = *reinterpret_cast<const int4*>(xb + 48);
+          const float4 ds = reinterpret_cast<const float4*>(xsb + t * p.xs_tok)[(b << 2) + q];  // {d8, s} of 2q, 2q+1
+          int dA, dB;
+          if (WT == KQ_Q5_K) {
+            dA = __dp4a(static_cast<int>(cl[0]), x0.x, 0);
+            dA = __dp4a(static_cast<int>(cl[1]), x0.y, dA);
+            dA = __dp4a(static_cast<int>(cl[2]), x0.z, dA);
+            dA = __dp4a(static_cast<int>(cl[3]), x0.w, dA);
+            dA = __dp4a(static_cast<int>(cl[4]), x1.x, dA);
+            dA = __dp4a(static_cast<int>(cl[5]), x1.y, dA);
+            dA = __dp4a(static_cast<int>(cl[6]), x1.z, dA);
+            dA = __dp4a(static_cast<int>(cl[7]), x1.w, dA);
+            dB = __dp4a(static_cast<int>(ch[0]), x2.x, 0);
+            dB = __dp4a(static_cast<int>(ch[1]), x2.y, dB);
+            dB = __dp4a(static_cast<int>(ch[2]), x2.z, dB);
+            dB = __dp4a(static_cast<int>(ch[3]), x2.w, dB);
+            dB = __dp4a(static_cast<int>(ch[4]), x3.x, dB);
+            dB = __dp4a(static_cast<int>(ch[5]), x3.y, dB);
+            dB = __dp4a(static_cast<int>(ch[6]), x3.z, dB);
+            dB = __dp4a(static_cast<int>(ch[7]), x3.w, dB);
+          } else {
+            int a0 = __dp4a(static_cast<int>(cl[0]), x0.x, 0);
+            int a1 = __dp4a(static_cast<int>(cl[4]), x1.x, 0);
+            int h0 = dp4a_us(ch[0], x2.x, 0);
+            int h1 = dp4a_us(ch[4], x3.x, 0);
+            a0 = __dp4a(static_cast<int>(cl[1]), x0.y, a0);
+            a1 = __dp4a(static_cast<int>(cl[5]), x1.y, a1);
+            h0 = dp4a_us(ch[1], x2.y, h0);
+            h1 = dp4a_us(ch[5], x3.y, h1);
+            a0 = __dp4a(static_cast<int>(cl[2]), x0.z, a0);
+            a1 = __dp4a(static_cast<int>(cl[6]), x1.z, a1);
+            h0 = dp4a_us(ch[2], x2.z, h0);
+            h1 = dp4a_us(ch[6], x3.z, h1);
+            a0 = __dp4a(static_cast<int>(cl[3]), x0.w, a0);
+            a1 = __dp4a(static_cast<int>(cl[7]), x1.w, a1);
+            h0 = dp4a_us(ch[3], x2.w, h0);
+            h1 = dp4a_us(ch[7], x3.w, h1);
+            dA = a0 + a1;
+            dB = (h0 + h1) >> 4;
+          }
+          lo[t] = fmaf(ds.x, i2f(scA * dA), lo[t]);
+          lo[t] = fmaf(ds.z, i2f(scB * dB), lo[t]);
+          mn[t] = fmaf(ds.y, i2f(mA), mn[t]);
+          mn[t] = fmaf(ds.w, i2f(mB), mn[t]);
+        }
       }
-      const float v = fmaf(-dmin, mn, d * lo);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) acc[k] += (g == k) ? v : 0.f;
+      for (int t = 0; t < NT; ++t) {
+        const float v = fmaf(-dmin, mn[t], d * lo[t]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc[t][k] += (g == k) ? v : 0.f;
+      }
     }
+    // part: [token][warp][row group][lane]
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
-      if (k < p.n_groups) part[(warp * p.n_groups + k) * 32 + lane] = acc[k];
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (t < tn && k < p.n_groups) part[((t * NW + warp) * p.n_groups + k) * 32 + lane] = acc[t][k];
     asm volatile("bar.sync 1, %0;" ::"r"(LR_CT) : "memory");
-    // y[token][row] = Sum over the token's warps, in warp order
+    // y[token][row] = Sum over the warps, in warp order
     for (int u = threadIdx.x; u < tn * rows; u += LR_CT) {
       const int t = u / rows, r = u - t * rows;
-      const float* pr = part + (r >> 5) * 32 + (r & 31);
-      float a = pr[t * p.n_groups * 32];
-      for (int w = t + tn; w < NW; w += tn) a += pr[w * p.n_groups * 32];
+      const float* pr = part + t * NW * p.n_groups * 32 + (r >> 5) * 32 + (r & 31);
+      float a = pr[0];
+      for (int w = 1; w < NW; ++w) a += pr[w * p.n_groups * 32];
       p.y[static_cast<int64_t>(t0 + t) * p.M + r0 + r] = a;
     }
   }
@@ -886,7 +942,7 @@ static inline int round_up(int v, int a) { return (v + a - 1) / a * a; }
 // allows fewer chunk slots than chunks (at least two). False when the rows do
 // not fit (then the item kernel above runs).
 static bool plan_lanerow(int64_t M, int64_t K, int num_sms, int nw, int nt, int budget, bool ring,
-                         MatvecLaneRowParams* p, int* grid, size_t* smem, int bb = Q4K_BYTES) {
+                         MatvecLaneRowParams* p, int* grid, size_t* smem, int bb = Q4K_BYTES, bool trim_tail = false) {
   if (K > (int64_t(1) << 20)) return false;
   p->M = static_cast<int>(M);
   p->K = static_cast<int>(K);
@@ -897,7 +953,7 @@ static bool plan_lanerow(int64_t M, int64_t K, int num_sms, int nw, int nt, int 
   p->R = static_cast<int>(R);
   *grid = static_cast<int>((M + R - 1) / R);
   p->n_groups = (p->R + 31) / 32;
-  const int part_bytes = nw * p->n_groups * 32 * 4;
+  const int part_bytes = nt * nw * p->n_groups * 32 * 4;  // per token: [warp][row group][lane]
   p->xq_tok = round_up(p->K, 128);                      // activation codes of a token
   p->xs_tok = round_up((p->K / 32) * 8, 128);           // {d8, d8 * Sum q} per 32-block
   const int fixed = nt * (p->xq_tok + p->xs_tok) + part_bytes;  // + per-warp partials
@@ -907,19 +963,26 @@ static bool plan_lanerow(int64_t M, int64_t K, int num_sms, int nw, int nt, int 
   for (int cb = (bb == Q5K_BYTES ? 5 : 7); cb >= 3; cb -= 2) {
     const int n_chunks = (p->nb + cb - 1) / cb;
     const int chunk_bytes = round_up(p->R * cb * bb, 128);
+    // trim_tail (staged form): the last chunk's slot holds only its own
+    // super-blocks, loaded through a second tensor map with a narrower box
+    const int tail_cb = trim_tail ? p->nb - (n_chunks - 1) * cb : cb;
+    const int trim = trim_tail ? chunk_bytes - round_up(p->R * tail_cb * bb, 128) : 0;
     int S = n_chunks;
-    auto total = [&](int slots) { return static_cast<size_t>(slots) * chunk_bytes + fixed + slots * 16 + 16; };
+    auto total = [&](int slots) {
+      return static_cast<size_t>(slots) * chunk_bytes - trim + fixed + slots * 16 + 16;
+    };
     while (ring && S > 2 && total(S) > static_cast<size_t>(budget)) --S;
     if (total(S) > static_cast<size_t>(budget)) continue;
     // i / d == umulhi(i, ceil(2^32 / d)) holds while i * d < 2^32
     if (static_cast<int64_t>(n_chunks) * p->n_groups * cb * p->n_groups * cb >= (int64_t(1) << 32)) return false;
     p->cb = cb;
+    p->tail_cb = tail_cb;
     p->n_chunks = n_chunks;
     p->chunk_bytes = chunk_bytes;
     p->S = S;
     p->inv_per_chunk = static_cast<uint32_t>(((uint64_t(1) << 32) + p->n_groups * cb - 1) / (p->n_groups * cb));
     p->inv_cb = static_cast<uint32_t>(((uint64_t(1) << 32) + cb - 1) / cb);
-    size_t off = static_cast<size_t>(S) * chunk_bytes;
+    size_t off = static_cast<size_t>(S) * chunk_bytes - trim;
     p->xq_off = static_cast<int>(off);
     off += static_cast<size_t>(nt) * p->xq_tok;
     p->xs_off = static_cast<int>(off);
@@ -1094,13 +1157,13 @@ __global__ void __launch_bounds__(256) quantize_split_kernel(const float* __rest
 // with LR_NT (else two) tokens per pass. *handled = false (nothing queued) when
 // the rows do not fit staged next to the activations of two tokens.
 template <int NT, int WT>
-static cudaError_t launch_tokens_kernel(const CUtensorMap& tmW, const MatvecLaneRowParams& lp, int grid, size_t smem,
-                                        cudaStream_t s) {
+static cudaError_t launch_tokens_kernel(const CUtensorMap& tmW, const CUtensorMap& tmT, const MatvecLaneRowParams& lp,
+                                        int grid, size_t smem, cudaStream_t s) {
   const int slot = WT == KQ_Q5_K ? (NT == LR_NT ? 35 : 36) : (NT == LR_NT ? 11 : 14);
   cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(matvec_q4k_lanerow_tokens_kernel<NT, WT>), slot);
   if (e != cudaSuccess) return e;
-  return launch_pdl(matvec_q4k_lanerow_tokens_kernel<NT, WT>, dim3(grid), dim3((LR_NW_FULL + 1) * 32), smem, s, tmW,
-                    lp);
+  return launch_pdl(matvec_q4k_lanerow_tokens_kernel<NT, WT>, dim3(grid), dim3((LR_NW_TOK + 1) * 32), smem, s, tmW,
+                    tmT, lp);
 }
 
 cudaError_t launch_matvec_tokens(int wtype, const void* W, const float* X, float* Y, int64_t M, int64_t K, int64_t N,
@@ -1113,14 +1176,18 @@ cudaError_t launch_matvec_tokens(int wtype, const void* W, const float* X, float
   size_t smem = 0;
   int grid = 0;
   int nt = LR_NT;
-  if (!plan_lanerow(M, K, num_sms, LR_NW_FULL, nt, MV_SMEM_LIMIT, false, &lp, &grid, &smem, bb)) {
+  if (!plan_lanerow(M, K, num_sms, LR_NW_TOK, nt, MV_SMEM_LIMIT, false, &lp, &grid, &smem, bb, true)) {
     nt = 2;
-    if (!plan_lanerow(M, K, num_sms, LR_NW_FULL, nt, MV_SMEM_LIMIT, false, &lp, &grid, &smem, bb)) return cudaSuccess;
+    if (!plan_lanerow(M, K, num_sms, LR_NW_TOK, nt, MV_SMEM_LIMIT, false, &lp, &grid, &smem, bb, true))
+      return cudaSuccess;
   }
-  CUtensorMap tmW;
+  CUtensorMap tmW, tmT;  // chunks of cb super-blocks; the last chunk's tail_cb
   const uint64_t rs = static_cast<uint64_t>(lp.nb) * bb;
   if (!encode_tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT32, W, rs / 4, static_cast<uint64_t>(M), rs,
-                      static_cast<uint32_t>(lp.cb * bb / 4), static_cast<uint32_t>(lp.R), CU_TENSOR_MAP_SWIZZLE_NONE))
+                      static_cast<uint32_t>(lp.cb * bb / 4), static_cast<uint32_t>(lp.R), CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !encode_tmap_2d(&tmT, CU_TENSOR_MAP_DATA_TYPE_UINT32, W, rs / 4, static_cast<uint64_t>(M), rs,
+                      static_cast<uint32_t>(lp.tail_cb * bb / 4), static_cast<uint32_t>(lp.R),
+                      CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaSuccess;
   const size_t xq_bytes = static_cast<size_t>(N) * lp.xq_tok, xs_bytes = static_cast<size_t>(N) * lp.xs_tok;
   if (xq_bytes + xs_bytes > scratch_bytes) return cudaSuccess;
@@ -1142,9 +1209,9 @@ cudaError_t launch_matvec_tokens(int wtype, const void* W, const float* X, float
     if (e != cudaSuccess) return e;
   }
   if (wtype == KQ_Q5_K)
-    return nt == LR_NT ? launch_tokens_kernel<LR_NT, KQ_Q5_K>(tmW, lp, grid, smem, s)
-                       : launch_tokens_kernel<2, KQ_Q5_K>(tmW, lp, grid, smem, s);
-  return nt == LR_NT ? launch_tokens_kernel<LR_NT, KQ_Q4_K>(tmW, lp, grid, smem, s)
-                     : launch_tokens_kernel<2, KQ_Q4_K>(tmW, lp, grid, smem, s);
+    return nt == LR_NT ? launch_tokens_kernel<LR_NT, KQ_Q5_K>(tmW, tmT, lp, grid, smem, s)
+                       : launch_tokens_kernel<2, KQ_Q5_K>(tmW, tmT, lp, grid, smem, s);
+  return nt == LR_NT ? launch_tokens_kernel<LR_NT, KQ_Q4_K>(tmW, tmT, lp, grid, smem, s)
+                     : launch_tokens_kernel<2, KQ_Q4_K>(tmW, tmT, lp, grid, smem, s);
 }
 }  // namespace kq

@@ -1,6 +1,6 @@
 """Small-N decode (2 to 16 tokens at once) against the oracle, element by
 element, within |y - y_ref| <= 1e-3 * Sum_k |w_k x_k| + 1e-5. Through the
-public GEMM entry point: Q4_K and Q5_K with 2 <= N <= 5 run on the decode matvec path
+public GEMM entry point: Q4_K and Q5_K with 2 <= N <= 7 run on the decode matvec path
 ("06 · 8e/8e② — decode MMVQ", §2 Principle: dp4a integer dots, the min term
 from the Q8_1 block sum), the staged weights multiplied with every token;
 larger N (the N = 8 and 16 cases) on the tensor-core GEMM."""
@@ -26,7 +26,9 @@ def _run(W, X, M, K, wtype="q4_k"):
     (300, 1024, 3),      # rows per CTA not a multiple of 32
     (1000, 4096, 4),
     (777, 2816, 5),      # two passes, the last with one token
-    (2048, 1024, 8),
+    (640, 2048, 6),
+    (4096, 11008, 7),    # the largest N on the decode path; two passes of four and three
+    (2048, 1024, 8),     # tensor-core GEMM
     (129, 256, 16),      # one super-block per row (tensor-core GEMM)
 ])
 def test_small_n_full_parity(M, K, N):
@@ -68,7 +70,7 @@ def test_small_n_deterministic_and_per_token():
     assert_within_bound(a[[3, 0, 5]], Yr, B, "the same tokens among six")
 
 
-@pytest.mark.parametrize("M,K,N", [(512, 2048, 2), (300, 1024, 3), (777, 2816, 5), (4096, 11008, 4)])
+@pytest.mark.parametrize("M,K,N", [(512, 2048, 2), (300, 1024, 3), (777, 2816, 5), (4096, 11008, 4), (1000, 2048, 7)])
 def test_small_n_q5k(M, K, N):
     # Q5_K takes the same matvec path (its fifth bits merged into each dp4a word).
     rng = np.random.default_rng(M + 11 * N)
