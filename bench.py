@@ -231,12 +231,20 @@ def run_ours(args, dist):
     pk, pk_kind = peaks()
 
     # ---- decode inputs: 8 independent weight copies per shape ----------------
+    # Both shapes' x (and y) are views of one buffer, so the end-to-end leg
+    # moves each step's inputs and results with one copy each way.
+    wls = [syn.make_workload(name, copies=DECODE_COPIES) for name in ("decode_q4k_4096x11008", "decode_q4k_11008x4096")]
+    x_all = torch.empty(sum(wl["K"] for wl in wls), dtype=torch.float32, device=dev)
+    y_all = torch.empty(sum(wl["M"] for wl in wls), dtype=torch.float32, device=dev)
     sets = []
-    for name in ("decode_q4k_4096x11008", "decode_q4k_11008x4096"):
-        wl = syn.make_workload(name, copies=DECODE_COPIES)
+    xo = yo = 0
+    for wl in wls:
         Ws = [torch.from_numpy(w).to(dev) for w in wl["W"]]
-        x = torch.from_numpy(wl["X"][0]).to(dev)
-        y = torch.empty(wl["M"], dtype=torch.float32, device=dev)
+        x = x_all[xo:xo + wl["K"]]
+        x.copy_(torch.from_numpy(wl["X"][0]))
+        y = y_all[yo:yo + wl["M"]]
+        xo += wl["K"]
+        yo += wl["M"]
         sets.append((wl["M"], wl["K"], Ws, x, y, wl["X"][0]))
     w_bytes_step = sum(W.numel() for s in sets for W in s[2])
     alg_bytes_launch = [M * Q4K_ROW(K) + 4 * K + 4 * M for (M, K) in DECODE_SHAPES]
@@ -300,15 +308,13 @@ def run_ours(args, dist):
         raise RuntimeError(f"device error {code} during the decode bench")
 
     # ---- end to end: pinned host x in, y out, through the public API ---------
-    hx = [torch.from_numpy(s[5]).pin_memory() for s in sets]
-    hy = [torch.empty(s[0], dtype=torch.float32).pin_memory() for s in sets]
+    hx = torch.from_numpy(np.concatenate([s[5] for s in sets])).pin_memory()
+    hy = torch.empty(y_all.numel(), dtype=torch.float32).pin_memory()
 
     def step_e2e():
-        for i, s in enumerate(sets):
-            s[3].copy_(hx[i], non_blocking=True)
+        x_all.copy_(hx, non_blocking=True)
         step()
-        for i, s in enumerate(sets):
-            hy[i].copy_(s[4], non_blocking=True)
+        hy.copy_(y_all, non_blocking=True)
 
     for _ in range(max(3, args.warmup)):
         step_e2e()
@@ -370,8 +376,8 @@ def run_ours(args, dist):
         "e2e": {
             "value": round(dist.world * w_bytes_step / (ms_e2e / 1e3) / 1e9, 2),
             "unit": "GB/s",
-            "h2d_bytes_per_step": sum(4 * K for (_, K) in DECODE_SHAPES),
-            "d2h_bytes_per_step": sum(4 * M for (M, _) in DECODE_SHAPES),
+            "h2d_bytes_per_step": hx.numel() * hx.element_size(),
+            "d2h_bytes_per_step": hy.numel() * hy.element_size(),
             "ms_per_step": round(ms_e2e, 5),
         },
         "gpu_launches": launches_step * args.steps,
