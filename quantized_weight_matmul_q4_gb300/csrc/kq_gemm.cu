@@ -1106,7 +1106,7 @@ cudaError_t launch_gemm(int wtype, const void* W, const float* X, float* Y, int6
 }
 
 // MoE workspace: counts[E] | offsets[E+1] | tile_start[E+1] | tile queue counter | entries[n] (slot of each bucket row) |
-// slot_pos[n] (bucket row of each slot) | x_hat of every token [T][K] fp16 | x_hat[n][K] fp16 (bucket order)
+// slot_pos[n] (bucket row of each slot) | x_hat[n][K] fp16 (bucket order)
 MoePlan plan_moe(int wtype, int64_t M, int64_t K, int64_t T, int n_experts, int top_k) {
   (void)wtype;
   MoePlan p{};
@@ -1125,8 +1125,6 @@ MoePlan plan_moe(int wtype, int64_t M, int64_t K, int64_t T, int n_experts, int 
   o += round_up64(4 * n, 256);
   p.off_src = o;
   o += round_up64(4 * n, 1024);
-  p.off_xtok = o;
-  o += round_up64(T * K * 2, 1024);
   p.off_xhat = o;
   o += round_up64(n * K * 2, 1024);
   p.total_bytes = o;
@@ -1150,22 +1148,19 @@ cudaError_t launch_moe(int wtype, const void* W, int n_experts, const int32_t* i
   int* tile_queue = reinterpret_cast<int*>(wsb + plan.off_queue);
   int* entries = reinterpret_cast<int*>(wsb + plan.off_entries);
   int* slot_pos = reinterpret_cast<int*>(wsb + plan.off_src);
-  __half* xtok = reinterpret_cast<__half*>(wsb + plan.off_xtok);
   __half* xh = reinterpret_cast<__half*>(wsb + plan.off_xhat);
   const int64_t n = T * top_k;
 
-  // x_hat of every token once; the routing kernel (which waits for it) and the
-  // row gather follow.
-  cudaError_t e = launch_quantize_xhat(X, xtok, K, T, num_sms, s);
-  if (e != cudaSuccess) return e;
+  // Routing first (bucket tables, the bucket row of every slot); then each
+  // token's x_hat row is made once and written to all of its bucket rows.
   const size_t rsmem = static_cast<size_t>(n_experts + 32) * sizeof(int);
-  e = allow_max_smem(reinterpret_cast<const void*>(moe_route_kernel), 8);
+  cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(moe_route_kernel), 8);
   if (e != cudaSuccess) return e;
   e = launch_pdl(moe_route_kernel, dim3(1), dim3(1024), rsmem, s, ids, static_cast<int>(n), top_k, n_experts,
                  plan.m_tiles, MOE_BN, counts, offsets, tile_start, tile_queue, slot_pos, Y, static_cast<int>(M),
                  err);
   if (e != cudaSuccess) return e;
-  e = launch_gather_rows(xtok, xh, K, n, top_k, slot_pos, entries, s);
+  e = launch_quantize_scatter(X, xh, K, T, top_k, slot_pos, entries, s);
   if (e != cudaSuccess) return e;
 
   CUtensorMap tmW, tmX;

@@ -12,10 +12,11 @@ namespace kq {
 
 cudaError_t launch_quantize_q8_1(const float* X, void* Xq, int64_t K, int64_t N, cudaStream_t s);
 cudaError_t launch_quantize_xhat(const float* X, __half* Xh, int64_t K, int64_t rows, int num_sms, cudaStream_t s);
-// MoE gather: bucket row slot_pos[i] of Xh <- row i / top_k of Xtok (x_hat
-// per token); entries[slot_pos[i]] = i. Negative positions are skipped.
-cudaError_t launch_gather_rows(const __half* Xtok, __half* Xh, int64_t K, int64_t n_slots, int top_k,
-                               const int* slot_pos, int* entries, cudaStream_t s);
+// MoE activations: the x_hat row of token p (Q8_1 of X row p, as
+// launch_quantize_xhat makes it) into bucket row slot_pos[s] of Xh for each
+// slot s = p * top_k + j; entries[slot_pos[s]] = s. Negative positions are skipped.
+cudaError_t launch_quantize_scatter(const float* X, __half* Xh, int64_t K, int64_t T, int top_k, const int* slot_pos,
+                                   int* entries, cudaStream_t s);
 
 // Producer of the decode matvec's activations (fused into its quantiser):
 // x itself; silu(x) * aux (SwiGLU, x the gate, aux the up projection);
@@ -61,7 +62,7 @@ cudaError_t launch_gemm(int wtype, const void* W, const float* X, float* Y, int6
 
 struct MoePlan {
   int m_tiles;
-  size_t off_counts, off_offsets, off_tiles, off_queue, off_entries, off_src, off_xtok, off_xhat, total_bytes;
+  size_t off_counts, off_offsets, off_tiles, off_queue, off_entries, off_src, off_xhat, total_bytes;
 };
 MoePlan plan_moe(int wtype, int64_t M, int64_t K, int64_t T, int n_experts, int top_k);
 cudaError_t launch_moe(int wtype, const void* W, int n_experts, const int32_t* ids, int top_k, const float* X,

@@ -62,37 +62,52 @@ __global__ void __launch_bounds__(256) quantize_xhat_kernel(const float* __restr
   }
 }
 
-// MoE gather: bucket row slot_pos[i] of Xh is the x_hat row of slot i's token
-// (row i / top_k of Xtok, quantised once per token); slots with a negative
-// position are skipped. One warp per slot, each lane moving 16-byte pieces of
-// the row with GR_UNROLL loads in flight; lane 0 also records
-// entries[slot_pos[i]] = i. K * 2 bytes is a multiple of 512, so every lane
-// moves whole rounds of 32 x 16 bytes.
-constexpr int GR_WARPS = 8;
-constexpr int GR_UNROLL = 8;
-__global__ void __launch_bounds__(GR_WARPS * 32) gather_rows_kernel(const __half* __restrict__ Xtok,
-                                                                    __half* __restrict__ Xh, int K, int64_t n_slots,
-                                                                    int top_k, const int* __restrict__ slot_pos,
-                                                                    int* __restrict__ entries) {
+// MoE activations: token p's x_hat row (the Q8_1 value of X row p, exactly as
+// quantize_xhat_kernel makes it) is written to the bucket row slot_pos[s] of
+// each of its slots s = p * top_k + j; slots with a negative position (an
+// invalid expert id) are skipped, and entries[slot_pos[s]] = s records the slot
+// of each bucket row. A warp takes one token's run of QS_ROUNDS rounds of 32
+// quads (K / 4 is a multiple of 64, so a run is whole rounds and the eight lanes
+// of a Q8_1 block stay together), quantises each round once and stores it to
+// every bucket row of the token.
+constexpr int QS_WARPS = 8;
+constexpr int QS_ROUNDS = 4;
+__global__ void __launch_bounds__(QS_WARPS * 32) quantize_scatter_kernel(const float* __restrict__ X,
+                                                                        __half* __restrict__ Xh, int K, int64_t T,
+                                                                        int top_k, const int* __restrict__ slot_pos,
+                                                                        int* __restrict__ entries) {
   pdl_enter();
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * GR_WARPS + (threadIdx.x >> 5);
+  const int rounds = K >> 7;  // rounds of 32 quads per row
+  const int runs = (rounds + QS_ROUNDS - 1) / QS_ROUNDS;
+  const int64_t w = static_cast<int64_t>(blockIdx.x) * QS_WARPS + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (i >= n_slots) return;
-  const int pos = __ldg(slot_pos + i);
-  if (pos < 0) return;
-  const uint4* src = reinterpret_cast<const uint4*>(Xtok + (i / top_k) * static_cast<int64_t>(K));
-  uint4* dst = reinterpret_cast<uint4*>(Xh + static_cast<int64_t>(pos) * K);
-  const int n16 = K / 8;  // 16-byte pieces per row
-  for (int c0 = lane; c0 < n16; c0 += 32 * GR_UNROLL) {
-    uint4 v[GR_UNROLL];
+  if (w >= T * runs) return;
+  const int64_t p = w / runs;
+  const int run = static_cast<int>(w - p * runs);
+  const int r1 = min(rounds, (run + 1) * QS_ROUNDS);
+  const float4* xrow = reinterpret_cast<const float4*>(X + p * K);
+  uint2* hrow0 = reinterpret_cast<uint2*>(Xh);
+  const int64_t quads = K >> 2;
+  const int* sp = slot_pos + p * top_k;
+  float4 v[QS_ROUNDS];
 #pragma unroll
-    for (int u = 0; u < GR_UNROLL; ++u)
-      if (c0 + 32 * u < n16) v[u] = __ldg(src + c0 + 32 * u);
+  for (int u = 0; u < QS_ROUNDS; ++u)
+    if (run * QS_ROUNDS + u < r1) v[u] = __ldg(xrow + (run * QS_ROUNDS + u) * 32 + lane);
 #pragma unroll
-    for (int u = 0; u < GR_UNROLL; ++u)
-      if (c0 + 32 * u < n16) dst[c0 + 32 * u] = v[u];
+  for (int u = 0; u < QS_ROUNDS; ++u) {
+    const int r = run * QS_ROUNDS + u;
+    if (r >= r1) break;  // warp-uniform
+    const uint2 h = xhat4(quantize_quad(v[u]));
+    for (int j0 = 0; j0 < top_k; j0 += 32) {
+      const int my = (j0 + lane < top_k) ? __ldg(sp + j0 + lane) : -1;
+      const int nj = min(32, top_k - j0);
+      for (int jj = 0; jj < nj; ++jj) {
+        const int pos = __shfl_sync(0xffffffffu, my, jj);
+        if (pos >= 0) hrow0[pos * quads + r * 32 + lane] = h;
+      }
+      if (run == 0 && u == 0 && my >= 0) entries[my] = static_cast<int>(p * top_k + j0 + lane);
+    }
   }
-  if (lane == 0) entries[pos] = static_cast<int>(i);
 }
 
 static unsigned xhat_grid(int64_t quads, int num_sms) {
@@ -108,11 +123,13 @@ cudaError_t launch_quantize_xhat(const float* X, __half* Xh, int64_t K, int64_t 
                     static_cast<int>(K), rows);
 }
 
-cudaError_t launch_gather_rows(const __half* Xtok, __half* Xh, int64_t K, int64_t n_slots, int top_k,
-                               const int* slot_pos, int* entries, cudaStream_t s) {
-  if (n_slots == 0) return cudaSuccess;
-  return launch_pdl(gather_rows_kernel, dim3(static_cast<unsigned>((n_slots + GR_WARPS - 1) / GR_WARPS)),
-                    dim3(GR_WARPS * 32), 0, s, Xtok, Xh, static_cast<int>(K), n_slots, top_k, slot_pos, entries);
+cudaError_t launch_quantize_scatter(const float* X, __half* Xh, int64_t K, int64_t T, int top_k, const int* slot_pos,
+                                   int* entries, cudaStream_t s) {
+  const int64_t runs = ((K >> 7) + QS_ROUNDS - 1) / QS_ROUNDS;
+  const int64_t warps = T * runs;
+  if (warps == 0) return cudaSuccess;
+  return launch_pdl(quantize_scatter_kernel, dim3(static_cast<unsigned>((warps + QS_WARPS - 1) / QS_WARPS)),
+                    dim3(QS_WARPS * 32), 0, s, X, Xh, static_cast<int>(K), T, top_k, slot_pos, entries);
 }
 
 cudaError_t launch_quantize_q8_1(const float* X, void* Xq, int64_t K, int64_t N, cudaStream_t s) {
