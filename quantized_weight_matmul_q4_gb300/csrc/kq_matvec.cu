@@ -458,7 +458,8 @@ __global__ void __launch_bounds__(MV_THREADS, 1) matvec_kernel(const MatvecParam
 // whole.
 constexpr int LR_NW_FULL = 24;
 constexpr int LR_NW_RING = 14;
-constexpr int LR_NW_TOK = 16;               // consumer warps of the several-token kernel
+constexpr int LR_NW_TOK = 16;               // several-token kernel: its per-token sums need the
+                                             // registers of a 17-warp CTA (96 a thread)
 constexpr int LR_RING_SMEM = 113 * 1024;     // two CTAs per SM (228 KB, 1 KB reserved per CTA)
 constexpr int LR_MAX_ROWS = 128;             // rows per CTA: at most four row groups
 constexpr int LR_XT = 2;                     // 8-value activation tasks loaded per thread per round
