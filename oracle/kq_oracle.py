@@ -238,14 +238,19 @@ def quantize_q8_1(X: np.ndarray):
     fp32, step by step:
       amax = max |x| over the block
       d    = amax / 127                 (fp32 division)
-      di   = 1 / d if d != 0 else 0     (fp32 division)
+      di   = 1 / d if d != 0 else 0     (fp32 division; also 0 where 1 / d
+                                         overflows fp32, see below)
       q    = clamp(rint(x * di), -128, 127)   (fp32 product, ties to even)
       d_h  = fp16(d)                    (stored scale, round to nearest even)
     plus the block sum of the Q8_1 format, s = d * Sum(q) ([MMQv2]: Q8_1
     carries the sum used by the min term). Reading taken for the open point of
     which d multiplies Sum(q): the stored d_h, so that s is the sum of the
     block's dequantised activations; d_h * Sum(q) is exact in fp32 (11-bit by
-    at most 13-bit integers) and is rounded once to fp16.
+    at most 13-bit integers) and is rounded once to fp16. Reading taken where
+    the pages' formula has no finite value: when amax is below about 3.7e-37,
+    1 / d overflows fp32 and x * di would be infinite or NaN; d_h = fp16(d) is
+    0 there, so the block's dequantised values are 0 whatever its codes, and
+    the codes are taken as 0 (di = 0), as for amax = 0.
 
     ``X``: fp32 [N, K] token-major, K % 32 == 0.
     Returns (q int8 [N, K/32, 32], d_h uint16 [N, K/32], s_h uint16 [N, K/32]).
@@ -258,7 +263,9 @@ def quantize_q8_1(X: np.ndarray):
     amax = np.max(np.abs(xb), axis=-1)
     d = (amax / np.float32(127.0)).astype(np.float32)
     di = np.zeros_like(d)
-    np.divide(np.float32(1.0), d, out=di, where=(d != 0))
+    with np.errstate(over="ignore", divide="ignore"):
+        np.divide(np.float32(1.0), d, out=di, where=(d != 0))
+    di[~np.isfinite(di)] = 0
     prod = (xb * di[..., None]).astype(np.float32)
     q = np.clip(np.rint(prod), -128, 127).astype(np.int8)
     d_h = f32_to_fp16_bits(d)

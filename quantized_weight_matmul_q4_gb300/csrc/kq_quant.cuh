@@ -3,7 +3,9 @@
 // The quantiser of "06 · 8e/8e② — decode MMVQ" (§2 Principle and §3.2
 // ``quantize_pad40_block``), with the Q8_1 block sum of "ZINC MMQ v2" (What
 // they do right: Q8_1 activations):
-//   amax = max|x|, d = amax / 127, di = d != 0 ? 1 / d : 0,
+//   amax = max|x|, d = amax / 127, di = 1 / d (0 when d = 0, or when 1 / d
+//   is not a finite fp32 value: max|x| below about 3.7e-37, where d_h = fp16(d)
+//   is 0 and the block dequantises to 0 whatever its codes),
 //   q = clamp(rint(x * di), -128, 127), stored scale d_h = fp16(d),
 //   block sum s = fp16(d_h * Sum q).
 // Every step is a single IEEE fp32 operation (correctly rounded division,
@@ -14,6 +16,13 @@
 #include "kq_common.cuh"
 
 namespace kq {
+
+// The reciprocal scale di of a block: 1 / d, or 0 when d is 0 or 1 / d
+// overflows (the comparison is false for inf), so that every code is finite.
+__device__ __forceinline__ float q8_inv_scale(float d) {
+  const float di = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
+  return (di <= 3.40282347e38f) ? di : 0.0f;
+}
 
 struct Q8Quad {
   int q[4];        // the four codes of this thread
@@ -32,7 +41,7 @@ __device__ __forceinline__ Q8Quad quantize_quad(float4 v) {
   a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
   a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
   const float d = __fdiv_rn(a, 127.0f);
-  const float di = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
+  const float di = q8_inv_scale(d);
   Q8Quad r;
   const float e[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -56,42 +65,8 @@ __device__ __forceinline__ uint32_t pack_q4(const int (&q)[4]) {
          ((static_cast<uint32_t>(q[2]) & 0xFFu) << 16) | ((static_cast<uint32_t>(q[3]) & 0xFFu) << 24);
 }
 
-// Quantises 16 consecutive values v[0..15] held by one lane; the two lanes of
-// an aligned lane pair hold one 32-element block (lane 2i: elements 0..15).
-// Same arithmetic as quantize_quad (IEEE division, product, round half to even,
-// saturation to [-128, 127]). Both lanes of the pair must call it.
-struct Q8Half {
-  uint32_t q[4];   // 16 packed int8 codes
-  float dh;        // fp16-rounded block scale d_h, as fp32
-  int sumq;        // Sum q over the whole 32-element block
-};
-
 // round half to even, then clamp to [-128, 127]
 __device__ __forceinline__ int cvt_rni_sat_s8(float x) { return max(-128, min(127, __float2int_rn(x))); }
-
-__device__ __forceinline__ Q8Half quantize_half(const float (&v)[16]) {
-  float a = 0.f;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) a = fmaxf(a, fabsf(v[i]));
-  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-  const float d = __fdiv_rn(a, 127.0f);
-  const float di = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
-  Q8Half r;
-  int s = 0;
-#pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    const int q0 = cvt_rni_sat_s8(__fmul_rn(v[4 * w + 0], di));
-    const int q1 = cvt_rni_sat_s8(__fmul_rn(v[4 * w + 1], di));
-    const int q2 = cvt_rni_sat_s8(__fmul_rn(v[4 * w + 2], di));
-    const int q3 = cvt_rni_sat_s8(__fmul_rn(v[4 * w + 3], di));
-    s += q0 + q1 + q2 + q3;
-    r.q[w] = (static_cast<uint32_t>(q0) & 0xFFu) | ((static_cast<uint32_t>(q1) & 0xFFu) << 8) |
-             ((static_cast<uint32_t>(q2) & 0xFFu) << 16) | ((static_cast<uint32_t>(q3) & 0xFFu) << 24);
-  }
-  r.sumq = s + __shfl_xor_sync(0xffffffffu, s, 1);
-  r.dh = __half2float(__float2half_rn(d));
-  return r;
-}
 
 // Quantises 8 consecutive values v[0..7] held by one lane; the four lanes of an
 // aligned lane quad hold one 32-element block (lane 4i + j: elements 8j..8j+7).
@@ -109,7 +84,7 @@ __device__ __forceinline__ Q8Oct quantize_oct(const float (&v)[8]) {
   a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
   a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
   const float d = __fdiv_rn(a, 127.0f);
-  const float di = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
+  const float di = q8_inv_scale(d);
   Q8Oct r;
   int s = 0;
 #pragma unroll

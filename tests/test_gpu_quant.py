@@ -37,7 +37,7 @@ def test_workload_activations_bit_exact(name):
 def test_edge_blocks_bit_exact():
     rng = np.random.default_rng(3)
     K = 32 * 16
-    X = np.zeros((6, K), np.float32)
+    X = np.zeros((7, K), np.float32)
     X[0] = rng.standard_normal(K)
     X[1, :32] = 0.0                                        # all-zero block
     X[1, 32:64] = -0.0
@@ -48,6 +48,10 @@ def test_edge_blocks_bit_exact():
     X[4] = np.repeat(rng.standard_normal(K // 32), 32)     # constant blocks
     X[5, ::32] = 1.0                                       # a single non-zero per block
     X[5, 1::32] = -1.0 + 2 ** -20
+    # max|x| around the point where 1/d overflows fp32 (~3.7e-37): subnormal,
+    # just below (codes 0), just above (codes as usual)
+    for b, sc in enumerate([1e-38, 3.0e-37, 5.0e-37, 1e-36] * (K // 128)):
+        X[6, 32 * b:32 * b + 32] = np.linspace(-1, 1, 32) * np.float32(sc)
     got, want = _gpu_q8(X), _ref_q8(X)
     assert np.array_equal(got, want)
 

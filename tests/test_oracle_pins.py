@@ -210,6 +210,24 @@ def test_q8_1_zero_block():
     assert d_h[0, 1] != 0
 
 
+def test_q8_1_reciprocal_overflow_block_is_zero():
+    # amax below ~3.7e-37: 1/d overflows fp32 and d_h = fp16(d) = 0, so the
+    # block dequantises to 0 whatever the codes; the codes are taken as 0. Just
+    # above the threshold 1/d is finite and the block quantises as usual.
+    X = np.zeros((1, 128), np.float32)
+    X[0, :32] = np.linspace(-1, 1, 32) * np.float32(1e-38)      # subnormal amax
+    X[0, 32:64] = np.linspace(-1, 1, 32) * np.float32(3.0e-37)  # d ~ 2.4e-39: 1/d = inf
+    X[0, 64:96] = np.linspace(-1, 1, 32) * np.float32(5.0e-37)  # d ~ 3.9e-39: 1/d finite
+    X[0, 96:] = _rand_x(8, 1, 32)[0]
+    d = (np.abs(X.reshape(4, 32)).max(-1) / np.float32(127)).astype(np.float32)
+    with np.errstate(over="ignore"):
+        assert np.isinf(np.float32(1) / d[1]) and np.isfinite(np.float32(1) / d[2])
+    q, d_h, s_h = ora.quantize_q8_1(X)
+    assert np.all(q[0, :2] == 0) and np.all(d_h[0, :3] == 0) and np.all(s_h[0, :3] == 0)
+    assert q[0, 2].tolist() == ora.quantize_q8_1(X[:, 64:96] * np.float32(2.0 ** 100))[0][0, 0].tolist()
+    assert np.abs(q[0, 2]).max() == 127
+
+
 def test_q8_1_unit_scale_block_is_round_half_even():
     # amax = 127 gives d = 1 and di = 1, so q = rint(x): round half to even.
     x = [127, 0.5, 1.5, 2.5, -0.5, -1.5, -2.5, 3.49, -3.51, 126.5, -126.5, 0.49999997,
