@@ -58,8 +58,12 @@ def test_large_workloads_sampled_rows(name):
     wl = syn.make_workload(name)
     M, K = wl["M"], wl["K"]
     Y = _run(wl["wtype"], wl["W"][0], wl["X"], M, K)
+    # every 128-row tile (and so every 256-row pair tile) is checked: its first
+    # and last rows and one random row inside it, plus the matrix's last row
     rng = np.random.default_rng(11)
-    rows = np.sort(np.concatenate([rng.choice(M, 192, replace=False), [0, 127, 128, M - 1]]))
+    starts = np.arange(0, M, 128)
+    inner = starts + rng.integers(1, 127, size=starts.size)
+    rows = np.unique(np.concatenate([starts, np.minimum(starts + 127, M - 1), np.minimum(inner, M - 1), [M - 1]]))
     Yr, B = ora.matmul_rows(wl["wtype"], wl["W"][0], wl["X"], K, rows)
     assert_within_bound(Y[:, rows], Yr, B, name)
     assert np.all(np.isfinite(Y))

@@ -1,5 +1,7 @@
 """kq_gemm_noalloc (the GEMM with the library's fixed per-device scratch)
-against kq_gemm, through the C ABI, on two calls in a row.
+through the C ABI, on two calls in a row: each call's output against the
+oracle's Y_ref within the per-element bound, and against kq_gemm's output on
+the same inputs within the same bound.
 
 The file name sorts last so that it runs after every other test as well as
 alone in a fresh process; both orders must pass."""
@@ -27,14 +29,16 @@ def test_noalloc_matches_gemm_twice(wtype, M, K, N):
     W = syn.weights(wtype, rng, M, K)
     X = syn.activations(rng, K, N)
     Wd, Xd = to_dev(W, torch), to_dev(X, torch)
-    Yref = kq_gemm(wtype, Wd, Xd, M, K)
+    Ygemm = kq_gemm(wtype, Wd, Xd, M, K)
     torch.cuda.synchronize()
-    Yref = Yref.cpu().numpy().astype(np.float64)
-    _, B = ora.matmul(wtype, W, X, M, K)
+    Ygemm = Ygemm.cpu().numpy().astype(np.float64)
+    Yref, B = ora.matmul(wtype, W, X, M, K)
     for call in range(2):
         Y = kq_gemm_noalloc(wtype, Wd, Xd, M, K)
         torch.cuda.synchronize()
-        assert_within_bound(Y.cpu().numpy(), Yref, B, f"call {call} {wtype} {M}x{K}x{N}")
+        Y = Y.cpu().numpy()
+        assert_within_bound(Y, Yref, B, f"call {call} {wtype} {M}x{K}x{N} vs oracle")
+        assert_within_bound(Y, Ygemm, B, f"call {call} {wtype} {M}x{K}x{N} vs kq_gemm")
 
 
 def test_noalloc_prefill_workload_twice():
@@ -42,14 +46,15 @@ def test_noalloc_prefill_workload_twice():
     wl = syn.make_workload("prefill_q4k_4096x4096_n512")
     M, K = wl["M"], wl["K"]
     Wd, Xd = to_dev(wl["W"][0], torch), to_dev(wl["X"], torch)
-    Yref = kq_gemm(wl["wtype"], Wd, Xd, M, K)
+    Ygemm = kq_gemm(wl["wtype"], Wd, Xd, M, K)
     torch.cuda.synchronize()
     rows = np.array([0, 1, 127, 128, 2047, M - 1])
-    _, B = ora.matmul_rows(wl["wtype"], wl["W"][0], wl["X"], K, rows)
-    ref = Yref.cpu().numpy().astype(np.float64)
+    Yref, B = ora.matmul_rows(wl["wtype"], wl["W"][0], wl["X"], K, rows)
+    ref = Ygemm.cpu().numpy().astype(np.float64)
     for call in range(2):
         Y = kq_gemm_noalloc(wl["wtype"], Wd, Xd, M, K).cpu().numpy()
-        assert_within_bound(Y[:, rows], ref[:, rows], B, f"call {call}")
+        assert_within_bound(Y[:, rows], Yref, B, f"call {call} vs oracle")
+        assert_within_bound(Y[:, rows], ref[:, rows], B, f"call {call} vs kq_gemm")
         assert np.all(np.isfinite(Y))
 
 
