@@ -274,6 +274,24 @@ KQ_API size_t kq_workspace_bytes(int op, int wtype, int64_t M, int64_t K, int64_
  */
 KQ_API kq_status kq_get_device_error(int32_t* code, kq_stream_t stream);
 
+/*
+ * kq_test_hold_copies — a test hook for the library's failure detection; the
+ * source pages have no counterpart to it. While `hold` is non-zero, launches
+ * made afterwards by kq_matvec, kq_matvec_prefetch and the fused matvecs (Q4_K,
+ * Q5_K, Q6_K), by kq_gemm's tensor-core kernel and by kq_moe_grouped_gemm run
+ * with their weight producer issuing no copy (and, on the tensor-core paths,
+ * handing out no tile). Their consumers' pipeline waits then run out after
+ * their limit (2 s), the kernel records KQ_DEVERR_WAIT_TIMEOUT, leaves its
+ * loops, frees its tensor memory and returns: the path a wait that gives up
+ * takes, with no copy in flight. Outputs of such calls are undefined. The
+ * flag is per process and is read when a call queues its launch (a call
+ * captured in a CUDA graph keeps the value it saw). Not for production use:
+ * hold = 0 (the default) restores normal calls. Always returns KQ_OK.
+ * Calls that take other kernels (TQ4_1S, the small-N decode of kq_gemm) are
+ * not affected.
+ */
+KQ_API kq_status kq_test_hold_copies(int hold);
+
 /* Name of a status code (static string). */
 KQ_API const char* kq_status_str(int status);
 

@@ -18,7 +18,7 @@ __all__ = [
     "KQ_DEVERR_NONE", "KQ_DEVERR_WAIT_TIMEOUT", "KQ_DEVERR_EXPERT_ID",
     "KQ_GEMM_STATIC_WS_BYTES", "kq_quantize_q8_1", "kq_matvec", "kq_matvec_prefetch", "kq_matvec_swiglu", "kq_matvec_rmsnorm",
     "kq_gemm", "kq_gemm_noalloc", "kq_moe_grouped_gemm", "kq_moe_combine", "kq_workspace_bytes",
-    "kq_get_device_error", "block_bytes", "row_bytes",
+    "kq_get_device_error", "kq_test_hold_copies", "block_bytes", "row_bytes",
 ]
 
 _BLOCK_BYTES = {KQ_Q4_K: 144, KQ_Q5_K: 176, KQ_Q6_K: 210, KQ_TQ4_1S: 20}
@@ -201,3 +201,9 @@ def kq_get_device_error(stream=None) -> int:
     if st not in (0, 7):
         raise KQError(st, "kq_get_device_error")
     return int(code.value)
+
+
+def kq_test_hold_copies(hold: bool) -> None:
+    """Test hook: while set, the weight producers of the decode and tensor-core
+    kernels issue nothing, so their waits run out (KQ_DEVERR_WAIT_TIMEOUT)."""
+    check(lib().kq_test_hold_copies(1 if hold else 0), "kq_test_hold_copies")

@@ -52,6 +52,7 @@ SIGNATURES = {
                                            _vp, _sz, _vp]),
     "kq_workspace_bytes": (_sz, [ctypes.c_int, ctypes.c_int, _i64, _i64, _i64, _i32, _i32]),
     "kq_get_device_error": (ctypes.c_int, [ctypes.POINTER(_i32), _vp]),
+    "kq_test_hold_copies": (ctypes.c_int, [ctypes.c_int]),
     "kq_status_str": (ctypes.c_char_p, [ctypes.c_int]),
 }
 

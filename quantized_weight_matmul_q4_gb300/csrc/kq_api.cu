@@ -65,6 +65,12 @@ kq_status finish(cudaError_t e, int status) {
 
 cudaError_t device_context(int* dev, int* num_sms, int** err) { return device_state(dev, num_sms, err); }
 
+namespace {
+std::atomic<int> g_hold_copies{0};
+}  // namespace
+
+int test_hold_copies() { return g_hold_copies.load(std::memory_order_relaxed); }
+
 cudaError_t allow_max_smem(const void* kernel, int slot) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -229,6 +235,11 @@ kq_status kq_moe_grouped_gemm(int wtype, const void* W_experts, int32_t n_expert
   e = launch_moe(wtype, W_experts, n_experts, expert_ids, top_k, X, Y, M, K, T, ws, plan, err, sms,
                  reinterpret_cast<cudaStream_t>(stream), &status);
   return finish(e, status);
+}
+
+kq_status kq_test_hold_copies(int hold) {
+  g_hold_copies.store(hold ? 1 : 0, std::memory_order_relaxed);
+  return KQ_OK;
 }
 
 kq_status kq_get_device_error(int32_t* code, kq_stream_t stream) {

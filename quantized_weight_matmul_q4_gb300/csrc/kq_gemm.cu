@@ -103,6 +103,7 @@ struct GemmArgs {
   const int* entries;
   int* tile_queue;  // MoE: next tile index minus gridDim.x (zeroed by the routing kernel)
   int* err;
+  int hold;         // kq_test_hold_copies: the raw producer issues nothing and hands out no tile
 };
 
 struct Tile {
@@ -441,7 +442,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
     // ---- raw weight producer -------------------------------------------------
     // It also picks the CTA's tiles: the first is its CTA (pair) index, later
     // ones come from the MoE tile queue or, for the dense GEMM, a fixed stride.
-    if (lane == 0) {
+    if (lane == 0 && !a.hold) {
       int st = 0, qi = 0;
       uint32_t ph = 0, qph = 0;
       for (int t = tile0;;) {
@@ -1073,6 +1074,7 @@ cudaError_t launch_gemm(int wtype, const void* W, const float* X, float* Y, int6
   a.partial = partial;
   a.n_experts = 0;
   a.err = err;
+  a.hold = test_hold_copies();
   bool launched = false;
   if (plan.pair) {
     GemmArgs ap = a;
@@ -1185,6 +1187,7 @@ cudaError_t launch_moe(int wtype, const void* W, int n_experts, const int32_t* i
   a.entries = entries;
   a.tile_queue = tile_queue;
   a.err = err;
+  a.hold = test_hold_copies();
   size_t smem = 0;
   if (!choose_stages(wtype, MOE_BN, n_experts, false, &a, &smem)) {
     *status = KQ_ERR_SHAPE;

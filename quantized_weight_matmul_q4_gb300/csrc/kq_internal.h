@@ -77,6 +77,9 @@ cudaError_t launch_moe_combine(const float* Y, const float* probs, float* out, i
 // (looked up once per device).
 cudaError_t device_context(int* dev, int* num_sms, int** err);
 
+// The flag set by kq_test_hold_copies, read when a launch's parameters are made.
+int test_hold_copies();
+
 // Raises a kernel's dynamic shared-memory limit to the 227 KB maximum, once per
 // device (later calls only read a flag, so launches stay cheap and capturable).
 cudaError_t allow_max_smem(const void* kernel, int slot);

@@ -59,6 +59,7 @@ struct MatvecParams {
   const uint8_t* pf;    // the next call's weights, prefetched into L2 (or null)
   uint64_t pf_bytes;    // a multiple of 16
   int* err;
+  int hold;             // kq_test_hold_copies: the producer issues nothing
 };
 
 // Activation codes live in 16-byte pieces; piece j (0..15) of K-block b is
@@ -325,7 +326,7 @@ __global__ void __launch_bounds__(MV_THREADS, 1) matvec_kernel(const MatvecParam
 
   if (warp == MV_CWARPS) {
     // Producer: the CTA's contiguous byte range, chunk by chunk, through the ring.
-    if (lane == 0) {
+    if (lane == 0 && !p.hold) {
       const uint8_t* base = p.W + static_cast<int64_t>(r0) * p.rs;
       const int64_t total = static_cast<int64_t>(n_items) * p.bb;
       for (int c = 0; c < n_chunks; ++c) {
@@ -488,6 +489,7 @@ struct MatvecLaneRowParams {
   const uint8_t* pf;                      // the next call's weights, prefetched into L2 (or null)
   uint64_t pf_bytes;                      // a multiple of 16
   int* err;
+  int hold;                               // kq_test_hold_copies: the weight producer issues nothing
 };
 
 
@@ -524,7 +526,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, RING ? 2 : 1)
   __syncthreads();
 
   if (warp == NW) {
-    if (lane == 0) {
+    if (lane == 0 && !p.hold) {
       tma_prefetch_desc(&tmW);
       const uint32_t box = static_cast<uint32_t>(p.R * p.cb * BB);
       if (!RING) {
@@ -1054,6 +1056,7 @@ static cudaError_t launch_matvec_p(int wtype, const void* W, const float* x, con
       lp.pf = static_cast<const uint8_t*>(pf);
       lp.pf_bytes = pf_bytes;
       lp.err = err;
+      lp.hold = test_hold_copies();
       if (wtype == KQ_Q5_K) return launch_lanerow<KQ_Q5_K, PROD>(ring, tmW, lp, grid, smem, s);
       return launch_lanerow<KQ_Q4_K, PROD>(ring, tmW, lp, grid, smem, s);
     }
@@ -1079,6 +1082,7 @@ static cudaError_t launch_matvec_p(int wtype, const void* W, const float* x, con
   p.pf = static_cast<const uint8_t*>(pf);
   p.pf_bytes = pf_bytes;
   p.err = err;
+  p.hold = test_hold_copies();
   if (p.rows_per_group < 1) {
     *status = KQ_ERR_SHAPE;
     return cudaSuccess;
