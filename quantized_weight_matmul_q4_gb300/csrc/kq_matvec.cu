@@ -248,43 +248,51 @@ __device__ __forceinline__ float block_dot_q5k(const uint8_t* __restrict__ blk, 
   return d * acc - dmin * acc_m;
 }
 
-// Four bytes from a 2-byte aligned shared address, as one 32-bit word.
-__device__ __forceinline__ uint32_t ld_u32_a2(const uint8_t* p) {
-  const uint16_t* q = reinterpret_cast<const uint16_t*>(p);
-  return static_cast<uint32_t>(q[0]) | (static_cast<uint32_t>(q[1]) << 16);
-}
-
 // Sum over one Q6_K super-block of w * x_hat, w = d * sc * (q - 32), taken as
 // d * Sum_16 sc * d8 * (dot(q, x) - 32 * Sum x) per group of 16 weights.
+// A 210-byte block is only 2-byte aligned in shared memory: its 53 words are
+// read once as the 54 4-byte aligned words around it and each is rebuilt with
+// one funnel shift (by 0 or 16 bits). Block word k: ql[4k..] for k < 32, qh
+// for 32 <= k < 48, the int8 scales for 48..51, d in the low half of word 52.
+// (The words read past the block's end stay inside its ring slot and only
+// feed bits that are not used.)
 __device__ __forceinline__ float block_dot_q6k(const uint8_t* __restrict__ blk, int b, const uint8_t* __restrict__ xq,
                                                const int4* __restrict__ xds) {
-  const float d = __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short*>(blk + 208)));
+  const uint32_t* aw = reinterpret_cast<const uint32_t*>(reinterpret_cast<uintptr_t>(blk) & ~uintptr_t(3));
+  const uint32_t sh = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(blk) & 2) * 8;  // 0 or 16
+  uint32_t u[54];
+#pragma unroll
+  for (int k = 0; k < 54; ++k) u[k] = aw[k];
+  uint32_t w[53];
+#pragma unroll
+  for (int k = 0; k < 53; ++k) w[k] = __funnelshift_r(u[k], u[k + 1], sh);
+  const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(w[52] & 0xFFFFu)));
   float acc = 0.f;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
-      const uint8_t* ql = blk + 64 * h + 32 * (g & 1);
-      const uint8_t* qh = blk + 128 + 32 * h;
-      const int g8 = 4 * h + g;                    // 32-weight group inside the block
+      const int g8 = 4 * h + g;  // 32-weight group inside the block
       const int4 xa = *reinterpret_cast<const int4*>(xq + xq_piece(b, 2 * g8));
       const int4 xb = *reinterpret_cast<const int4*>(xq + xq_piece(b, 2 * g8 + 1));
       const int xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
       int dot0 = 0, dot1 = 0;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const uint32_t l = ld_u32_a2(ql + 4 * i);
-        const uint32_t hb = ld_u32_a2(qh + 4 * i);
-        const uint32_t lo = (g < 2) ? (l & 0x0F0F0F0Fu) : ((l >> 4) & 0x0F0F0F0Fu);
-        const uint32_t q = lo | (((hb >> (2 * g)) & 0x03030303u) << 4);
+        const uint32_t l = w[16 * h + 8 * (g & 1) + i];   // ql[64h + 32(g & 1) + 4i ..]
+        const uint32_t hq = w[32 + 8 * h + i];              // qh[32h + 4i ..]
+        const uint32_t lo = (g < 2) ? l : (l >> 4);
+        const uint32_t hi = (g < 2) ? (hq << (4 - 2 * g)) : (hq >> (2 * g - 4));
+        const uint32_t q = (lo & 0x0F0F0F0Fu) | (hi & 0x30303030u);  // the 6-bit codes of four weights
         if (i < 4)
           dot0 = dp4a_us(q, xv[i], dot0);
         else
           dot1 = dp4a_us(q, xv[i], dot1);
       }
       const int4 ds = xds[xds_q6k(b, g8)];
-      const int sc0 = static_cast<int>(reinterpret_cast<const int8_t*>(blk)[192 + 8 * h + 2 * g]);
-      const int sc1 = static_cast<int>(reinterpret_cast<const int8_t*>(blk)[192 + 8 * h + 2 * g + 1]);
+      const int si = 8 * h + 2 * g;  // scale index of the first 16 weights
+      const int sc0 = static_cast<int>(static_cast<int8_t>(w[48 + (si >> 2)] >> (8 * (si & 3))));
+      const int sc1 = static_cast<int>(static_cast<int8_t>(w[48 + (si >> 2)] >> (8 * (si & 3) + 8)));
       const int t = sc0 * (dot0 - 32 * ds.y) + sc1 * (dot1 - 32 * ds.z);
       acc = fmaf(__int_as_float(ds.x), i2f(t), acc);
     }
