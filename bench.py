@@ -49,7 +49,7 @@ def parse():
     p.add_argument("--no-sections", action="store_true", help="skip the prefill/MoE sections")
     p.add_argument("--section-iters", type=int, default=10)
     p.add_argument("--only", default=None,
-                   help="profiling aid: run only 'decode' or one section (prefill_*/moe_*) and print its numbers")
+                   help="profiling aid: run only 'decode' or one section (prefill_*/moe_*/decode_*/mma_rate) and print its numbers")
     p.add_argument("--eager", action="store_true", help="launch the decode step eagerly instead of as a CUDA graph")
     return p.parse_args()
 
@@ -201,16 +201,46 @@ def _oracle_decode_sample(rows: int, reps: int, min_seconds: float):
     return nbytes, time.perf_counter() - t0
 
 
-def oracle_decode_gbs(rows: int, reps: int, min_seconds: float):
+def oracle_decode_gbs(rows: int, reps: int, min_seconds: float, procs: int = 1):
+    """Oracle decode throughput (GB/s of weights) with `procs` single-threaded
+    oracle processes running the sample at once (fresh interpreters: no fork
+    after any CUDA use); returns (GB/s summed over the processes, wall seconds)."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
     code = ("import json, bench; b, s = bench._oracle_decode_sample(%d, %d, %f); "
             "print(json.dumps([b, s]))" % (rows, reps, min_seconds))
-    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError("oracle timing failed: " + r.stderr[-2000:])
-    b, s = json.loads(r.stdout.strip().splitlines()[-1])
-    return b / s / 1e9, s
+    t0 = time.perf_counter()
+    ps = [subprocess.Popen([sys.executable, "-c", code], cwd=ROOT, env=env, stdout=subprocess.PIPE,
+                           stderr=subprocess.PIPE, text=True) for _ in range(procs)]
+    total = 0.0
+    for pr in ps:
+        out, err = pr.communicate()
+        if pr.returncode != 0:
+            raise RuntimeError("oracle timing failed: " + err[-2000:])
+        b, _ = json.loads(out.strip().splitlines()[-1])
+        total += b
+    wall = time.perf_counter() - t0
+    return total / wall / 1e9, wall
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def oracle_baseline(rows: int, min_seconds: float) -> dict:
+    """The oracle as it stands on the host: all cores (one single-threaded
+    process per core) and one thread."""
+    cores = host_cores()
+    gbs_all, secs_all = oracle_decode_gbs(rows, 2, min_seconds, procs=cores)
+    gbs_one, secs_one = oracle_decode_gbs(rows, 2, min_seconds, procs=1)
+    return {"value": round(gbs_all, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"oracle matvec on the first {rows} rows of each decode shape, repeated for about "
+                      f"{min_seconds:.0f} s; {cores} single-threaded processes at once ({secs_all:.1f} s wall), "
+                      f"and one alone ({secs_one:.1f} s)",
+            "single_thread": {"value": round(gbs_one, 4), "unit": "GB/s", "cores": 1}}
 
 
 # ----------------------------------------------------------------------------
@@ -483,6 +513,43 @@ def _decode_sweep(kq, syn, torch, dev, stream, names, copies, reps, pk):
             "gbs": round(gbs, 1), "frac_hbm_peak": round(gbs / pk["hbm_gbs"], 4)}
 
 
+def _mma_rate(torch, pk):
+    """Issue rate of tcgen05 kind::f16 MMAs (M = 128, K = 16, fp32 accumulator)
+    on every SM, with A read from shared memory or from tensor memory, for
+    N = 64, 128, 256 (the measurement aid libkqprobe.so)."""
+    import ctypes
+    from quantized_weight_matmul_q4_gb300.build import PROBE_LIB_PATH
+    L = ctypes.CDLL(PROBE_LIB_PATH)
+    L.kqprobe_mma.restype = ctypes.c_int
+    L.kqprobe_mma.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
+                              ctypes.c_void_p]
+    nsm = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    cyc = torch.zeros(nsm, dtype=torch.int64, device="cuda")
+    s = torch.cuda.current_stream()
+    iters = 8192
+    out = {}
+    for kind, where in ((0, "a_smem"), (2, "a_tmem")):
+        for n in (64, 128, 256):
+            for _ in range(2):
+                rc = L.kqprobe_mma(kind, n, iters, ctypes.c_void_p(cyc.data_ptr()), nsm, ctypes.c_void_p(s.cuda_stream))
+                if rc != 0:
+                    raise RuntimeError(f"kqprobe_mma failed ({rc})")
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            L.kqprobe_mma(kind, n, iters, ctypes.c_void_p(cyc.data_ptr()), nsm, ctypes.c_void_p(s.cuda_stream))
+            b.record(s)
+            torch.cuda.synchronize()
+            ms = a.elapsed_time(b)
+            c = cyc.cpu().tolist()
+            if min(c) <= 0:
+                raise RuntimeError("kqprobe_mma: a wait gave up")
+            tf = 2.0 * 128 * n * 16 * iters * nsm / (ms / 1e3) / 1e12
+            out[f"{where}_n{n}"] = {"cycles_per_mma": round(statistics.median(c) / iters, 1),
+                                    "tflops": round(tf, 1), "frac_bf16_peak": round(tf / pk["bf16_tflops"], 4)}
+    return out
+
+
 def run_sections(args, kq, syn, torch, dev, stream, pk, only=None):
     # L2 flush between timed calls: write 256 MB (> L2), then read another
     # 256 MB, so L2 holds only clean lines when the call starts (the write-back
@@ -494,6 +561,10 @@ def run_sections(args, kq, syn, torch, dev, stream, pk, only=None):
         flush_w.zero_()
         flush_r.sum()
     res = {}
+    if only is None or only == "mma_rate":
+        res["mma_rate_f16_m128"] = _mma_rate(torch, pk)
+    if only == "mma_rate":
+        return res
     for name, (names, copies) in DECODE_SECTIONS.items():
         if only is None or only == name:
             res[name] = _decode_sweep(kq, syn, torch, dev, stream, names, copies, 20, pk)
@@ -552,19 +623,21 @@ def run_sections(args, kq, syn, torch, dev, stream, pk, only=None):
 
 # ----------------------------------------------------------------------------
 def run_reference(args):
-    """The CPU oracle, as it stands, on bounded samples of the decode workload."""
-    cores = 1
+    """The CPU oracle, as it stands, on bounded samples of the decode workload,
+    on every host core (one single-threaded oracle process per core)."""
+    cores = host_cores()
     rows = 256
     vals = []
     for _ in range(args.warmup):
-        oracle_decode_gbs(rows, 1, 0.0)
+        oracle_decode_gbs(rows, 1, 0.0, procs=cores)
     t_all = 0.0
     for _ in range(args.steps):
-        gbs, s = oracle_decode_gbs(rows, 1, 0.0)
+        gbs, s = oracle_decode_gbs(rows, 1, 0.0, procs=cores)
         vals.append(gbs)
         t_all += s
     v = statistics.mean(vals)
-    sample = f"oracle matvec on the first {rows} rows of each decode shape per step (single thread)"
+    sample = (f"oracle matvec on the first {rows} rows of each decode shape per step, "
+              f"{cores} single-threaded processes at once")
     return {
         "impl": "reference",
         "metric": METRIC,
@@ -600,10 +673,7 @@ def main():
         dist.close()
         return
     if dist.rank == 0 and not args.only:
-        gbs, secs = oracle_decode_gbs(512, 2, 10.0)
-        out["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                               "sample": f"oracle matvec on the first 512 rows of each decode shape, "
-                                         f"repeated for {secs:.1f} s (single thread)"}
+        out["cpu_baseline"] = oracle_baseline(512, 8.0)
         print(json.dumps(out), flush=True)
     dist.close()
 

@@ -19,6 +19,9 @@ LIB_PATH = os.path.join(OUT_DIR, "libkq.so")
 INCLUDE = os.path.join(ROOT, "include")
 
 SOURCES = ["kq_api.cu", "kq_quant.cu", "kq_matvec.cu", "kq_gemm.cu", "kq_gemm_noalloc.cu", "kq_combine.cu", "kq_tq4.cu"]
+# A measurement aid outside libkq (the tensor-core MMA issue rate), in a library of its own.
+PROBE_SOURCES = ["probe_mma.cu"]
+PROBE_LIB_PATH = os.path.join(OUT_DIR, "libkqprobe.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", f"-I{INCLUDE}"]
@@ -58,6 +61,12 @@ def build(verbose: bool = False, ptxas_info: bool = False) -> str:
     extra = ["-Xptxas", "-v"] if ptxas_info else []
     jobs = []
     objs = []
+    probe_objs = [os.path.join(OUT_DIR, s.replace(".cu", ".o")) for s in PROBE_SOURCES]
+    for s in PROBE_SOURCES:
+        src = os.path.join(CSRC, s)
+        obj = os.path.join(OUT_DIR, s.replace(".cu", ".o"))
+        if ptxas_info or _stale(obj, [src, *hdrs]):
+            jobs.append((src, obj))
     for s in SOURCES:
         src = os.path.join(CSRC, s)
         obj = os.path.join(OUT_DIR, s.replace(".cu", ".o"))
@@ -69,13 +78,14 @@ def build(verbose: bool = False, ptxas_info: bool = False) -> str:
             futs = [ex.submit(_compile, s, o, extra) for s, o in jobs]
             for f in futs:
                 f.result()
-    if jobs or _stale(LIB_PATH, objs):
-        tmp = LIB_PATH + ".tmp"
-        cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-Xcompiler", "-fPIC"]
-        r = subprocess.run(cmd, capture_output=True, text=True)
-        if r.returncode != 0:
-            raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB_PATH)
+    for path, parts in ((LIB_PATH, objs), (PROBE_LIB_PATH, probe_objs)):
+        if _stale(path, parts):
+            tmp = path + ".tmp"
+            cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *parts, "-Xcompiler", "-fPIC"]
+            r = subprocess.run(cmd, capture_output=True, text=True)
+            if r.returncode != 0:
+                raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+            os.replace(tmp, path)
     if verbose:
         print(f"libkq: {LIB_PATH} ({len(jobs)} unit(s) rebuilt)")
     return LIB_PATH
