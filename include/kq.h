@@ -49,6 +49,11 @@
  *    A status other than KQ_OK means nothing was queued, except KQ_ERR_CUDA
  *    after a failed launch.
  *  - Results are deterministic: the same inputs give bit-identical outputs.
+ *  - Per-device state: the library looks up, once per device, the device
+ *    addresses of its error word (and of kq_gemm_noalloc's scratch) and sets
+ *    its kernels' shared-memory limits. That state belongs to the device's
+ *    primary context: do not call the library after cudaDeviceReset in the
+ *    same process.
  *  - Accuracy: Q8_1 codes and block sums are bit-exact against the IEEE fp32
  *    definition. Y satisfies |Y - Y_ref| <= 1e-3 * Sum_k |w_k x_k| + 1e-5 per
  *    element, Y_ref being the exact product of the dequantised operands. The
@@ -208,7 +213,10 @@ KQ_API kq_status kq_gemm(int wtype, const void* W, const float* X, float* Y, int
  * (cudaMalloc may synchronise the device, which such a loop cannot afford).
  * The library itself allocates nothing here: the scratch (fp16 x_hat and
  * split-K partials) is a fixed array of KQ_GEMM_STATIC_WS_BYTES per device,
- * part of the library's device image, which no caller has to clear.
+ * part of the library's device image, which no caller has to clear. With
+ * CUDA's default lazy module loading the array takes device memory only once
+ * this entry point is first called on a device; with eager loading
+ * (CUDA_MODULE_LOADING=EAGER) every context that loads the library reserves it.
  *
  * Limit: returns KQ_ERR_WORKSPACE, with nothing queued, when the call would
  * need more scratch than KQ_GEMM_STATIC_WS_BYTES, i.e. when
@@ -271,6 +279,9 @@ KQ_API size_t kq_workspace_bytes(int op, int wtype, int64_t M, int64_t K, int64_
  * kq_get_device_error — waits for `stream`, then returns in *code the first
  * device error recorded on the current device since the previous call
  * (KQ_DEVERR_*), and clears it. Returns KQ_ERR_DEVICE when *code != 0.
+ * There is one error word per device, shared by every stream and every call
+ * on it (not one per workspace): with kernels in flight on other streams, a
+ * code may come from one of those, and only `stream` is waited for.
  */
 KQ_API kq_status kq_get_device_error(int32_t* code, kq_stream_t stream);
 

@@ -2,8 +2,10 @@
 // x_hat copy of X and the split-K partial sums) in a fixed device array of
 // this file instead of a caller-provided workspace. Contract: include/kq.h.
 //
-// The array lives in this translation unit's own module, so a process that
-// never calls kq_gemm_noalloc never loads it and never pays its device memory.
+// The array lives in this translation unit's own module. Under CUDA's default
+// lazy module loading, a process that never calls kq_gemm_noalloc never loads
+// the module and never pays its device memory; with eager loading
+// (CUDA_MODULE_LOADING=EAGER) every context that loads the library reserves it.
 #include <mutex>
 
 #include "kq_common.cuh"
