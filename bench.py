@@ -152,16 +152,17 @@ class ClockSampler:
 
 def traffic_for(kernel: str):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, if the
-    kernel source is unchanged since the capture (else None)."""
+    kernel source is unchanged since the capture (else None): (read + write,
+    read, write)."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(path):
-        return None
+        return None, None, None
     with open(path) as f:
         d = json.load(f)
     e = d.get(kernel)
-    if not e:
-        return None
-    return e["dram_bytes_per_launch"] if sources_digest(e["sources"]) == e["sources_sha256_16"] else None
+    if not e or sources_digest(e["sources"]) != e["sources_sha256_16"]:
+        return None, None, None
+    return e["dram_bytes_per_launch"], e.get("dram_read_bytes_per_launch"), e.get("dram_write_bytes_per_launch")
 
 
 def sources_digest(sources) -> str:
@@ -201,26 +202,38 @@ def _oracle_decode_sample(rows: int, reps: int, min_seconds: float):
     return nbytes, time.perf_counter() - t0
 
 
-def oracle_decode_gbs(rows: int, reps: int, min_seconds: float, procs: int = 1):
-    """Oracle decode throughput (GB/s of weights) with `procs` single-threaded
-    oracle processes running the sample at once (fresh interpreters: no fork
-    after any CUDA use); returns (GB/s summed over the processes, wall seconds)."""
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
-               CUDA_VISIBLE_DEVICES="")
-    code = ("import json, bench; b, s = bench._oracle_decode_sample(%d, %d, %f); "
-            "print(json.dumps([b, s]))" % (rows, reps, min_seconds))
-    t0 = time.perf_counter()
-    ps = [subprocess.Popen([sys.executable, "-c", code], cwd=ROOT, env=env, stdout=subprocess.PIPE,
-                           stderr=subprocess.PIPE, text=True) for _ in range(procs)]
-    total = 0.0
-    for pr in ps:
-        out, err = pr.communicate()
-        if pr.returncode != 0:
-            raise RuntimeError("oracle timing failed: " + err[-2000:])
-        b, _ = json.loads(out.strip().splitlines()[-1])
-        total += b
-    wall = time.perf_counter() - t0
-    return total / wall / 1e9, wall
+def _oracle_worker_init():
+    # one thread per worker process (set before numpy loads)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[k] = "1"
+    os.environ["CUDA_VISIBLE_DEVICES"] = ""
+
+
+def _oracle_worker(args):
+    rows, reps, min_seconds = args
+    return _oracle_decode_sample(rows, reps, min_seconds)
+
+
+class OraclePool:
+    """`procs` single-threaded oracle processes, started once with the spawn
+    method (never a fork of a process that has used CUDA)."""
+
+    def __init__(self, procs: int):
+        import multiprocessing as mp
+        self.procs = procs
+        self.pool = mp.get_context("spawn").Pool(procs, initializer=_oracle_worker_init)
+        self.pool.map(_oracle_worker, [(8, 1, 0.0)] * procs)  # imports and first calls
+
+    def gbs(self, rows: int, reps: int, min_seconds: float):
+        """Every process runs the sample at once: GB/s of weights summed over the
+        processes, over the longest process's timed loop; and that time."""
+        res = self.pool.map(_oracle_worker, [(rows, reps, min_seconds)] * self.procs)
+        secs = max(r[1] for r in res)
+        return sum(r[0] for r in res) / secs / 1e9, secs
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
 
 
 def host_cores() -> int:
@@ -234,12 +247,20 @@ def oracle_baseline(rows: int, min_seconds: float) -> dict:
     """The oracle as it stands on the host: all cores (one single-threaded
     process per core) and one thread."""
     cores = host_cores()
-    gbs_all, secs_all = oracle_decode_gbs(rows, 2, min_seconds, procs=cores)
-    gbs_one, secs_one = oracle_decode_gbs(rows, 2, min_seconds, procs=1)
+    pool = OraclePool(cores)
+    try:
+        gbs_all, secs_all = pool.gbs(rows, 2, min_seconds)
+    finally:
+        pool.close()
+    one = OraclePool(1)
+    try:
+        gbs_one, secs_one = one.gbs(rows, 2, min_seconds)
+    finally:
+        one.close()
     return {"value": round(gbs_all, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": f"oracle matvec on the first {rows} rows of each decode shape, repeated for about "
-                      f"{min_seconds:.0f} s; {cores} single-threaded processes at once ({secs_all:.1f} s wall), "
-                      f"and one alone ({secs_one:.1f} s)",
+                      f"{min_seconds:.0f} s in each of {cores} single-threaded processes at once "
+                      f"(longest loop {secs_all:.1f} s), and in one process alone ({secs_one:.1f} s)",
             "single_thread": {"value": round(gbs_one, 4), "unit": "GB/s", "cores": 1}}
 
 
@@ -366,6 +387,7 @@ def run_ours(args, dist):
     clk = clocks.stop()
 
     avg_launch_s = ms_step / 1e3 / calls_step
+    traffic, traffic_read, traffic_write = traffic_for("matvec_q4k_lanerow_kernel")
     achieved = statistics.mean(alg_bytes_launch) / avg_launch_s / 1e9
     value = dist.world * w_bytes_step / (ms_step / 1e3) / 1e9
     out = {
@@ -399,7 +421,11 @@ def run_ours(args, dist):
             "unit": "GB/s",
             "frac": round(achieved / pk["hbm_gbs"], 4),
             "peak_source": f"{pk_kind} (copy bandwidth)",
-            "traffic": traffic_for("matvec_q4k_lanerow_kernel"),
+            "traffic": traffic,
+            "traffic_read": traffic_read,
+            "traffic_write": traffic_write,
+            "traffic_note": "dram bytes per launch from profiles/ncu_traffic.json (steady state); the writes "
+                            "are L2 write-backs of other kernels' lines, the kernel itself writes only y",
             "algorithmic_bytes_per_launch": statistics.mean(alg_bytes_launch),
             "duration": "mean time per kq_matvec_prefetch launch over the timed region (launches PDL-chained in a CUDA graph)",
         },
@@ -628,13 +654,17 @@ def run_reference(args):
     cores = host_cores()
     rows = 256
     vals = []
-    for _ in range(args.warmup):
-        oracle_decode_gbs(rows, 1, 0.0, procs=cores)
-    t_all = 0.0
-    for _ in range(args.steps):
-        gbs, s = oracle_decode_gbs(rows, 1, 0.0, procs=cores)
-        vals.append(gbs)
-        t_all += s
+    pool = OraclePool(cores)
+    try:
+        for _ in range(args.warmup):
+            pool.gbs(rows, 1, 0.0)
+        t_all = 0.0
+        for _ in range(args.steps):
+            gbs, s = pool.gbs(rows, 1, 0.0)
+            vals.append(gbs)
+            t_all += s
+    finally:
+        pool.close()
     v = statistics.mean(vals)
     sample = (f"oracle matvec on the first {rows} rows of each decode shape per step, "
               f"{cores} single-threaded processes at once")
