@@ -576,6 +576,19 @@ def _mma_rate(torch, pk):
     return out
 
 
+def section_ncu():
+    """Per-section ncu figures (the capture each section's kernels were profiled
+    at), from profiles/ncu_sections.json, for entries whose sources still hash
+    to the captured ones."""
+    path = os.path.join(ROOT, "profiles", "ncu_sections.json")
+    if not os.path.exists(path):
+        return {}
+    with open(path) as f:
+        d = json.load(f)
+    ok = sources_digest(d["sources"]) == d["sources_sha256_16"]
+    return {k: dict(v, current=ok) for k, v in d["sections"].items()}
+
+
 def run_sections(args, kq, syn, torch, dev, stream, pk, only=None):
     # L2 flush between timed calls: write 256 MB (> L2), then read another
     # 256 MB, so L2 holds only clean lines when the call starts (the write-back
@@ -600,11 +613,12 @@ def run_sections(args, kq, syn, torch, dev, stream, pk, only=None):
     gemm_names = ["smalln_q4k_4096x11008_n4", "prefill_q4k_4096x4096_n64", "prefill_q4k_4096x4096_n512",
                   "prefill_q4k_14336x4096_n2048", "prefill_q6k_4096x14336_n2048",
                   "prefill_q5k_14336x4096_n2048"]
-    moe_name = "moe_q4k_128x768x2048_t1024_top8"
+    moe_names = ["moe_q4k_128x768x2048_t1024_top8", "moe_q6k_128x768x2048_t1024_top8"]
     if only is not None:
-        if only not in gemm_names + [moe_name] + list(DECODE_SECTIONS):
+        if only not in gemm_names + moe_names + list(DECODE_SECTIONS):
             raise SystemExit(f"unknown section {only!r}")
         gemm_names = [n for n in gemm_names if n == only]
+        moe_names = [n for n in moe_names if n == only]
     for name in gemm_names:
         wl = syn.make_workload(name)
         M, K, N = wl["M"], wl["K"], wl["N"]
@@ -623,27 +637,31 @@ def run_sections(args, kq, syn, torch, dev, stream, pk, only=None):
                      "alg_gbs": round(wbytes / (ms / 1e3) / 1e9, 1),
                      "frac_hbm_peak": round(wbytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"], 4)}
         del W, X, Y, ws
-    if only is not None and only != moe_name:
-        return res
-    wl = syn.make_workload(moe_name)
-    E, M, K, T, top_k = wl["n_experts"], wl["M"], wl["K"], wl["T"], wl["top_k"]
-    W = torch.from_numpy(wl["W"][0]).to(dev)
-    X = torch.from_numpy(wl["X"]).to(dev)
-    ids = torch.from_numpy(wl["ids"]).to(dev)
-    Y = torch.empty((T, top_k, M), dtype=torch.float32, device=dev)
-    ws = torch.empty(kq.kq_workspace_bytes(kq.KQ_OP_MOE, "q4_k", M, K, T, E, top_k), dtype=torch.uint8, device=dev)
-    fn = lambda: kq.kq_moe_grouped_gemm("q4_k", W, E, ids, X, M, K, Y=Y, ws=ws)  # noqa: E731
-    ms, ms_min, ms_eager = _timed_calls(fn, iters, 2, flush, torch, stream)
-    flops = 2.0 * M * K * T * top_k
-    nbytes = W.numel() + X.numel() * 4 + Y.numel() * 4 + ids.numel() * 4
-    tf = flops / (ms / 1e3) / 1e12
-    res["moe_q4k_128x768x2048_t1024_top8"] = {
-        "ms": round(ms, 4), "ms_min": round(ms_min, 4), "ms_eager": round(ms_eager, 4), "tflops": round(tf, 1),
-        "frac_bf16_peak": round(tf / pk["bf16_tflops"], 4),
-        "alg_gbs": round(nbytes / (ms / 1e3) / 1e9, 1),
-        "frac_hbm_peak": round(nbytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"], 4)}
+    for moe_name in moe_names:
+        wl = syn.make_workload(moe_name)
+        E, M, K, T, top_k = wl["n_experts"], wl["M"], wl["K"], wl["T"], wl["top_k"]
+        W = torch.from_numpy(wl["W"][0]).to(dev)
+        X = torch.from_numpy(wl["X"]).to(dev)
+        ids = torch.from_numpy(wl["ids"]).to(dev)
+        Y = torch.empty((T, top_k, M), dtype=torch.float32, device=dev)
+        ws = torch.empty(kq.kq_workspace_bytes(kq.KQ_OP_MOE, wl["wtype"], M, K, T, E, top_k), dtype=torch.uint8,
+                         device=dev)
+        fn = lambda: kq.kq_moe_grouped_gemm(wl["wtype"], W, E, ids, X, M, K, Y=Y, ws=ws)  # noqa: E731
+        ms, ms_min, ms_eager = _timed_calls(fn, iters, 2, flush, torch, stream)
+        flops = 2.0 * M * K * T * top_k
+        nbytes = W.numel() + X.numel() * 4 + Y.numel() * 4 + ids.numel() * 4
+        tf = flops / (ms / 1e3) / 1e12
+        res[moe_name] = {
+            "ms": round(ms, 4), "ms_min": round(ms_min, 4), "ms_eager": round(ms_eager, 4), "tflops": round(tf, 1),
+            "frac_bf16_peak": round(tf / pk["bf16_tflops"], 4),
+            "alg_gbs": round(nbytes / (ms / 1e3) / 1e9, 1),
+            "frac_hbm_peak": round(nbytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"], 4)}
+        del W, X, ids, Y, ws
     if kq.kq_get_device_error():
         raise RuntimeError("device error during the sections")
+    for name, fig in section_ncu().items():
+        if name in res:
+            res[name]["ncu"] = fig
     return res
 
 

@@ -165,6 +165,8 @@ WORKLOADS = {
     "prefill_q6k_4096x14336_n2048": dict(kind="gemm", wtype="q6_k", M=4096, K=14336, N=2048, seed=3),
     "moe_q4k_128x768x2048_t1024_top8": dict(kind="moe", wtype="q4_k", M=768, K=2048, T=1024,
                                            n_experts=128, top_k=8, seed=4),
+    "moe_q6k_128x768x2048_t1024_top8": dict(kind="moe", wtype="q6_k", M=768, K=2048, T=1024,
+                                           n_experts=128, top_k=8, seed=4),
 }
 
 

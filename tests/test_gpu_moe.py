@@ -20,12 +20,13 @@ def _run(wtype, W, ids, X, E, M, K):
     return Y.cpu().numpy()
 
 
-def test_workload_full_parity():
-    wl = syn.make_workload("moe_q4k_128x768x2048_t1024_top8")
-    E, M, K = wl["n_experts"], wl["M"], wl["K"]
-    Y = _run("q4_k", wl["W"][0], wl["ids"], wl["X"], E, M, K)
-    Yr, B = ora.moe("q4_k", wl["W"][0], wl["ids"], wl["X"], E, M, K)
-    assert_within_bound(Y, Yr, B, "moe workload")
+@pytest.mark.parametrize("name", ["moe_q4k_128x768x2048_t1024_top8", "moe_q6k_128x768x2048_t1024_top8"])
+def test_workload_full_parity(name):
+    wl = syn.make_workload(name)
+    E, M, K, wtype = wl["n_experts"], wl["M"], wl["K"], wl["wtype"]
+    Y = _run(wtype, wl["W"][0], wl["ids"], wl["X"], E, M, K)
+    Yr, B = ora.moe(wtype, wl["W"][0], wl["ids"], wl["X"], E, M, K)
+    assert_within_bound(Y, Yr, B, name)
     assert kq.kq_get_device_error() == kq.KQ_DEVERR_NONE
 
 
