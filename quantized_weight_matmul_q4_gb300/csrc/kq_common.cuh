@@ -211,6 +211,16 @@ __device__ __forceinline__ void prefetch_share_l2(const uint8_t* pf, uint64_t by
     bulk_prefetch_l2(pf + off, static_cast<uint32_t>(min(static_cast<uint64_t>(65536), end - off)));
 }
 
+// Slice `part` of `parts` equal slices of [pf, pf + bytes), itself shared over
+// the grid's CTAs as prefetch_share_l2 does: several threads of a CTA issue
+// their slices at once.
+__device__ __forceinline__ void prefetch_slice_l2(const uint8_t* pf, uint64_t bytes, int part, int parts) {
+  if (!pf || bytes == 0) return;
+  const uint64_t slice = (bytes / parts) & ~uint64_t(15);
+  const uint64_t off = static_cast<uint64_t>(part) * slice;
+  prefetch_share_l2(pf + off, part == parts - 1 ? bytes - off : slice);
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* tm) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
 }

@@ -65,9 +65,6 @@ __device__ __forceinline__ uint32_t pack_q4(const int (&q)[4]) {
          ((static_cast<uint32_t>(q[2]) & 0xFFu) << 16) | ((static_cast<uint32_t>(q[3]) & 0xFFu) << 24);
 }
 
-// round half to even, then clamp to [-128, 127]
-__device__ __forceinline__ int cvt_rni_sat_s8(float x) { return max(-128, min(127, __float2int_rn(x))); }
-
 // Quantises 8 consecutive values v[0..7] held by one lane; the four lanes of an
 // aligned lane quad hold one 32-element block (lane 4i + j: elements 8j..8j+7).
 // Same arithmetic as quantize_quad. All four lanes of the quad must call it.
@@ -85,17 +82,21 @@ __device__ __forceinline__ Q8Oct quantize_oct(const float (&v)[8]) {
   a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
   const float d = __fdiv_rn(a, 127.0f);
   const float di = q8_inv_scale(d);
+  // q = rint(p) with p = fl(x * di): adding 1.5 * 2^23 to p (|p| < 2^22) rounds it
+  // to the nearest integer, ties to even, into the low mantissa bits, whose low
+  // byte is then q as a two's-complement int8; four such bytes are gathered by
+  // byte permutes and summed by one dp4a. |p| never exceeds 127.0001 (amax * di
+  // with di = 1 / fl(amax / 127), also for subnormal d; di = 0 where 1 / d
+  // overflows), so the clamp to [-128, 127] of the definition never applies.
   Q8Oct r;
   int s = 0;
 #pragma unroll
   for (int w = 0; w < 2; ++w) {
-    const int q0 = cvt_rni_sat_s8(__fmul_rn(v[4 * w + 0], di));
-    const int q1 = cvt_rni_sat_s8(__fmul_rn(v[4 * w + 1], di));
-    const int q2 = cvt_rni_sat_s8(__fmul_rn(v[4 * w + 2], di));
-    const int q3 = cvt_rni_sat_s8(__fmul_rn(v[4 * w + 3], di));
-    s += q0 + q1 + q2 + q3;
-    r.q[w] = (static_cast<uint32_t>(q0) & 0xFFu) | ((static_cast<uint32_t>(q1) & 0xFFu) << 8) |
-             ((static_cast<uint32_t>(q2) & 0xFFu) << 16) | ((static_cast<uint32_t>(q3) & 0xFFu) << 24);
+    uint32_t u[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) u[k] = __float_as_uint(__fadd_rn(__fmul_rn(v[4 * w + k], di), 12582912.0f));
+    r.q[w] = __byte_perm(__byte_perm(u[0], u[1], 0x0040), __byte_perm(u[2], u[3], 0x0040), 0x5410);
+    s = __dp4a(static_cast<int>(r.q[w]), 0x01010101, s);
   }
   s += __shfl_xor_sync(0xffffffffu, s, 1);
   s += __shfl_xor_sync(0xffffffffu, s, 2);
