@@ -534,11 +534,25 @@ __global__ void __launch_bounds__((NW + 1) * 32, RING ? 2 : 1)
   __syncthreads();
 
   if (warp == NW) {
+    const uint32_t box = static_cast<uint32_t>(p.R * p.cb * BB);
+    if (!RING) {
+      // Staged form: chunk 0 at once, so that the first work items find their
+      // weights; the other chunks only when the dependency wait returns, beside
+      // the consumers' loads of x. Issued at the CTA's start, the whole range
+      // (~167 KB per SM) held up those loads behind the wait (6.1 against 5.5 us
+      // per decode launch); issued once x has landed, it came too late for the
+      // dots (6.1 us).
+      if (lane == 0 && !p.hold) {
+        tma_prefetch_desc(&tmW);
+        mbar_expect_tx(&full[0], box);
+        tma_load_2d(smem, &tmW, &full[0], 0, r0);
+      }
+      __syncwarp();
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+    }
     if (lane == 0 && !p.hold) {
-      tma_prefetch_desc(&tmW);
-      const uint32_t box = static_cast<uint32_t>(p.R * p.cb * BB);
       if (!RING) {
-        for (int c = 0; c < p.n_chunks; ++c) {
+        for (int c = 1; c < p.n_chunks; ++c) {
           mbar_expect_tx(&full[c], box);
           tma_load_2d(smem + static_cast<size_t>(c) * p.chunk_bytes, &tmW, &full[c], c * p.cb * (BB / 4), r0);
         }
@@ -546,6 +560,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, RING ? 2 : 1)
         for (int c = 0; c < p.n_chunks; ++c)
           if (!mbar_wait_bounded(&full[c], 0)) report_error(p.err, ERR_WAIT_TIMEOUT);
       } else {
+        tma_prefetch_desc(&tmW);
         int issued = 0;
         for (int c = 0; c < p.n_chunks; ++c) {
           const int sl = c % p.S;
