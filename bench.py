@@ -578,15 +578,14 @@ def _mma_rate(torch, pk):
 
 def section_ncu():
     """Per-section ncu figures (the capture each section's kernels were profiled
-    at), from profiles/ncu_sections.json, for entries whose sources still hash
-    to the captured ones."""
+    at), from profiles/ncu_sections.json; `current` says whether the section's
+    listed sources still hash to the captured ones."""
     path = os.path.join(ROOT, "profiles", "ncu_sections.json")
     if not os.path.exists(path):
         return {}
     with open(path) as f:
         d = json.load(f)
-    ok = sources_digest(d["sources"]) == d["sources_sha256_16"]
-    return {k: dict(v, current=ok) for k, v in d["sections"].items()}
+    return {k: dict(v, current=sources_digest(v["sources"]) == v["sources_sha256_16"]) for k, v in d["sections"].items()}
 
 
 def run_sections(args, kq, syn, torch, dev, stream, pk, only=None):
