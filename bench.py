@@ -489,7 +489,7 @@ DECODE_SECTIONS = {
 
 
 def _decode_sweep(kq, syn, torch, dev, stream, names, copies, reps, pk):
-    """One kq_matvec per weight copy and shape, captured as a CUDA graph and
+    """One decode call per weight copy and shape, captured as a CUDA graph and
     replayed `reps` times back to back (weights larger than L2, so no flush).
     Returns the section's numbers: algorithmic GB/s = (weights + x + y bytes)
     / device time."""
@@ -501,10 +501,18 @@ def _decode_sweep(kq, syn, torch, dev, stream, names, copies, reps, pk):
         y = torch.empty(wl["M"], dtype=torch.float32, device=dev)
         sets.append((wl["wtype"], wl["M"], wl["K"], Ws, x, y))
 
-    def step():  # plain calls: the next-weights prefetch measured no gain for these kernels (TQ4_1S: slower)
-        for c in range(copies):
-            for (wt, M, K, Ws, x, y) in sets:
+    # The step's calls in order; as in the headline decode step each call names
+    # the next call's weights for an L2 prefetch (kq_matvec_prefetch), except
+    # for TQ4_1S, whose ring refills were slower beside the prefetch.
+    order = [(c, st) for c in range(copies) for st in sets]
+
+    def step():
+        for i, (c, (wt, M, K, Ws, x, y)) in enumerate(order):
+            if wt == "tq4_1s":
                 kq.kq_matvec(wt, Ws[c], x, M, K, y=y)
+            else:
+                c2, st2 = order[(i + 1) % len(order)]
+                kq.kq_matvec_prefetch(wt, Ws[c], x, M, K, W_next=st2[3][c2], y=y)
 
     for _ in range(3):
         step()

@@ -150,9 +150,9 @@ KQ_API kq_status kq_matvec(int wtype, const void* W, const float* x, float* y, i
  * fetch its share of W_next[0, W_next_bytes) (rounded down to a multiple of 16):
  * the weights of the call that follows on the stream, e.g. the next layer's
  * matrix in a decode step. That call's weight stream then starts from L2 while
- * this one computes (the staged lane-row forms ask for it once their
- * activations are in, so that it does not delay them; ring forms once their
- * ring is primed). y is bit-identical to
+ * this one computes (the staged lane-row forms and the item kernel of Q6_K
+ * ask for it once their activations are in, so that it does not delay them;
+ * the lane-row ring form once its ring is primed). y is bit-identical to
  * kq_matvec's; the prefetch is a hint (nothing waits for it). An addition of
  * this library (the pages launch one matrix per call without it). Every decode
  * kernel form takes it except the TQ4_1S fallback for K % 128 != 0.
