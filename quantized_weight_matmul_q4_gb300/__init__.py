@@ -25,9 +25,13 @@ _BLOCK_BYTES = {KQ_Q4_K: 144, KQ_Q5_K: 176, KQ_Q6_K: 210, KQ_TQ4_1S: 20}
 _BLOCK_WEIGHTS = {KQ_Q4_K: 256, KQ_Q5_K: 256, KQ_Q6_K: 256, KQ_TQ4_1S: 32}
 
 
+_WTYPES = {"q4_k": KQ_Q4_K, "q5_k": KQ_Q5_K, "q6_k": KQ_Q6_K, "tq4_1s": KQ_TQ4_1S}
+
+
 def _wt(wtype) -> int:
     if isinstance(wtype, str):
-        return {"q4_k": KQ_Q4_K, "q5_k": KQ_Q5_K, "q6_k": KQ_Q6_K, "tq4_1s": KQ_TQ4_1S}[wtype.lower()]
+        w = _WTYPES.get(wtype)
+        return w if w is not None else _WTYPES[wtype.lower()]
     return int(wtype)
 
 
@@ -40,18 +44,28 @@ def row_bytes(wtype, K: int) -> int:
 
 
 _TORCH = None
+_TENSOR = None        # torch.Tensor
+_RAW_STREAM = None    # the current stream's handle of a device, without a Stream object (or False)
+_GET_DEVICE = None    # the current device index
 
 
 def _torch():
-    global _TORCH
+    global _TORCH, _TENSOR, _RAW_STREAM, _GET_DEVICE
     if _TORCH is None:
         import torch
+        _TENSOR = torch.Tensor
+        _RAW_STREAM = getattr(torch._C, "_cuda_getCurrentRawStream", None) or False
+        _GET_DEVICE = getattr(torch._C, "_cuda_getDevice", None) or torch.cuda.current_device
         _TORCH = torch
     return _TORCH
 
 
 def _dev(t, name: str, dtype=None):
     """Device pointer (an int) of a contiguous CUDA tensor of the given dtype."""
+    # The checks of a decode loop's every call, with as few attribute reads as
+    # possible; anything unusual takes the path below for its error.
+    if type(t) is _TENSOR and t.is_cuda and (dtype is None or t.dtype is dtype) and t.is_contiguous():
+        return t.data_ptr()
     torch = _torch()
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor (libkq has no CPU path)")
@@ -67,9 +81,8 @@ def _stream(stream):
     else the current stream of the current device."""
     torch = _torch()
     if stream is None:
-        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)  # the handle, without a Stream object
-        if raw is not None:
-            return raw(torch.cuda.current_device())
+        if _RAW_STREAM:
+            return _RAW_STREAM(_GET_DEVICE())
         stream = torch.cuda.current_stream()
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
