@@ -12,6 +12,10 @@
 // clock64 cycles from the first issue to the commit of the last. Kinds:
 //   0: A fp16 in shared memory (128-byte swizzle, K-major)
 //   2: A fp16 in tensor memory (as the library's GEMM issues them)
+//   3: as 2, with a commit to a second mbarrier after every 4 MMAs (as the
+//      GEMM frees one K step's stage), nothing waiting on it
+//   4: as 3, and the issuing thread waits for each of those commits before
+//      issuing the next 4 MMAs (the round trip of one K step)
 // Built into its own library (libkqprobe.so) by the package's build step.
 #include "kq_common.cuh"
 
@@ -34,11 +38,13 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int kind, int n, int i
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + A_BYTES + B_BYTES);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
   volatile int* abort = reinterpret_cast<volatile int*>(bar + 2);
+  uint64_t* bar2 = bar + 3;
   const int warp = threadIdx.x >> 5;
   for (int i = threadIdx.x; i < (A_BYTES + B_BYTES) / 16; i += blockDim.x)
     reinterpret_cast<uint4*>(smem)[i] = make_uint4(0u, 0u, 0u, 0u);
   if (threadIdx.x == 0) {
     mbar_init(bar, 1);
+    mbar_init(bar2, 1);
     *abort = 0;
     fence_mbar_init();
   }
@@ -52,7 +58,7 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int kind, int n, int i
   tc_fence_after();
   const uint32_t tmem = *tslot;
   if (warp == 0) {
-    if (kind == 2) {  // A operand in tensor memory: columns 256.. (zeros)
+    if (kind >= 2) {  // A operand in tensor memory: columns 256.. (zeros)
       uint32_t z[8] = {0, 0, 0, 0, 0, 0, 0, 0};
       tmem_st_32x32b_x8(tmem + 256, z);
       tmem_st_wait();
@@ -64,7 +70,20 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int kind, int n, int i
     const uint64_t adesc = smem_desc_sw128(smem_u32(sA));
     const uint64_t bdesc = smem_desc_sw128(smem_u32(sB));
     unsigned long long t0 = 0;
-    if (elect_one()) {
+    bool ok2 = true;
+    if (kind == 4) {
+      // the whole warp waits (bounded), one elected lane issues
+      t0 = clock64();
+      for (int i = 0; i < iters && ok2; i += 4) {
+        if (elect_one()) {
+          for (int k = 0; k < 4; ++k) umma_f16_ta(tmem, tmem + 256, bdesc + 2 * k, idesc, (i + k) > 0 ? 1u : 0u);
+          umma_commit(bar2);
+        }
+        __syncwarp();
+        ok2 = __all_sync(0xffffffffu, mbar_wait(bar2, (i >> 2) & 1, abort, nullptr));
+      }
+      if (elect_one()) umma_commit(bar);
+    } else if (elect_one()) {
       t0 = clock64();
       for (int i = 0; i < iters; ++i) {
         const int k = i & 3;  // the four 32-byte K slices of the 128-byte rows
@@ -72,12 +91,13 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int kind, int n, int i
           umma_f16(tmem, adesc + 2 * k, bdesc + 2 * k, idesc, i > 0 ? 1u : 0u);
         else
           umma_f16_ta(tmem, tmem + 256, bdesc + 2 * k, idesc, i > 0 ? 1u : 0u);
+        if (kind == 3 && k == 3) umma_commit(bar2);
       }
       umma_commit(bar);
     }
     __syncwarp();
     const bool ok = mbar_wait(bar, 0, abort, nullptr);
-    if (elect_one()) cycles[blockIdx.x] = ok ? clock64() - t0 : 0ull;
+    if (elect_one()) cycles[blockIdx.x] = (ok && ok2) ? clock64() - t0 : 0ull;
     __syncwarp();
   }
   tc_fence_before();
@@ -93,7 +113,7 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int kind, int n, int i
 extern "C" __attribute__((visibility("default"))) int kqprobe_mma(int kind, int n, int iters,
                                                                    unsigned long long* cycles, int grid,
                                                                    void* stream) {
-  if ((kind != 0 && kind != 2) || n < 16 || n > 256 || n % 16 != 0 || iters < 1 || grid < 1 || !cycles) return -1;
+  if ((kind != 0 && kind != 2 && kind != 3 && kind != 4) || n < 16 || n > 256 || n % 16 != 0 || iters < 1 || grid < 1 || !cycles) return -1;
   cudaError_t e = cudaFuncSetAttribute(mma_rate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return static_cast<int>(e);
   mma_rate_kernel<<<grid, 128, SMEM_BYTES, static_cast<cudaStream_t>(stream)>>>(kind, n, iters, cycles);
