@@ -19,7 +19,7 @@ pytestmark = pytest.mark.gpu
 D = 4096  # every matrix is D x D, so each output feeds the next call
 
 STAGES = [("q4_k", "plain"), ("q5_k", "prefetch"), ("tq4_1s", "plain"), ("q6_k", "plain"),
-          ("q4_k", "rmsnorm"), ("q4_k", "prefetch")]
+          ("q4_k", "rmsnorm"), ("q6_k", "prefetch"), ("q4_k", "prefetch")]
 
 
 # Where each format keeps its fp16 scales (byte offsets in a block, block size),
