@@ -35,6 +35,11 @@ constexpr int MV_SMEM_LIMIT = 227 * 1024;
 constexpr int MV_PART_MAX = 4096;                   // block partials per row group
 constexpr int MV_CHUNK_BLOCKS_Q4K = 112;            // 16128 B per chunk
 constexpr int MV_CHUNK_BLOCKS_Q6K = 80;             // 16800 B per chunk
+// Q6_K rows with K < 8192 take 25200-byte chunks, fewer and larger copies
+// (measured: decode 11008 x 4096 went from 11.0 to 9.8 us per launch with them;
+// 4096 x 11008 went from 11.6 to 11.8 us, so longer rows keep 80 blocks).
+constexpr int MV_CHUNK_BLOCKS_Q6K_SHORT_K = 120;
+constexpr int MV_Q6K_LONG_K = 8192;
 constexpr int MV_CHUNK_BLOCKS_Q5K = 92;             // 16192 B per chunk
 constexpr int MV_MAX_RING = 14;
 
@@ -47,8 +52,7 @@ struct MatvecParams {
   int M, K, nb;
   int bb;               // bytes per block (144 or 210)
   int rs;               // bytes per weight row
-  int unit_rows;        // CTA row ranges start at multiples of this (16-byte aligned copies)
-  int n_units;          // ceil(M / unit_rows)
+  int64_t w_bytes;      // M * rs: copies never read past this
   int chunk_blocks;     // blocks per ring chunk
   int chunk_bytes;      // chunk_blocks * bb (a multiple of 16)
   int slot_bytes;       // ring slot stride (multiple of 128)
@@ -313,12 +317,16 @@ __global__ void __launch_bounds__(MV_THREADS, 1) matvec_kernel(const MatvecParam
   volatile int* issued = abort + 1;  // chunks the producer has issued
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t u0 = static_cast<int64_t>(blockIdx.x) * p.n_units / gridDim.x;
-  const int64_t u1 = static_cast<int64_t>(blockIdx.x + 1) * p.n_units / gridDim.x;
-  const int r0 = static_cast<int>(u0 * p.unit_rows);
-  const int r1 = static_cast<int>(min(static_cast<int64_t>(p.M), u1 * p.unit_rows));
+  const int r0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * p.M / gridDim.x);
+  const int r1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * p.M / gridDim.x);
   const int n_items = (r1 - r0) * p.nb;                 // (row, block) pairs of this CTA
   const int n_chunks = (n_items + p.chunk_blocks - 1) / p.chunk_blocks;
+  // Rows of an odd number of 210-byte Q6_K block pairs are not 16-byte
+  // multiples, so a CTA's first row need not start on a 16-byte boundary: its
+  // copies then start `lead` bytes early, at the aligned address below, and
+  // every item of a slot sits `lead` bytes in.
+  const int64_t start = static_cast<int64_t>(r0) * p.rs;
+  const int lead = static_cast<int>(start & 15);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < p.n_ring; ++i) {
@@ -338,16 +346,22 @@ __global__ void __launch_bounds__(MV_THREADS, 1) matvec_kernel(const MatvecParam
   if (warp == MV_CWARPS) {
     // Producer: the CTA's contiguous byte range, chunk by chunk, through the ring.
     if (lane == 0 && !p.hold) {
-      const uint8_t* base = p.W + static_cast<int64_t>(r0) * p.rs;
+      const uint8_t* base = p.W + (start - lead);         // 16-byte aligned
       const int64_t total = static_cast<int64_t>(n_items) * p.bb;
       for (int c = 0; c < n_chunks; ++c) {
         const int slot = c % p.n_ring;
         if (c >= p.n_ring && !mbar_wait(&empty[slot], ((c / p.n_ring) & 1) ^ 1, abort, p.err)) break;
-        const int64_t off = static_cast<int64_t>(c) * p.chunk_bytes;
-        const uint32_t bytes = static_cast<uint32_t>(min(static_cast<int64_t>(p.chunk_bytes), total - off));
-        const uint32_t main_bytes = bytes & ~15u;
+        const int64_t off = static_cast<int64_t>(c) * p.chunk_bytes;  // a multiple of 16
+        // The chunk's items end `bytes` past base + off. The copy rounds that up
+        // to 16 bytes unless it would pass the end of W; then this thread copies
+        // the ragged tail (< 16 B) itself.
+        const uint32_t bytes =
+            static_cast<uint32_t>(lead + min(static_cast<int64_t>(p.chunk_bytes), total - off));
+        const int64_t room = p.w_bytes - (start - lead) - off;
+        uint32_t main_bytes = (bytes + 15u) & ~15u;
+        if (main_bytes > room) main_bytes = bytes & ~15u;
         uint8_t* dst = ring + static_cast<size_t>(slot) * p.slot_bytes;
-        for (uint32_t i = main_bytes; i < bytes; ++i) dst[i] = base[off + i];  // ragged end of W (< 16 B)
+        for (uint32_t i = main_bytes; i < bytes; ++i) dst[i] = base[off + i];
         mbar_expect_tx(&full[slot], main_bytes);
         if (main_bytes) bulk_g2s(dst, base + off, main_bytes, &full[slot]);
         *issued = c + 1;
@@ -418,7 +432,7 @@ __global__ void __launch_bounds__(MV_THREADS, 1) matvec_kernel(const MatvecParam
         ok = false;
         break;
       }
-      const uint8_t* blk = ring + static_cast<size_t>(slot) * p.slot_bytes +
+      const uint8_t* blk = ring + static_cast<size_t>(slot) * p.slot_bytes + lead +
                            static_cast<size_t>(it - c * p.chunk_blocks) * p.bb;
       const int b = it % p.nb;
       part[it - g0] = (WT == KQ_Q4_K)   ? block_dot_q4k(blk, b, xq, xds)
@@ -428,12 +442,21 @@ __global__ void __launch_bounds__(MV_THREADS, 1) matvec_kernel(const MatvecParam
     }
     (void)ok;
     asm volatile("bar.sync 1, %0;" ::"r"(MV_CTHREADS) : "memory");
+    // Row sums: S lanes per row (the largest power of two up to 32 that keeps
+    // every row of the group in one pass), each adding every S-th partial, then
+    // a butterfly over the S lanes. The order is fixed: deterministic.
     const int rows = (g1 - g0) / p.nb;
-    for (int r = threadIdx.x; r < rows; r += MV_CTHREADS) {
-      const float* pr = part + r * p.nb;
+    int S = 32;
+    while (S > 1 && rows * S > MV_CTHREADS) S >>= 1;
+    for (int t0 = 0; t0 < rows * S; t0 += MV_CTHREADS) {
+      const int t = t0 + threadIdx.x, r = t / S, j = t % S;
       float acc = 0.f;
-      for (int i = 0; i < p.nb; ++i) acc += pr[i];
-      p.y[r0 + g0 / p.nb + r] = acc;
+      if (r < rows) {
+        const float* pr = part + r * p.nb;
+        for (int i = j; i < p.nb; i += S) acc += pr[i];
+      }
+      for (int o = S >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (r < rows && j == 0) p.y[r0 + g0 / p.nb + r] = acc;
     }
     asm volatile("bar.sync 1, %0;" ::"r"(MV_CTHREADS) : "memory");
   }
@@ -1104,10 +1127,14 @@ static cudaError_t launch_matvec_p(int wtype, const void* W, const float* x, con
   p.nb = static_cast<int>(K / QK_K);
   p.bb = wtype == KQ_Q4_K ? Q4K_BYTES : wtype == KQ_Q5_K ? Q5K_BYTES : Q6K_BYTES;
   p.rs = p.nb * p.bb;
-  p.unit_rows = (p.rs % 16 == 0) ? 1 : 8;  // 8 rows of 210-byte blocks span a multiple of 16 bytes
-  p.chunk_blocks = wtype == KQ_Q4_K ? MV_CHUNK_BLOCKS_Q4K : wtype == KQ_Q5_K ? MV_CHUNK_BLOCKS_Q5K : MV_CHUNK_BLOCKS_Q6K;
+  p.w_bytes = static_cast<int64_t>(M) * p.rs;
+  p.chunk_blocks = wtype == KQ_Q4_K   ? MV_CHUNK_BLOCKS_Q4K
+                   : wtype == KQ_Q5_K ? MV_CHUNK_BLOCKS_Q5K
+                   : K < MV_Q6K_LONG_K ? MV_CHUNK_BLOCKS_Q6K_SHORT_K
+                                       : MV_CHUNK_BLOCKS_Q6K;
   p.chunk_bytes = p.chunk_blocks * p.bb;
-  p.slot_bytes = round_up(p.chunk_bytes, 128);
+  // room for a copy that starts up to 15 bytes before a CTA's first row
+  p.slot_bytes = round_up(p.chunk_bytes + (p.rs % 16 ? 16 : 0), 128);
   p.rows_per_group = MV_PART_MAX / p.nb;
   p.xq_bytes = round_up(p.K, 128);
   p.xds_bytes = round_up((p.K / QK_K) * 8 * 16, 128);
@@ -1126,10 +1153,9 @@ static cudaError_t launch_matvec_p(int wtype, const void* W, const float* x, con
     *status = KQ_ERR_SHAPE;
     return cudaSuccess;
   }
-  p.n_units = static_cast<int>((M + p.unit_rows - 1) / p.unit_rows);
-  const int G = p.n_units < num_sms ? p.n_units : num_sms;
+  const int G = M < num_sms ? static_cast<int>(M) : num_sms;
   // a ring deeper than the largest CTA range buys nothing
-  const int64_t max_rows = (static_cast<int64_t>(p.n_units + G - 1) / G) * p.unit_rows;
+  const int64_t max_rows = (M + G - 1) / G;
   const int64_t need = (max_rows * p.nb + p.chunk_blocks - 1) / p.chunk_blocks;
   if (n_ring > need) n_ring = static_cast<int>(need < 1 ? 1 : need);
   p.n_ring = n_ring;

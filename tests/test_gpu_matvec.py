@@ -32,7 +32,7 @@ def test_workload_full_parity(name):
 @pytest.mark.parametrize("M,K", [(1, 256), (17, 512), (37, 11008), (300, 4096), (1000, 2304), (33, 65536)])
 def test_ragged_shapes(wtype, M, K):
     if wtype == "q6_k" and K == 65536:
-        K = 14336                                    # Q6_K rows of 16-byte multiples, 8 rows per stage
+        K = 14336                                    # Q6_K rows of 16-byte multiples
     rng = np.random.default_rng(M * 7 + K)
     W = syn.weights(wtype, rng, M, K)
     x = syn.activations(rng, K, 1)
@@ -43,7 +43,9 @@ def test_ragged_shapes(wtype, M, K):
 
 def test_q6k_ragged_tail_bytes():
     # 43 Q6_K blocks per row = 9030 bytes: rows are not 16-byte multiples, so
-    # ranges start at 8-row boundaries and the last copy ends in a <16-byte tail.
+    # each CTA's copies start up to 14 bytes before its first row (one row per
+    # CTA here: every even offset occurs) and the last copy ends in a <16-byte
+    # tail copied by the producer thread.
     M, K = 45, 11008
     rng = np.random.default_rng(5)
     W = syn.q6_k_weights(rng, M, K)
@@ -95,7 +97,9 @@ def test_ring_staging_shapes_sampled_rows(M, K):
 
 @pytest.mark.parametrize("wtype,M,K", [
     ("q4_k", 256, 102400),    # item kernel, 3 ring slots for up to 8 chunks per CTA
-    ("q6_k", 304, 102400),    # item kernel, 3 slots, 8-row units
+    ("q6_k", 304, 102400),    # item kernel, 3 slots
+    ("q6_k", 304, 102144),    # item kernel, 3 slots; rows of 399 blocks (83790 B), so CTA
+                              # ranges start off 16-byte boundaries
     ("q4_k", 4560, 49152),    # lane-row ring form with 2 slots of 5-block chunks
 ])
 def test_shallow_rings_sampled_rows(wtype, M, K):
