@@ -321,10 +321,10 @@ __global__ void __launch_bounds__(MV_THREADS, 1) matvec_kernel(const MatvecParam
   const int r1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * p.M / gridDim.x);
   const int n_items = (r1 - r0) * p.nb;                 // (row, block) pairs of this CTA
   const int n_chunks = (n_items + p.chunk_blocks - 1) / p.chunk_blocks;
-  // Rows of an odd number of 210-byte Q6_K block pairs are not 16-byte
-  // multiples, so a CTA's first row need not start on a 16-byte boundary: its
-  // copies then start `lead` bytes early, at the aligned address below, and
-  // every item of a slot sits `lead` bytes in.
+  // Q6_K rows are 16-byte multiples only when K / 256 is a multiple of 8, so
+  // a CTA's first row need not start on a 16-byte boundary: its copies then
+  // start `lead` bytes early, at the aligned address below, and every item of
+  // a slot sits `lead` bytes in.
   const int64_t start = static_cast<int64_t>(r0) * p.rs;
   const int lead = static_cast<int>(start & 15);
 
